@@ -1,0 +1,208 @@
+"""CPU oracle for the QuantSpec hierarchical quantized KV cache hot path.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this package; the product path
+(the CUDA library and its binding) never does.
+
+The arithmetic lives in ``qs_oracle.c`` (plain C, fp64 attention, exact fp32
+quantization under convention QS-RN-v1); this module is argument marshalling
+over ctypes plus numpy storage for the logical cache state:
+
+* key/value codes as full 8-bit values [B, H, cap, G tokens, D channels]
+  (upper level = code >> 4, lower level = code & 15);
+* key scale/zero per channel [B, H, cap, D], value scale/zero per token
+  [B, H, cap, G], all fp16;
+* the fp16 double buffer [B, H, 2G, D] and per-sequence counters [B, 8]
+  (n_groups, fill, pending, half_base, err, 3 reserved).
+
+Parity pins: see the ``-m "not gpu"`` tests (nibble repack, dequantization
+bounds, closed-form groups, history independence, empty-cache attention,
+draft == verify when every lower level is 8, causal mask via rollback).
+"""
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+N_GROUPS, FILL, PENDING, HALF_BASE, ERR = 0, 1, 2, 3, 4
+STATE_WORDS = 8
+DEV_OVERFLOW, DEV_OVER_ROLLBACK, DEV_FLUSH_UNCOMMITTED, DEV_CAPACITY, DEV_NQ_GT_FILL = 1, 2, 4, 8, 16
+
+_lib = None
+
+
+class _Cache(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int), ("H", ctypes.c_int), ("D", ctypes.c_int),
+                ("G", ctypes.c_int), ("cap", ctypes.c_int),
+                ("kq", ctypes.c_void_p), ("vq", ctypes.c_void_p),
+                ("ks", ctypes.c_void_p), ("kz", ctypes.c_void_p),
+                ("vs", ctypes.c_void_p), ("vz", ctypes.c_void_p),
+                ("bk", ctypes.c_void_p), ("bv", ctypes.c_void_p),
+                ("state", ctypes.c_void_p)]
+
+
+def lib():
+    """Load (building first if needed) the oracle shared library."""
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        L = ctypes.CDLL(path)
+        P, I, D_, L_ = ctypes.c_void_p, ctypes.c_int, ctypes.c_double, ctypes.c_long
+        L.qso_half_to_double.restype = D_
+        L.qso_half_to_double.argtypes = [ctypes.c_uint16]
+        L.qso_float_to_half_rn.restype = ctypes.c_uint16
+        L.qso_float_to_half_rn.argtypes = [ctypes.c_float]
+        L.qso_float_to_half_ru.restype = ctypes.c_uint16
+        L.qso_float_to_half_ru.argtypes = [ctypes.c_float]
+        L.qso_quantize_group.restype = None
+        L.qso_quantize_group.argtypes = [P, L_, I, P, P, P, L_]
+        L.qso_dequant.restype = D_
+        L.qso_dequant.argtypes = [ctypes.c_uint8, ctypes.c_uint16, ctypes.c_uint16, I]
+        L.qso_split_code.restype = None
+        L.qso_split_code.argtypes = [ctypes.c_uint8, P, P]
+        for name, args in (("qso_append", [P, P, P, I]), ("qso_rollback", [P, P]),
+                           ("qso_need_flush", [P, I, P]), ("qso_flush", [P, P]),
+                           ("qso_attn", [P, I, P, I, D_, P, P])):
+            f = getattr(L, name)
+            f.restype = None
+            f.argtypes = args
+        L.qso_num_threads.restype = I
+        L.qso_num_threads.argtypes = []
+        _lib = L
+    return _lib
+
+
+def _ptr(a):
+    assert a.flags["C_CONTIGUOUS"]
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _as_half_bits(x):
+    x = np.ascontiguousarray(x)
+    if x.dtype == np.float16:
+        return x.view(np.uint16)
+    assert x.dtype == np.uint16
+    return x
+
+
+# ------------------------------------------------------------------ scalars
+
+def half_to_double(h):
+    return lib().qso_half_to_double(int(h))
+
+
+def float_to_half_rn(f):
+    return lib().qso_float_to_half_rn(float(np.float32(f)))
+
+
+def float_to_half_ru(f):
+    return lib().qso_float_to_half_ru(float(np.float32(f)))
+
+
+def quantize_group(x):
+    """QS-RN-v1 on a 1-D fp16 group -> (scale bits, zero bits, uint8 codes)."""
+    x = _as_half_bits(np.asarray(x))
+    assert x.ndim == 1
+    s = np.zeros(1, np.uint16)
+    z = np.zeros(1, np.uint16)
+    q = np.zeros(x.shape[0], np.uint8)
+    lib().qso_quantize_group(_ptr(x), 1, x.shape[0], _ptr(s), _ptr(z), _ptr(q), 1)
+    return int(s[0]), int(z[0]), q
+
+
+def split_code(q):
+    u = ctypes.c_uint8()
+    l_ = ctypes.c_uint8()
+    lib().qso_split_code(int(q), ctypes.byref(u), ctypes.byref(l_))
+    return u.value, l_.value
+
+
+def dequant(q, scale_bits, zero_bits, upper_only):
+    return lib().qso_dequant(int(q), int(scale_bits), int(zero_bits), int(bool(upper_only)))
+
+
+def num_threads():
+    return lib().qso_num_threads()
+
+
+# ------------------------------------------------------------------ cache
+
+class OracleCache:
+    """Logical cache state held in numpy arrays; every method calls the C
+    oracle on them in place."""
+
+    def __init__(self, B, H, D=128, G=128, cap=8):
+        self.B, self.H, self.D, self.G, self.cap = B, H, D, G, cap
+        self.kq = np.zeros((B, H, cap, G, D), np.uint8)
+        self.vq = np.zeros((B, H, cap, G, D), np.uint8)
+        self.ks = np.zeros((B, H, cap, D), np.uint16)
+        self.kz = np.zeros((B, H, cap, D), np.uint16)
+        self.vs = np.zeros((B, H, cap, G), np.uint16)
+        self.vz = np.zeros((B, H, cap, G), np.uint16)
+        self.bk = np.zeros((B, H, 2 * G, D), np.uint16)
+        self.bv = np.zeros((B, H, 2 * G, D), np.uint16)
+        self.state = np.zeros((B, STATE_WORDS), np.int32)
+
+    def _c(self):
+        return _Cache(self.B, self.H, self.D, self.G, self.cap,
+                      _ptr(self.kq).value, _ptr(self.vq).value,
+                      _ptr(self.ks).value, _ptr(self.kz).value,
+                      _ptr(self.vs).value, _ptr(self.vz).value,
+                      _ptr(self.bk).value, _ptr(self.bv).value,
+                      _ptr(self.state).value)
+
+    def append(self, k_new, v_new):
+        k = _as_half_bits(k_new)
+        v = _as_half_bits(v_new)
+        assert k.shape == v.shape and k.shape[:2] == (self.B, self.H) and k.shape[3] == self.D
+        c = self._c()
+        lib().qso_append(ctypes.byref(c), _ptr(k), _ptr(v), k.shape[2])
+
+    def rollback(self, n_drop):
+        n = np.ascontiguousarray(np.broadcast_to(np.asarray(n_drop, np.int32), (self.B,)))
+        c = self._c()
+        lib().qso_rollback(ctypes.byref(c), _ptr(n))
+
+    def need_flush(self, n_next):
+        m = np.zeros(self.B, np.uint8)
+        c = self._c()
+        lib().qso_need_flush(ctypes.byref(c), int(n_next), _ptr(m))
+        return m
+
+    def flush(self, mask=None):
+        c = self._c()
+        if mask is None:
+            lib().qso_flush(ctypes.byref(c), None)
+        else:
+            m = np.ascontiguousarray(np.asarray(mask, np.uint8))
+            lib().qso_flush(ctypes.byref(c), _ptr(m))
+
+    def attn(self, q, upper_only, scale=None):
+        """Decode attention in fp64: q [B, H, n_q, D] fp16 ->
+        (out [B, H, n_q, D] float64, lse [B, H, n_q] float64)."""
+        qb = _as_half_bits(q)
+        n_q = qb.shape[2]
+        if scale is None:
+            scale = 1.0 / np.sqrt(self.D)
+        scale = float(np.float32(scale))
+        out = np.zeros((self.B, self.H, n_q, self.D), np.float64)
+        lse = np.zeros((self.B, self.H, n_q), np.float64)
+        c = self._c()
+        lib().qso_attn(ctypes.byref(c), int(bool(upper_only)), _ptr(qb), n_q, scale,
+                       _ptr(out), _ptr(lse))
+        return out, lse
+
+    # views ------------------------------------------------------------
+    def counters(self, b):
+        s = self.state[b]
+        return dict(n_groups=int(s[N_GROUPS]), fill=int(s[FILL]), pending=int(s[PENDING]),
+                    half_base=int(s[HALF_BASE]), err=int(s[ERR]))
+
+    def buffer_tokens(self, b, h):
+        """Logical buffer tokens (oldest first): (k, v) fp16 bit arrays [fill, D]."""
+        s = self.state[b]
+        G = self.G
+        idx = (s[HALF_BASE] * G + np.arange(s[FILL])) % (2 * G)
+        return self.bk[b, h, idx], self.bv[b, h, idx]
