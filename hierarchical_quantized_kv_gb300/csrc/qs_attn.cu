@@ -1,0 +1,696 @@
+// qs_attn.cu -- split-KV decode attention over the hierarchical quantized KV
+// cache (draft: C_U only; verify: INT8 = 16 C_U + C_L) plus the fp16 buffer,
+// and the log-sum-exp combine.
+//
+// Sources: "QuantSpec Guide: Self-Speculative Decoding & Quantized KV",
+// "1. Hierarchical Two-Level Quantization with Bit-Sharing" (draft loads only
+// the upper 4 bits from HBM, target reconstructs INT8 from both) and the
+// quantizer listing (draft reconstruction at the nibble midpoint);
+// "QuantSpec: Self-Speculative Decoding with Hierarchical Quantized KV Cache"
+// (Pith review), "What carries the argument" and Appendix E (the buffer design
+// works with Flash Decoding: split-KV partial softmax, then an LSE combine).
+//
+// Design (GB300):
+//  * One persistent CTA per resident slot (SMs x occupancy).  All (sequence,
+//    head) segments are laid end to end as units (a quantized group of 128
+//    tokens, or a chunk of fp16 buffer tokens) and every CTA takes an equal
+//    contiguous range, so ragged batches balance without a host round trip.
+//  * Warp 4 is the producer: for each unit it issues bulk async copies
+//    (cp.async.bulk, TMA engine) of the unit's contiguous plane blocks into a
+//    ring of shared-memory stages guarded by mbarriers.  Draft units copy only
+//    the C_U planes (8 KB keys + 8 KB values + 1 KB scales/zeros).
+//  * Warps 0-3 are consumers, each on 32 tokens of a group: nibbles become
+//    exact fp16 integers in registers (bit tricks, no conversion
+//    instructions), and the dense contractions q.K^T and P.V run on
+//    m16n8k16 tensor-core MMAs with fp32 accumulation.  Scales are folded:
+//    B = q * s_K per channel, P' = p * s_V per token, zero-point terms as
+//    per-query biases, so the inner loops touch codes only.
+//  * Each consumer warp keeps its own online softmax and writes one partial
+//    per (piece of a segment); the combine kernel merges them.
+#include <math.h>
+
+#include "qs_common.cuh"
+
+namespace qs {
+namespace {
+
+constexpr int kConsumers = 4;
+constexpr int kThreads = (kConsumers + 1) * 32;
+constexpr int kTailRow = 272;  // padded fp16 row stride (bytes) of buffer tiles
+constexpr int kOffKU = 0, kOffVU = 8192, kOffMeta = 16384, kOffKL = 17408, kOffVL = 25600;
+
+template <int MODE>
+struct Cfg;
+template <>
+struct Cfg<QS_DRAFT_UPPER4> {
+  static constexpr int kGroupBytes = 8192 + 8192 + 1024;
+  static constexpr int kTailTok = 32;
+  static constexpr int kStages = 6;
+};
+template <>
+struct Cfg<QS_VERIFY_INT8> {
+  static constexpr int kGroupBytes = 4 * 8192 + 1024;
+  static constexpr int kTailTok = 64;
+  static constexpr int kStages = 3;
+};
+
+template <int MODE>
+struct Layout {
+  static constexpr int kTailBytes = Cfg<MODE>::kTailTok * kTailRow * 2;
+  static constexpr int kStageBytes =
+      Cfg<MODE>::kGroupBytes > kTailBytes ? Cfg<MODE>::kGroupBytes : kTailBytes;
+  static constexpr int kBarOff = Cfg<MODE>::kStages * kStageBytes;
+  static constexpr int kZeroOff = kBarOff + 2 * Cfg<MODE>::kStages * 8;
+  static constexpr int kTabOff = kZeroOff + 32;
+  // per-sequence tables: n_groups, fill, half_base, segment length, base unit
+  static constexpr int kSmemBytes = kTabOff + 5 * kMaxB * 4;
+};
+
+struct Params {
+  qs_cache c;
+  const uint16_t *q;
+  uint16_t *out;
+  float *lse;
+  float *ws;
+  int n_q;
+  int P;  // split-kernel grid size (number of contiguous unit ranges)
+  float sl2;  // softmax_scale * log2(e)
+};
+
+struct Tables {
+  int *ng, *fill, *hb, *len, *base;  // base in units, len in units per head
+};
+
+__device__ __forceinline__ Tables tables_at(uint8_t *smem, int off) {
+  int *t = reinterpret_cast<int *>(smem + off);
+  return Tables{t, t + kMaxB, t + 2 * kMaxB, t + 3 * kMaxB, t + 4 * kMaxB};
+}
+
+// Warp-cooperative: read counters, segment lengths (units per head) and the
+// exclusive prefix of units (x H) into the tables.  Returns the total.
+template <int TT>
+__device__ long long build_tables(const qs_cache &c, int n_q, Tables T, int lane) {
+  const int per = (c.B + 31) / 32;
+  const int b0 = lane * per;
+  int local = 0;
+  for (int i = 0; i < per; ++i) {
+    const int b = b0 + i;
+    if (b < c.B) {
+      const int32_t *st = c.state + (size_t)b * QS_STATE_WORDS;
+      // clamped so that no counter value can address outside the arrays
+      const int ng = min(max(st[QS_ST_N_GROUPS], 0), c.cap_groups);
+      const int fill = min(max(st[QS_ST_FILL], 0), kRing);
+      T.ng[b] = ng;
+      T.fill[b] = fill;
+      T.hb[b] = st[QS_ST_HALF_BASE] & 1;
+      const int len = (n_q <= fill) ? ng + (fill + TT - 1) / TT : 0;
+      T.len[b] = len;
+      local += len;
+    }
+  }
+  int incl = local;
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  long long run = (long long)(incl - local) * c.H;
+  for (int i = 0; i < per; ++i) {
+    const int b = b0 + i;
+    if (b < c.B) {
+      T.base[b] = (int)run;
+      run += (long long)T.len[b] * c.H;
+    }
+  }
+  return (long long)__shfl_sync(0xffffffffu, incl, 31) * c.H;
+}
+
+// CTA p owns units [floor(p U / P), floor((p+1) U / P)).
+__device__ __forceinline__ long long range_lo(int p, long long U, int P) {
+  return (long long)p * U / P;
+}
+// The CTA whose range holds unit x.
+__device__ __forceinline__ int cta_of(long long x, long long U, int P) {
+  return (int)(((x + 1) * P - 1) / U);
+}
+
+struct Cursor {
+  int b, h, u;
+  __device__ void init(long long x, const Tables &T, int B, int H) {
+    int lo = 0, hi = B - 1;  // largest b with base[b] <= x
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (T.base[mid] <= x) lo = mid; else hi = mid - 1;
+    }
+    b = lo;
+    const long long off = x - T.base[b];
+    h = (int)(off / T.len[b]);
+    u = (int)(off % T.len[b]);
+  }
+  __device__ void advance(const Tables &T, int B, int H) {
+    if (++u < T.len[b]) return;
+    u = 0;
+    if (++h < H) return;
+    h = 0;
+    do { ++b; } while (b < B && T.len[b] == 0);
+  }
+};
+
+// ---- nibble / byte planes -> exact fp16 integers (one half2 per pair) -----
+// Pair p of a 32-bit word holds elements (p, p + 4) of its 8 nibbles; draft
+// returns 16 * C_U, verify the 8-bit code 16 * C_U + C_L.
+__device__ __forceinline__ void pairs_upper(uint32_t w, uint32_t (&e)[4]) {
+  const uint32_t w8 = w >> 8;
+  e[0] = hsub2_u32((w & 0x000F000Fu) | 0x74007400u, 0x74007400u);
+  e[1] = hsub2_u32((w & 0x00F000F0u) | 0x64006400u, 0x64006400u);
+  e[2] = hsub2_u32((w8 & 0x000F000Fu) | 0x74007400u, 0x74007400u);
+  e[3] = hsub2_u32((w8 & 0x00F000F0u) | 0x64006400u, 0x64006400u);
+}
+
+__device__ __forceinline__ void pairs_int8(uint32_t wu, uint32_t wl, uint32_t (&e)[4]) {
+  const uint32_t ev = (wl & 0x0F0F0F0Fu) | ((wu << 4) & 0xF0F0F0F0u);  // codes 0,2,4,6
+  const uint32_t od = ((wl >> 4) & 0x0F0F0F0Fu) | (wu & 0xF0F0F0F0u);  // codes 1,3,5,7
+  e[0] = hsub2_u32(prmt(ev, 0x64646464u, 0x4240), 0x64006400u);
+  e[1] = hsub2_u32(prmt(od, 0x64646464u, 0x4240), 0x64006400u);
+  e[2] = hsub2_u32(prmt(ev, 0x64646464u, 0x4341), 0x64006400u);
+  e[3] = hsub2_u32(prmt(od, 0x64646464u, 0x4341), 0x64006400u);
+}
+
+template <int MODE>
+__device__ __forceinline__ void pairs(uint32_t wu, uint32_t wl, uint32_t (&e)[4]) {
+  if (MODE == QS_DRAFT_UPPER4) pairs_upper(wu, e);
+  else pairs_int8(wu, wl, e);
+}
+
+__device__ __forceinline__ uint32_t lds32(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint16_t lds16(uint32_t a) {
+  uint16_t v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ float h2f(uint16_t b) { return __half2float(__ushort_as_half(b)); }
+
+// Per-warp online-softmax state for its two queries (columns 2c, 2c+1).
+struct Softmax {
+  float m[2], l[2], bv[2];
+  float o[8][4];  // O^T accumulators: rows = channels 16 md + r (+8), cols = queries
+  __device__ void reset() {
+#pragma unroll
+    for (int i = 0; i < 2; ++i) { m[i] = -INFINITY; l[i] = 0.f; bv[i] = 0.f; }
+#pragma unroll
+    for (int md = 0; md < 8; ++md)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) o[md][k] = 0.f;
+  }
+  // New maximum from this step's warp-wide maxima; rescales the state and
+  // returns the offset to subtract (0 when nothing is visible yet).
+  __device__ void update(float g0, float g1, float &u0, float &u1) {
+    const float n0 = fmaxf(m[0], g0), n1 = fmaxf(m[1], g1);
+    u0 = (n0 == -INFINITY) ? 0.f : n0;
+    u1 = (n1 == -INFINITY) ? 0.f : n1;
+    const float a0 = fast_exp2(m[0] - u0), a1 = fast_exp2(m[1] - u1);
+    m[0] = n0;
+    m[1] = n1;
+    if (a0 != 1.f || a1 != 1.f) {
+      l[0] *= a0; l[1] *= a1; bv[0] *= a0; bv[1] *= a1;
+#pragma unroll
+      for (int md = 0; md < 8; ++md) {
+        o[md][0] *= a0; o[md][1] *= a1; o[md][2] *= a0; o[md][3] *= a1;
+      }
+    }
+  }
+};
+
+__device__ __forceinline__ float warp_max8(float v) {  // over lanes sharing lane & 3
+  v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
+  v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
+  v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
+  return v;
+}
+__device__ __forceinline__ float warp_sum8(float v) {
+  v += __shfl_xor_sync(0xffffffffu, v, 4);
+  v += __shfl_xor_sync(0xffffffffu, v, 8);
+  v += __shfl_xor_sync(0xffffffffu, v, 16);
+  return v;
+}
+
+// q row of query r as tensor-core B pairs in the key-plane channel order:
+// k-block kb, first register {q(ch0), q(ch0+4)}, second {q(ch0+1), q(ch0+5)},
+// ch0 = 32c + 8 (kb >> 1) + 2 (kb & 1).
+__device__ __forceinline__ void load_q_pairs(const uint16_t *qrow, bool valid, int c,
+                                             uint32_t (&q0)[8], uint32_t (&q1)[8]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint4 w = make_uint4(0, 0, 0, 0);
+    if (valid) w = __ldg(reinterpret_cast<const uint4 *>(qrow + 32 * c) + i);
+    q0[2 * i] = prmt(w.x, w.z, 0x5410);
+    q1[2 * i] = prmt(w.x, w.z, 0x7632);
+    q0[2 * i + 1] = prmt(w.y, w.w, 0x5410);
+    q1[2 * i + 1] = prmt(w.y, w.w, 0x7632);
+  }
+}
+
+// ------------------------------------------------------------ split kernel
+template <int MODE>
+__global__ void __launch_bounds__(kThreads, 2) split_kernel(const Params prm) {
+  using C = Cfg<MODE>;
+  using L = Layout<MODE>;
+  constexpr int TT = C::kTailTok, S = C::kStages;
+  extern __shared__ __align__(128) uint8_t smem[];
+  const qs_cache &c = prm.c;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t sbase = smem_addr(smem);
+  const uint32_t full0 = sbase + L::kBarOff, empty0 = full0 + 8 * S;
+  const uint32_t zero_row = sbase + L::kZeroOff;
+  Tables T = tables_at(smem, L::kTabOff);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, kConsumers);
+    }
+    fence_mbar_init();
+  }
+  if (threadIdx.x < 8) reinterpret_cast<uint32_t *>(smem + L::kZeroOff)[threadIdx.x] = 0;
+  __shared__ long long s_total;
+  if (warp == 0) {
+    const long long tot = build_tables<TT>(c, prm.n_q, T, lane);
+    if (lane == 0) s_total = tot;
+  }
+  __syncthreads();
+  const long long U = s_total;
+  const int p = blockIdx.x;
+  const long long x0 = range_lo(p, U, prm.P), x1 = range_lo(p + 1, U, prm.P);
+  if (x0 >= x1) return;
+
+  if (warp == kConsumers) {
+    // ------------------------------------------------------- producer
+    Cursor cur;
+    cur.init(x0, T, c.B, c.H);
+    long long issued = 0;
+    for (long long x = x0; x < x1; ++x, ++issued) {
+      const int stage = (int)(issued % S);
+      const uint32_t par = (uint32_t)((issued / S) & 1);
+      if (!mbar_wait(empty0 + 8 * stage, par ^ 1u)) {
+        if (lane == 0) atomicOr(&c.state[(size_t)cur.b * QS_STATE_WORDS + QS_ST_ERR], QS_DEV_TIMEOUT);
+        break;
+      }
+      const uint32_t dst = sbase + stage * L::kStageBytes, bar = full0 + 8 * stage;
+      const size_t bh = (size_t)cur.b * c.H + cur.h;
+      const int ng = T.ng[cur.b];
+      if (cur.u < ng) {
+        if (lane == 0) {
+          const size_t grp = bh * c.cap_groups + cur.u;
+          mbar_arrive_expect_tx(bar, C::kGroupBytes);
+          bulk_g2s(dst + kOffKU, c.k_upper + grp * 8192, 8192, bar);
+          bulk_g2s(dst + kOffVU, c.v_upper + grp * 8192, 8192, bar);
+          bulk_g2s(dst + kOffMeta, c.meta + grp * 512, 1024, bar);
+          if (MODE == QS_VERIFY_INT8) {
+            bulk_g2s(dst + kOffKL, c.k_lower + grp * 8192, 8192, bar);
+            bulk_g2s(dst + kOffVL, c.v_lower + grp * 8192, 8192, bar);
+          }
+        }
+      } else {
+        const int i0 = (cur.u - ng) * TT;
+        const int rows = min(TT, T.fill[cur.b] - i0);
+        if (lane == 0) mbar_arrive_expect_tx(bar, rows * 2 * kD * 2);
+        __syncwarp();
+        const int slot0 = T.hb[cur.b] * kG + i0;  // chunks never straddle the ring end
+        for (int rr = lane; rr < 2 * rows; rr += 32) {
+          const bool isv = rr >= rows;
+          const int row = isv ? rr - rows : rr;
+          const int slot = (slot0 + row) & (kRing - 1);
+          const uint16_t *src = (isv ? c.buf_v : c.buf_k) + (bh * kRing + slot) * kD;
+          bulk_g2s(dst + (isv ? TT * kTailRow : 0) + row * kTailRow, src, kD * 2, bar);
+        }
+      }
+      cur.advance(T, c.B, c.H);
+    }
+    // drain: no copy may still be in flight when this warp leaves
+    const long long first = issued > S ? issued - S : 0;
+    for (long long k = first; k < issued; ++k)
+      if (!mbar_wait(full0 + 8 * (int)(k % S), (uint32_t)((k / S) & 1))) break;
+    return;
+  }
+
+  // --------------------------------------------------------- consumers
+  const int w = warp, r = lane >> 2, cq = lane & 3;
+  Cursor cur;
+  cur.init(x0, T, c.B, c.H);
+  Softmax sm;
+  sm.reset();
+  uint32_t qp0[8], qp1[8];
+  int fill = 0, ng = 0;
+  long long idx = 0;
+  for (long long x = x0; x < x1; ++x, ++idx) {
+    const size_t bh = (size_t)cur.b * c.H + cur.h;
+    if (x == x0 || cur.u == 0) {  // a new piece: this (sequence, head)
+      load_q_pairs(prm.q + (bh * prm.n_q + r) * kD, r < prm.n_q, cq, qp0, qp1);
+      sm.reset();
+      fill = T.fill[cur.b];
+      ng = T.ng[cur.b];
+    }
+    const int stage = (int)(idx % S);
+    const uint32_t par = (uint32_t)((idx / S) & 1);
+    if (!mbar_wait(full0 + 8 * stage, par)) {
+      if (lane == 0) atomicOr(&c.state[(size_t)cur.b * QS_STATE_WORDS + QS_ST_ERR], QS_DEV_TIMEOUT);
+      return;
+    }
+    const uint32_t st = sbase + stage * L::kStageBytes;
+
+    if (cur.u < ng) {
+      // ================================================ quantized group
+      // per-group B = q * s_K (fp16) and key bias sum_d q_d (z_d [+ 8 s_d])
+      uint32_t bm0[8], bm1[8];
+      float bacc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint4 sw = lds128(st + kOffMeta + QS_META_K_SCALE * 256 + 64 * cq + 16 * i);
+        const uint4 zw = lds128(st + kOffMeta + QS_META_K_ZERO * 256 + 64 * cq + 16 * i);
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          const int kb = 2 * i + t;
+          const uint32_t sa = t ? sw.y : sw.x, sb = t ? sw.w : sw.z;
+          const uint32_t za = t ? zw.y : zw.x, zb = t ? zw.w : zw.z;
+          const uint32_t sp0 = prmt(sa, sb, 0x5410), sp1 = prmt(sa, sb, 0x7632);
+          const uint32_t zp0 = prmt(za, zb, 0x5410), zp1 = prmt(za, zb, 0x7632);
+          bm0[kb] = hmul2_u32(qp0[kb], sp0);
+          bm1[kb] = hmul2_u32(qp1[kb], sp1);
+          // rows 0-7 of A = zero-points, rows 8-15 = scales: one MMA gives
+          // sum_d z_d q_d and sum_d s_d q_d for every query
+          mma16816(bacc, zp0, sp0, zp1, sp1, qp0[kb], qp1[kb]);
+        }
+      }
+      const float kb0 = (MODE == QS_DRAFT_UPPER4) ? bacc[0] + 8.f * bacc[2] : bacc[0];
+      const float kb1 = (MODE == QS_DRAFT_UPPER4) ? bacc[1] + 8.f * bacc[3] : bacc[1];
+      const float bk0 = kb0 * prm.sl2, bk1 = kb1 * prm.sl2;
+
+      // scores for the warp's 32 tokens: two m-tiles of 16
+      float s[2][4];
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt) {
+        const int t0 = 32 * w + 16 * mt + r;
+        const uint4 u0 = lds128(st + kOffKU + t0 * 64 + 16 * cq);
+        const uint4 u1 = lds128(st + kOffKU + (t0 + 8) * 64 + 16 * cq);
+        uint4 l0 = make_uint4(0, 0, 0, 0), l1 = l0;
+        if (MODE == QS_VERIFY_INT8) {
+          l0 = lds128(st + kOffKL + t0 * 64 + 16 * cq);
+          l1 = lds128(st + kOffKL + (t0 + 8) * 64 + 16 * cq);
+        }
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        const uint32_t wu0[4] = {u0.x, u0.y, u0.z, u0.w}, wu1[4] = {u1.x, u1.y, u1.z, u1.w};
+        const uint32_t wl0[4] = {l0.x, l0.y, l0.z, l0.w}, wl1[4] = {l1.x, l1.y, l1.z, l1.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          uint32_t a[4], b8[4];
+          pairs<MODE>(wu0[i], wl0[i], a);
+          pairs<MODE>(wu1[i], wl1[i], b8);
+          mma16816(acc, a[0], b8[0], a[1], b8[1], bm0[2 * i], bm1[2 * i]);
+          mma16816(acc, a[2], b8[2], a[3], b8[3], bm0[2 * i + 1], bm1[2 * i + 1]);
+        }
+        s[mt][0] = fmaf(acc[0], prm.sl2, bk0);
+        s[mt][1] = fmaf(acc[1], prm.sl2, bk1);
+        s[mt][2] = fmaf(acc[2], prm.sl2, bk0);
+        s[mt][3] = fmaf(acc[3], prm.sl2, bk1);
+      }
+      float g0 = fmaxf(fmaxf(s[0][0], s[0][2]), fmaxf(s[1][0], s[1][2]));
+      float g1 = fmaxf(fmaxf(s[0][1], s[0][3]), fmaxf(s[1][1], s[1][3]));
+      float u0, u1;
+      sm.update(warp_max8(g0), warp_max8(g1), u0, u1);
+
+      // probabilities, value scale folded in, value zero-point as a bias
+      uint32_t bp0[2], bp1[2];
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt) {
+        float pv[4];
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int t = 32 * w + 16 * mt + r + 8 * hh;
+          const float sv = h2f(lds16(st + kOffMeta + QS_META_V_SCALE * 256 + 2 * t));
+          float zv = h2f(lds16(st + kOffMeta + QS_META_V_ZERO * 256 + 2 * t));
+          if (MODE == QS_DRAFT_UPPER4) zv = fmaf(8.f, sv, zv);
+          const float pa = fast_exp2(s[mt][2 * hh] - u0), pb = fast_exp2(s[mt][2 * hh + 1] - u1);
+          sm.l[0] += pa;
+          sm.l[1] += pb;
+          sm.bv[0] = fmaf(pa, zv, sm.bv[0]);
+          sm.bv[1] = fmaf(pb, zv, sm.bv[1]);
+          pv[2 * hh] = pa * sv;
+          pv[2 * hh + 1] = pb * sv;
+        }
+        bp0[mt] = movmatrix_trans(pack_half2(pv[0], pv[1]));
+        bp1[mt] = movmatrix_trans(pack_half2(pv[2], pv[3]));
+      }
+      // O^T += V^T P'  (values: quarter w of the group, channel-major rows)
+#pragma unroll
+      for (int md = 0; md < 8; ++md) {
+        const uint32_t ra = st + kOffVU + (w * 128 + 16 * md + r) * 16 + 4 * cq;
+        const uint32_t vu0 = lds32(ra), vu1 = lds32(ra + 8 * 16);
+        uint32_t vl0 = 0, vl1 = 0;
+        if (MODE == QS_VERIFY_INT8) {
+          vl0 = lds32(ra - kOffVU + kOffVL);
+          vl1 = lds32(ra - kOffVU + kOffVL + 8 * 16);
+        }
+        uint32_t a[4], b8[4];
+        pairs<MODE>(vu0, vl0, a);
+        pairs<MODE>(vu1, vl1, b8);
+        mma16816(sm.o[md], a[0], b8[0], a[1], b8[1], bp0[0], bp1[0]);
+        mma16816(sm.o[md], a[2], b8[2], a[3], b8[3], bp0[1], bp1[1]);
+      }
+    } else {
+      // ================================================ fp16 buffer chunk
+      const int i0 = (cur.u - ng) * TT;
+      const int rows = min(TT, fill - i0);
+      const int mr = 16 * w;
+      if (mr < rows) {
+        // natural-order B pairs of q for query r
+        const uint32_t *qw = reinterpret_cast<const uint32_t *>(prm.q + (bh * prm.n_q + r) * kD);
+        const bool qv = r < prm.n_q;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int kb = 0; kb < 8; ++kb) {
+          const uint32_t b0 = qv ? __ldg(qw + 8 * kb + cq) : 0u;
+          const uint32_t b1 = qv ? __ldg(qw + 8 * kb + cq + 4) : 0u;
+          const int row = mr + (lane & 7) + ((lane >> 3) & 1) * 8;
+          const int col = 16 * kb + (lane >> 4) * 8;
+          const uint32_t addr = row < rows ? st + row * kTailRow + col * 2 : zero_row;
+          uint32_t a0, a1, a2, a3;
+          ldmatrix_x4(addr, a0, a1, a2, a3);
+          mma16816(acc, a0, a1, a2, a3, b0, b1);
+        }
+        const int lim0 = fill - prm.n_q + 2 * cq;  // last visible buffer index, query 2c
+        float sv[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int tok = mr + r + 8 * (k >> 1);
+          const int j = k & 1;
+          const bool vis = tok < rows && (i0 + tok) <= lim0 + j;
+          sv[k] = vis ? acc[k] * prm.sl2 : -INFINITY;
+        }
+        float u0, u1;
+        sm.update(warp_max8(fmaxf(sv[0], sv[2])), warp_max8(fmaxf(sv[1], sv[3])), u0, u1);
+        float pv[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          pv[k] = fast_exp2(sv[k] - ((k & 1) ? u1 : u0));
+          sm.l[k & 1] += pv[k];
+        }
+        const uint32_t bq0 = movmatrix_trans(pack_half2(pv[0], pv[1]));
+        const uint32_t bq1 = movmatrix_trans(pack_half2(pv[2], pv[3]));
+        const uint32_t vbase = st + TT * kTailRow;
+#pragma unroll
+        for (int md = 0; md < 8; ++md) {
+          const int mi = lane >> 3;
+          const int tok = mr + (lane & 7) + (mi >> 1) * 8;
+          const int ch = 16 * md + (mi & 1) * 8;
+          const uint32_t addr = tok < rows ? vbase + tok * kTailRow + ch * 2 : zero_row;
+          uint32_t a0, a1, a2, a3;
+          ldmatrix_x4_trans(addr, a0, a1, a2, a3);
+          mma16816(sm.o[md], a0, a1, a2, a3, bq0, bq1);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty0 + 8 * stage);
+
+    if (x + 1 == x1 || cur.u + 1 == T.len[cur.b]) {
+      // ---- piece done: one partial per warp (unnormalized, log2 domain)
+      const float l0 = warp_sum8(sm.l[0]), l1 = warp_sum8(sm.l[1]);
+      const float v0 = warp_sum8(sm.bv[0]), v1 = warp_sum8(sm.bv[1]);
+      const int stride = prm.n_q * kD + 16;
+      const long long seg = (long long)cur.b * c.H + cur.h;
+      float *dst = prm.ws + ((seg + p) * kConsumers + w) * stride;
+      const int j0 = 2 * cq, j1 = 2 * cq + 1;
+#pragma unroll
+      for (int md = 0; md < 8; ++md) {
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int d = 16 * md + r + 8 * hh;
+          if (j0 < prm.n_q) dst[j0 * kD + d] = sm.o[md][2 * hh] + v0;
+          if (j1 < prm.n_q) dst[j1 * kD + d] = sm.o[md][2 * hh + 1] + v1;
+        }
+      }
+      if (r == 0) {
+        if (j0 < prm.n_q) { dst[prm.n_q * kD + j0] = sm.m[0]; dst[prm.n_q * kD + 8 + j0] = l0; }
+        if (j1 < prm.n_q) { dst[prm.n_q * kD + j1] = sm.m[1]; dst[prm.n_q * kD + 8 + j1] = l1; }
+      }
+    }
+    cur.advance(T, c.B, c.H);
+  }
+}
+
+// ----------------------------------------------------------- combine kernel
+// One CTA per (head, sequence), one thread per channel:
+// o = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s.
+template <int MODE>
+__global__ void __launch_bounds__(128) combine_kernel(const Params prm) {
+  constexpr int TT = Cfg<MODE>::kTailTok;
+  __shared__ int tab[5 * kMaxB];
+  __shared__ long long s_total;
+  const qs_cache &c = prm.c;
+  Tables T{tab, tab + kMaxB, tab + 2 * kMaxB, tab + 3 * kMaxB, tab + 4 * kMaxB};
+  const int h = blockIdx.x, b = blockIdx.y, d = threadIdx.x;
+  if (threadIdx.x < 32) {
+    const long long tot = build_tables<TT>(c, prm.n_q, T, threadIdx.x);
+    if (threadIdx.x == 0) s_total = tot;
+  }
+  __syncthreads();
+  const size_t bh = (size_t)b * c.H + h;
+  const int nq = prm.n_q;
+  if (T.len[b] == 0) {  // n_q > fill: nothing is visible
+    if (h == 0 && d == 0 && nq > T.fill[b])
+      atomicOr(&c.state[(size_t)b * QS_STATE_WORDS + QS_ST_ERR], QS_DEV_NQ_GT_FILL);
+    for (int j = 0; j < nq; ++j) {
+      prm.out[(bh * nq + j) * kD + d] = 0;
+      if (prm.lse && d == 0) prm.lse[bh * nq + j] = -INFINITY;
+    }
+    return;
+  }
+  const long long U = s_total;
+  const long long S0 = T.base[b] + (long long)h * T.len[b], E0 = S0 + T.len[b];
+  const int plo = cta_of(S0, U, prm.P), phi = cta_of(E0 - 1, U, prm.P);
+  const long long seg = (long long)bh;
+  const int stride = nq * kD + 16;
+  for (int j = 0; j < nq; ++j) {
+    float M = -INFINITY;
+    for (int pp = plo; pp <= phi; ++pp)
+      for (int w = 0; w < kConsumers; ++w)
+        M = fmaxf(M, prm.ws[((seg + pp) * kConsumers + w) * stride + nq * kD + j]);
+    float Lsum = 0.f, acc = 0.f;
+    for (int pp = plo; pp <= phi; ++pp)
+      for (int w = 0; w < kConsumers; ++w) {
+        const float *part = prm.ws + ((seg + pp) * kConsumers + w) * stride;
+        const float ms = part[nq * kD + j];
+        const float f = (ms == -INFINITY) ? 0.f : exp2f(ms - M);
+        Lsum = fmaf(f, part[nq * kD + 8 + j], Lsum);
+        acc = fmaf(f, part[j * kD + d], acc);
+      }
+    prm.out[(bh * nq + j) * kD + d] = __half_as_ushort(__float2half_rn(acc / Lsum));
+    if (prm.lse && d == 0) prm.lse[bh * nq + j] = (M + log2f(Lsum)) * 0.69314718055994531f;
+  }
+}
+
+// --------------------------------------------------------------- host side
+struct DevInfo {
+  int ready[2];
+  int grid[2];
+};
+DevInfo g_dev[64];
+
+template <int MODE>
+qs_status grid_for_device(int dev, int &P) {
+  DevInfo &di = g_dev[dev];
+  if (!__atomic_load_n(&di.ready[MODE], __ATOMIC_ACQUIRE)) {
+    const int smem = Layout<MODE>::kSmemBytes;
+    if (cudaFuncSetAttribute(split_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem) != cudaSuccess)
+      return QS_ERR_CUDA;
+    int sms = 0, occ = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return QS_ERR_CUDA;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, split_kernel<MODE>, kThreads, smem) !=
+        cudaSuccess)
+      return QS_ERR_CUDA;
+    if (occ < 1) return QS_ERR_CUDA;
+    di.grid[MODE] = sms * occ;
+    __atomic_store_n(&di.ready[MODE], 1, __ATOMIC_RELEASE);
+  }
+  P = di.grid[MODE];
+  return QS_OK;
+}
+
+qs_status grid_size(qs_mode mode, int &P) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return QS_ERR_CUDA;
+  if (dev < 0 || dev >= 64) return QS_ERR_UNSUPPORTED;
+  return mode == QS_DRAFT_UPPER4 ? grid_for_device<QS_DRAFT_UPPER4>(dev, P)
+                                 : grid_for_device<QS_VERIFY_INT8>(dev, P);
+}
+
+size_t ws_bytes(int P, int B, int H, int n_q) {
+  return (size_t)(P + (size_t)B * H) * kConsumers * (size_t)(n_q * kD + 16) * sizeof(float);
+}
+
+template <int MODE>
+qs_status launch(const Params &prm, cudaStream_t s) {
+  split_kernel<MODE><<<prm.P, kThreads, Layout<MODE>::kSmemBytes, s>>>(prm);
+  qs_status st = launch_status();
+  if (st != QS_OK) return st;
+  combine_kernel<MODE><<<dim3(prm.c.H, prm.c.B), 128, 0, s>>>(prm);
+  return launch_status();
+}
+
+}  // namespace
+}  // namespace qs
+
+using namespace qs;
+
+extern "C" {
+
+qs_status qs_attn_workspace_size(const qs_cache *c, int32_t n_q, size_t *bytes) {
+  qs_status s = check_cache(c);
+  if (s != QS_OK) return s;
+  if (!bytes || n_q < 1 || n_q > kMaxQ) return QS_ERR_ARG;
+  int P0 = 0, P1 = 0;
+  if ((s = grid_size(QS_DRAFT_UPPER4, P0)) != QS_OK) return s;
+  if ((s = grid_size(QS_VERIFY_INT8, P1)) != QS_OK) return s;
+  *bytes = ws_bytes(P0 > P1 ? P0 : P1, c->B, c->H, n_q);
+  return QS_OK;
+}
+
+qs_status qs_attn_decode(const qs_cache *c, qs_mode mode, const uint16_t *q, int32_t n_q,
+                         float softmax_scale, uint16_t *out, float *lse, void *workspace,
+                         size_t workspace_bytes, qs_stream_t stream) {
+  qs_status s = check_cache(c);
+  if (s != QS_OK) return s;
+  if (!q || !out || n_q < 1 || n_q > kMaxQ) return QS_ERR_ARG;
+  if (mode != QS_DRAFT_UPPER4 && mode != QS_VERIFY_INT8) return QS_ERR_ARG;
+  if (!(softmax_scale > 0.f) || !isfinite(softmax_scale)) return QS_ERR_ARG;
+  if (!aligned16(q) || !aligned16(out) || (lse && !aligned16(lse))) return QS_ERR_ALIGN;
+  Params prm;
+  prm.c = *c;
+  prm.q = q;
+  prm.out = out;
+  prm.lse = lse;
+  prm.n_q = n_q;
+  prm.sl2 = softmax_scale * 1.4426950408889634f;
+  if ((s = grid_size(mode, prm.P)) != QS_OK) return s;
+  if (!workspace || !aligned16(workspace) ||
+      workspace_bytes < ws_bytes(prm.P, c->B, c->H, n_q))
+    return QS_ERR_WORKSPACE;
+  prm.ws = static_cast<float *>(workspace);
+  cudaStream_t st = (cudaStream_t)stream;
+  return mode == QS_DRAFT_UPPER4 ? launch<QS_DRAFT_UPPER4>(prm, st)
+                                 : launch<QS_VERIFY_INT8>(prm, st);
+}
+
+}  // extern "C"

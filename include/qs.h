@@ -1,0 +1,209 @@
+/*
+ * qs.h -- C ABI of libqs: the QuantSpec hierarchical quantized KV cache hot
+ * path on one NVIDIA GB300 (sm_103a).
+ *
+ * What it computes (sources named by page title and section):
+ *  - "QuantSpec: Self-Speculative Decoding with Hierarchical Quantized KV
+ *    Cache" (Pith review), "What carries the argument": each key or value group
+ *    of size G is stored once as an upper INT4 tensor C_U and a lower INT4
+ *    residual C_L sharing one scale and zero-point, C_INT8 = 2^4 C_U + C_L;
+ *    the draft pass dequantizes C_U only, the target (verify) pass the INT8
+ *    reconstruction; a double full-precision buffer of two halves of G tokens
+ *    takes new tokens, rejected speculative tokens are dropped before
+ *    quantization, and a half is quantized once every G decoding steps.
+ *  - same page, Figure 7 caption and Appendix D: keys are quantized per
+ *    channel (a group = G tokens of one channel), values per token (a group =
+ *    G channels of one token); asymmetric quantization.
+ *  - same page, Appendix E: the buffer design is compatible with Flash
+ *    Decoding (split-KV partial softmax plus a log-sum-exp combine).
+ *  - "QuantSpec Guide: Self-Speculative Decoding & Quantized KV", sections
+ *    "1. Hierarchical Two-Level Quantization with Bit-Sharing" (draft loads only
+ *    the upper 4 bits from HBM) and the quantizer listing (min/max over the
+ *    group, 255 levels, round, clamp, upper = q >> 4, lower = q & 15, draft
+ *    reconstruction at the nibble midpoint).
+ *
+ * Rounding convention QS-RN-v1 (this library's reading; the pages print no
+ * rule for the stored scale): for a group x_0..x_{G-1} of fp16 values
+ *   r = fp32(max) - fp32(min), s = r == 0 ? 0 : fp16_round_up(r / 255.0f),
+ *   z = min (a zero minimum is stored as +0),
+ *   q_i = s == 0 ? 0 : clamp(rne((fp32(x_i) - fp32(z)) / fp32(s)), 0, 255)
+ * (every fp32 step IEEE round-to-nearest-even), C_U = q >> 4, C_L = q & 15,
+ *   verify: deq = s * (16 C_U + C_L) + z,   draft: deq = s * (16 C_U + 8) + z.
+ *
+ * Ownership: every array is caller-owned device memory; the library never
+ * allocates and keeps no global state.  Every call is asynchronous on the
+ * given stream except qs_get_errors.  Calls on different caches may run
+ * concurrently; calls on one cache must be ordered by the caller (one stream).
+ *
+ * Host-side errors are returned as qs_status before anything is launched.
+ * Preconditions that depend on device-resident counters (overflow, rollback
+ * beyond the pending tokens, flush without G committed tokens, capacity,
+ * fewer buffered tokens than queries) are checked on the device: the
+ * operation becomes a no-op for that sequence and a bit is set in the
+ * sequence's error word (QS_DEV_*), read back with qs_get_errors.  No kernel
+ * of this library traps or waits without a time limit.
+ *
+ * v1 supports D = G = 128 only (all workloads of the pages use head_dim 128
+ * and G = 128); other values return QS_ERR_UNSUPPORTED.
+ */
+#ifndef QS_H_
+#define QS_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* cudaStream_t without pulling in the CUDA headers */
+typedef struct CUstream_st *qs_stream_t;
+
+typedef enum {
+  QS_OK = 0,
+  QS_ERR_ARG = 1,         /* null pointer, bad count or mode */
+  QS_ERR_SHAPE = 2,       /* inconsistent sizes */
+  QS_ERR_ALIGN = 3,       /* a device pointer is not 16-byte aligned */
+  QS_ERR_CUDA = 4,        /* a CUDA call or launch failed */
+  QS_ERR_UNSUPPORTED = 5, /* D or G other than 128 */
+  QS_ERR_WORKSPACE = 6    /* workspace missing or smaller than required */
+} qs_status;
+
+typedef enum {
+  QS_DRAFT_UPPER4 = 0, /* keys/values from C_U only: s * (16 C_U + 8) + z */
+  QS_VERIFY_INT8 = 1   /* keys/values from C_U and C_L: s * (16 C_U + C_L) + z */
+} qs_mode;
+
+/* Device-side error bits, one error word per sequence. */
+enum {
+  QS_DEV_OVERFLOW = 1,           /* append would exceed the 2G buffer */
+  QS_DEV_OVER_ROLLBACK = 2,      /* n_drop < 0 or > pending tokens */
+  QS_DEV_FLUSH_UNCOMMITTED = 4,  /* flush with fewer than G committed tokens */
+  QS_DEV_CAPACITY = 8,           /* flush with n_groups == cap_groups */
+  QS_DEV_NQ_GT_FILL = 16,        /* attention with n_q > buffered tokens */
+  QS_DEV_TIMEOUT = 32            /* a pipeline wait ran out of time (never
+                                    expected; the call's results are invalid) */
+};
+
+/* Per-sequence counters: int32 state[B][QS_STATE_WORDS]. */
+enum {
+  QS_ST_N_GROUPS = 0,  /* quantized groups; quantized tokens Tq = n_groups * G */
+  QS_ST_FILL = 1,      /* tokens in the fp16 buffer (committed + pending) */
+  QS_ST_PENDING = 2,   /* speculative tokens at the end of the buffer */
+  QS_ST_HALF_BASE = 3, /* 0/1: buffer half that holds logical token 0 */
+  QS_ST_ERR = 4,       /* QS_DEV_* bits */
+  QS_ST_TICKET = 5,    /* internal arrival counter; must start at 0 */
+  QS_STATE_WORDS = 8
+};
+
+/* Rows of the per-group metadata block (fp16 [4][128] per group). */
+enum { QS_META_K_SCALE = 0, QS_META_K_ZERO = 1, QS_META_V_SCALE = 2, QS_META_V_ZERO = 3 };
+
+/*
+ * The cache: one struct of device pointers, all caller-owned, 16-byte
+ * aligned.  Logical buffer token i of sequence b lives in slot
+ * (half_base * G + i) mod 2G.  Sizes for each array: qs_cache_bytes.
+ *
+ *  k_upper, k_lower  uint8 [B][H][cap][G tokens][D/2]: C_U / C_L of the keys,
+ *      token-major; byte i of a token row holds channel 2i in bits 0-3 and
+ *      channel 2i+1 in bits 4-7 (64 bytes per token).
+ *  v_upper, v_lower  uint8 [B][H][cap][G/32][D][16]: C_U / C_L of the values,
+ *      per group in four quarters of 32 tokens, channel-major inside a
+ *      quarter: 16 bytes = 32 nibbles per (quarter u, channel d).  Nibble
+ *      position p (byte p/2, bits 0-3 for even p, 4-7 for odd p) holds token
+ *        32u + 16*((p>>1)&1) + 8*(p&1) + 2*(p>>3) + ((p>>2)&1)
+ *      of the group.  This fixed permutation lets one 32-bit shared-memory
+ *      word per lane feed tensor-core fragments without byte shuffles.
+ *  meta  fp16 [B][H][cap][4][128]: per group, rows QS_META_*: key scale and
+ *      zero per channel, value scale and zero per token.
+ *  buf_k, buf_v  fp16 [B][H][2G][D]: the double full-precision buffer.
+ *  state  int32 [B][QS_STATE_WORDS]: counters above; zero it (qs_state_reset)
+ *      before first use.
+ */
+typedef struct {
+  int32_t B, H, D, G, cap_groups;
+  uint8_t *k_upper, *k_lower, *v_upper, *v_lower;
+  uint16_t *meta;         /* fp16 bits */
+  uint16_t *buf_k, *buf_v; /* fp16 bits */
+  int32_t *state;
+} qs_cache;
+
+typedef struct {
+  size_t k_upper, k_lower, v_upper, v_lower, meta, buf_k, buf_v, state;
+} qs_cache_bytes_t;
+
+/* Byte size of every cache array for the given dimensions.  Pure host
+ * function.  Errors: QS_ERR_ARG (null out, non-positive sizes),
+ * QS_ERR_UNSUPPORTED (D or G != 128). */
+qs_status qs_cache_bytes(int32_t B, int32_t H, int32_t D, int32_t G, int32_t cap_groups,
+                         qs_cache_bytes_t *out);
+
+/* Zero every sequence's counters (empty cache).  Asynchronous memset. */
+qs_status qs_state_reset(const qs_cache *c, qs_stream_t stream);
+
+/* Append n_new tokens per sequence to the fp16 buffer as pending tokens.
+ * k_new, v_new: fp16 [B][H][n_new][D] device arrays, 1 <= n_new <= 2G.
+ * Per sequence: needs fill + n_new <= 2G, else QS_DEV_OVERFLOW and no-op.
+ * Source: Pith review page, "What carries the argument" (new tokens enter
+ * the double full-precision buffer). */
+qs_status qs_buffer_append(const qs_cache *c, const uint16_t *k_new, const uint16_t *v_new,
+                           int32_t n_new, qs_stream_t stream);
+
+/* Drop the last n_drop[b] pending tokens of each sequence and commit the
+ * rest (pending becomes 0).  d_n_drop: int32 [B] device array.  n_drop < 0 or
+ * > pending gives QS_DEV_OVER_ROLLBACK and a no-op.  The quantized cache is
+ * never touched.  Source: Pith review page, "What carries the argument"
+ * (rejected tokens dropped before quantization); "QuantSpec Guide",
+ * "Zero-Overhead Rollback". */
+qs_status qs_buffer_rollback(const qs_cache *c, const int32_t *d_n_drop, qs_stream_t stream);
+
+/* d_mask[b] = 1 if appending n_next more tokens would exceed 2G, else 0.
+ * d_mask: uint8 [B] device array.  Feed it to qs_quantize_flush. */
+qs_status qs_need_flush(const qs_cache *c, int32_t n_next, uint8_t *d_mask, qs_stream_t stream);
+
+/* Quantize-on-flush.  For every sequence with d_mask[b] != 0 (all when
+ * d_mask is NULL): quantize the oldest buffer half (logical tokens 0..G-1,
+ * which must be committed: fill - pending >= G) into group n_groups --
+ * keys per channel over the G tokens, values per token over the D channels,
+ * convention QS-RN-v1 -- then n_groups += 1, half_base ^= 1, fill -= G.
+ * Failing preconditions give QS_DEV_FLUSH_UNCOMMITTED or QS_DEV_CAPACITY and a
+ * no-op.  Source: Pith review page, "What carries the argument", Figure 7 and
+ * Appendix D; "QuantSpec Guide", "Periodic Group Quantization". */
+qs_status qs_quantize_flush(const qs_cache *c, const uint8_t *d_mask, qs_stream_t stream);
+
+/* Bytes of device workspace qs_attn_decode needs for n_q queries (1..8) on
+ * the current device.  Pure host function (reads device attributes). */
+qs_status qs_attn_workspace_size(const qs_cache *c, int32_t n_q, size_t *bytes);
+
+/* Split-KV decode attention over the quantized groups and the fp16 buffer.
+ *   q      fp16 [B][H][n_q][D] device, 1 <= n_q <= 8; query j of sequence b sits
+ *          at buffer position fill - n_q + j and sees every token at or before
+ *          it (all quantized tokens plus a causal prefix of the buffer);
+ *   mode   QS_DRAFT_UPPER4 (reads C_U planes only) or QS_VERIFY_INT8;
+ *   softmax_scale  multiplies q . k (usually 1/sqrt(D));
+ *   out    fp16 [B][H][n_q][D] device: softmax-weighted sum of the values;
+ *   lse    float [B][H][n_q] device or NULL: natural log of the softmax
+ *          denominator of the scaled scores;
+ *   workspace  device scratch of at least qs_attn_workspace_size bytes, 16-byte
+ *          aligned; it holds split partials and is not read across calls.
+ * Sequences with n_q > fill get QS_DEV_NQ_GT_FILL, zero output, lse = -inf.
+ * Kernels: a persistent split kernel over a balanced partition of all
+ * (sequence, head, group) units, then a log-sum-exp combine kernel.
+ * Sources: "QuantSpec Guide", "Hierarchical Two-Level Quantization with
+ * Bit-Sharing"; Pith review page, "What carries the argument" and Appendix E
+ * (Flash Decoding). */
+qs_status qs_attn_decode(const qs_cache *c, qs_mode mode, const uint16_t *q, int32_t n_q,
+                         float softmax_scale, uint16_t *out, float *lse, void *workspace,
+                         size_t workspace_bytes, qs_stream_t stream);
+
+/* Copy every sequence's error word to h_err (int32 [B], host memory) and
+ * clear them on the device.  Synchronizes the stream. */
+qs_status qs_get_errors(const qs_cache *c, int32_t *h_err, qs_stream_t stream);
+
+/* Human-readable name of a status code (static string). */
+const char *qs_status_string(qs_status s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* QS_H_ */

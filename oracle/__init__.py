@@ -206,3 +206,35 @@ class OracleCache:
         G = self.G
         idx = (s[HALF_BASE] * G + np.arange(s[FILL])) % (2 * G)
         return self.bk[b, h, idx], self.bv[b, h, idx]
+
+
+def prefill(oc, tokens, n_groups, fill):
+    """Bring an oracle cache to a starting state with the same sequence of
+    state-machine operations a device prefill uses: per group append G tokens,
+    commit (dropping them for sequences that already hold all their groups),
+    flush the sequences that still need groups; then append the buffer tokens
+    and commit each sequence's fill level.
+
+    ``tokens(b, t0, n)`` returns that sequence's keys and values for tokens
+    [t0, t0 + n) as fp16 arrays [H, n, D]."""
+    B, H, D, G = oc.B, oc.H, oc.D, oc.G
+    ng = np.asarray(n_groups)
+    fl = np.asarray(fill)
+    for g in range(int(ng.max(initial=0))):
+        k = np.zeros((B, H, G, D), np.float16)
+        v = np.zeros_like(k)
+        for b in range(B):
+            if g < ng[b]:
+                k[b], v[b] = tokens(b, g * G, G)
+        oc.append(k, v)
+        oc.rollback(np.where(g < ng, 0, G).astype(np.int32))
+        oc.flush((g < ng).astype(np.uint8))
+    fmax = int(fl.max(initial=0))
+    if fmax:
+        k = np.zeros((B, H, fmax, D), np.float16)
+        v = np.zeros_like(k)
+        for b in range(B):
+            if fl[b]:
+                k[b, :, :fl[b]], v[b, :, :fl[b]] = tokens(b, int(ng[b]) * G, int(fl[b]))
+        oc.append(k, v)
+        oc.rollback((fmax - fl).astype(np.int32))

@@ -1,0 +1,81 @@
+"""Test-side model of the device cache layout, written from include/qs.h.
+
+It converts the oracle's logical state (8-bit codes, scales, zeros, buffer,
+counters) to the byte layout the header specifies and back, so tests can
+compare device arrays bit for bit or load oracle state into a device cache.
+It shares no code with the CUDA library.
+"""
+import numpy as np
+
+import oracle
+
+
+def vperm(p):
+    """Token (within a 32-token quarter) stored at nibble position p of a
+    16-byte value row: 32u + 16((p>>1)&1) + 8(p&1) + 2(p>>3) + ((p>>2)&1)."""
+    p = np.asarray(p)
+    return 16 * ((p >> 1) & 1) + 8 * (p & 1) + 2 * (p >> 3) + ((p >> 2) & 1)
+
+
+def _nibbles_to_bytes(n):
+    return (n[..., 0::2] | (n[..., 1::2] << 4)).astype(np.uint8)
+
+
+def pack_k(kq):
+    """codes [..., G, D] -> (upper, lower) planes [..., G, D/2]."""
+    return _nibbles_to_bytes(kq >> 4), _nibbles_to_bytes(kq & 15)
+
+
+def pack_v(vq):
+    """codes [..., G tokens, D] -> planes [..., G/32, D, 16]."""
+    G, D = vq.shape[-2], vq.shape[-1]
+    tok = (32 * np.arange(G // 32)[:, None] + vperm(np.arange(32))[None, :])  # [4, 32]
+    perm = vq[..., tok, :]                    # [..., 4, 32, D]
+    perm = np.swapaxes(perm, -1, -2)          # [..., 4, D, 32]
+    return _nibbles_to_bytes(perm >> 4), _nibbles_to_bytes(perm & 15)
+
+
+def unpack_k(upper, lower):
+    u = np.stack([upper & 15, upper >> 4], -1).reshape(*upper.shape[:-1], -1)
+    l_ = np.stack([lower & 15, lower >> 4], -1).reshape(*lower.shape[:-1], -1)
+    return (u << 4 | l_).astype(np.uint8)
+
+
+def meta(ks, kz, vs, vz):
+    """fp16 bit arrays [..., 128] x4 -> [..., 4, 128] (rows: K scale, K zero,
+    V scale, V zero)."""
+    return np.stack([ks, kz, vs, vz], axis=-2).astype(np.uint16)
+
+
+def device_arrays(oc: oracle.OracleCache):
+    """The oracle state in the device layout (numpy)."""
+    ku, kl = pack_k(oc.kq)
+    vu, vl = pack_v(oc.vq)
+    return dict(k_upper=ku, k_lower=kl, v_upper=vu, v_lower=vl,
+                meta=meta(oc.ks, oc.kz, oc.vs, oc.vz),
+                buf_k=oc.bk, buf_v=oc.bv, state=oc.state)
+
+
+def load_into(cache, oc: oracle.OracleCache):
+    """Copy the oracle's state into a device cache (qs.Cache)."""
+    import torch
+    arrs = device_arrays(oc)
+    for name, a in arrs.items():
+        t = getattr(cache, name)
+        src = torch.from_numpy(np.ascontiguousarray(a))
+        if t.dtype == torch.float16:
+            src = src.view(torch.int16).view(torch.float16)
+        t.copy_(src.reshape(t.shape))
+
+
+def read_device(cache):
+    """Device cache arrays as numpy (fp16 as uint16 bits)."""
+    import torch
+    out = {}
+    for name in ("k_upper", "k_lower", "v_upper", "v_lower", "meta", "buf_k", "buf_v", "state"):
+        t = getattr(cache, name).detach().cpu()
+        if t.dtype == torch.float16:
+            t = t.view(torch.int16)
+        a = t.numpy()
+        out[name] = a.view(np.uint16) if a.dtype == np.int16 else a
+    return out

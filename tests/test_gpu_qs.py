@@ -1,0 +1,316 @@
+"""GPU parity: libqs (through the C ABI) against the CPU oracle.
+
+Bit-exact: codes (as packed planes), scales, zeros, buffer contents, counters
+and error words.  Attention outputs: max-abs <= 1e-2 and relative RMS <=
+2e-3 against the oracle's fp64 result on the same seeded inputs; the
+log-sum-exp within 5e-3 (bounded by the fp16 rounding of q * s_K, about
+2^-11 of sum_d |q_d k_d| * softmax_scale, far below this on these inputs).
+"""
+import numpy as np
+import pytest
+
+import oracle
+from hierarchical_quantized_kv_gb300 import driver, qs, synthetic
+from tests import layout
+
+pytestmark = pytest.mark.gpu
+
+ATOL, RRMS, LSE_TOL = 1e-2, 2e-3, 5e-3
+DRAFT, VERIFY = qs.QS_DRAFT_UPPER4, qs.QS_VERIFY_INT8
+
+
+@pytest.fixture(scope="module")
+def torch():
+    import torch as t
+    assert t.cuda.is_available(), "GPU tests need CUDA"
+    import __graft_entry__
+    __graft_entry__.build()
+    return t
+
+
+def h16(rng, shape, scale=1.0):
+    return (rng.standard_normal(shape) * scale).astype(np.float16)
+
+
+def to_dev(torch, a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def assert_state_equal(cache, oc, what=""):
+    got = layout.read_device(cache)
+    want = layout.device_arrays(oc)
+    for name in want:
+        g, w_ = got[name], want[name]
+        if name == "state":
+            w_ = w_.copy()
+            w_[:, oracle.ERR] = g[:, oracle.ERR]  # error words are compared separately
+        assert np.array_equal(g.reshape(w_.shape), w_), "%s: %s differs" % (what, name)
+
+
+def run_attn(torch, cache, mode, q, scale=None, lse=True):
+    B, H, n_q, D = q.shape
+    if scale is None:
+        scale = 1.0 / np.sqrt(D)
+    qd = to_dev(torch, q)
+    out = torch.full_like(qd, float("nan"))
+    l_ = torch.full((B, H, n_q), float("nan"), dtype=torch.float32, device="cuda") if lse else None
+    ws = torch.empty(qs.qs_attn_workspace_size(cache, n_q), dtype=torch.uint8, device="cuda")
+    qs.qs_attn_decode(cache, mode, qd, scale, out, l_, ws)
+    torch.cuda.synchronize()
+    return out.double().cpu().numpy(), (l_.double().cpu().numpy() if lse else None)
+
+
+def assert_close(got, ref, got_lse=None, ref_lse=None, what=""):
+    assert np.all(np.isfinite(got)), what
+    err = np.abs(got - ref).max()
+    rel = np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-30)
+    assert err <= ATOL and rel <= RRMS, "%s: max-abs %.3g rel-rms %.3g" % (what, err, rel)
+    if got_lse is not None:
+        fin = np.isfinite(ref_lse)
+        assert np.array_equal(np.isfinite(got_lse), fin), what
+        assert np.abs(got_lse[fin] - ref_lse[fin]).max() <= LSE_TOL, what
+    return err, rel
+
+
+# ---------------------------------------------------------- bookkeeping
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_buffer_and_flush_bit_exact(torch, seed):
+    """Random append / rollback / flush sequences, including failing
+    preconditions, give bit-identical device and oracle state."""
+    rng = np.random.default_rng(seed)
+    B, H, cap = 3, 4, 5
+    cache = qs.Cache(B, H, cap)
+    oc = oracle.OracleCache(B, H, 128, 128, cap)
+    qs.qs_state_reset(cache)
+    mask_d = torch.zeros(B, dtype=torch.uint8, device="cuda")
+    for step in range(260):
+        op = rng.random()
+        if op < 0.06:   # a flush with a random mask, may fail per sequence
+            m = rng.integers(0, 2, B).astype(np.uint8)
+            qs.qs_quantize_flush(cache, to_dev(torch, m))
+            oc.flush(m)
+        elif op < 0.08:  # rollback that may exceed the pending tokens
+            r = rng.integers(0, 8, B).astype(np.int32)
+            qs.qs_buffer_rollback(cache, to_dev(torch, r))
+            oc.rollback(r)
+        else:
+            qs.qs_need_flush(cache, 6, mask_d)
+            m = oc.need_flush(6)
+            assert np.array_equal(mask_d.cpu().numpy(), m)
+            qs.qs_quantize_flush(cache, mask_d)
+            oc.flush(m)
+            n = int(rng.integers(1, 7))
+            k, v = h16(rng, (B, H, n, 128), 3.0), h16(rng, (B, H, n, 128))
+            qs.qs_buffer_append(cache, to_dev(torch, k), to_dev(torch, v))
+            oc.append(k, v)
+            r = np.array([rng.integers(0, n + 1) for _ in range(B)], np.int32)
+            qs.qs_buffer_rollback(cache, to_dev(torch, r))
+            oc.rollback(r)
+        if step % 20 == 0 or step == 259:
+            assert_state_equal(cache, oc, "step %d" % step)
+            errs = qs.qs_get_errors(cache)
+            assert np.array_equal(errs, oc.state[:, oracle.ERR]), step
+            oc.state[:, oracle.ERR] = 0
+    assert oc.state[:, oracle.N_GROUPS].sum() >= 4
+
+
+def test_append_overflow_is_a_no_op(torch):
+    rng = np.random.default_rng(5)
+    cache = qs.Cache(2, 2, 2)
+    oc = oracle.OracleCache(2, 2, 128, 128, 2)
+    qs.qs_state_reset(cache)
+    k, v = h16(rng, (2, 2, 200, 128)), h16(rng, (2, 2, 200, 128))
+    for c in (cache,):
+        qs.qs_buffer_append(c, to_dev(torch, k), to_dev(torch, v))
+    oc.append(k, v)
+    qs.qs_buffer_append(cache, to_dev(torch, k[:, :, :57]), to_dev(torch, v[:, :, :57]))
+    oc.append(k[:, :, :57], v[:, :, :57])
+    assert_state_equal(cache, oc)
+    assert np.all(qs.qs_get_errors(cache) == qs.DEV_OVERFLOW)
+    assert np.all(qs.qs_get_errors(cache) == 0)  # read-back clears
+
+
+def test_host_argument_errors(torch):
+    cache = qs.Cache(1, 1, 1)
+    with pytest.raises(qs.QsError) as e:
+        qs.qs_buffer_append(cache, torch.zeros((1, 1, 0, 128), dtype=torch.float16, device="cuda"),
+                            torch.zeros((1, 1, 0, 128), dtype=torch.float16, device="cuda"))
+    assert e.value.status == qs.QS_ERR_ARG
+    q = torch.zeros((1, 1, 9, 128), dtype=torch.float16, device="cuda")
+    with pytest.raises(qs.QsError) as e:
+        qs.qs_attn_decode(cache, DRAFT, q, 0.1, torch.empty_like(q), None, None)
+    assert e.value.status == qs.QS_ERR_ARG
+    q = q[:, :, :2].contiguous()
+    with pytest.raises(qs.QsError) as e:
+        qs.qs_attn_decode(cache, DRAFT, q, 0.1, torch.empty_like(q), None, None)
+    assert e.value.status == qs.QS_ERR_WORKSPACE
+
+
+# ----------------------------------------------------------- tiny config
+
+def test_tiny_config_round(torch):
+    """The tiny workload: 768 quantized + 256 buffer tokens, 4 outlier key
+    channels x10.  Draft 1 query, verify 5 queries, flush one half, then a
+    5-token round that rolls back 3 rejected tokens; state bit-exact and
+    outputs within tolerance at every step."""
+    w = synthetic.tiny()
+    cache = qs.Cache(w.B, w.H, 8)
+    driver.prefill(cache, w)
+    oc = oracle.OracleCache(w.B, w.H, w.D, w.G, 8)
+    oracle.prefill(oc, lambda b, t0, n: synthetic.kv_tokens(w, b, t0, n), w.n_groups, w.fill)
+    assert_state_equal(cache, oc, "prefill")
+    assert oc.counters(0)["n_groups"] == 6 and oc.counters(0)["fill"] == 256
+
+    def both(mode, q, what):
+        got, gl = run_attn(torch, cache, mode, q)
+        ref, rl = oc.attn(q, upper_only=(mode == DRAFT))
+        assert_close(got, ref, gl, rl, what)
+
+    both(DRAFT, synthetic.queries(w, 0, 1), "draft")
+    both(VERIFY, synthetic.queries(w, 1, 5), "verify")
+    qs.qs_quantize_flush(cache)
+    oc.flush()
+    assert_state_equal(cache, oc, "flush")
+    k, v = synthetic.kv_tokens(w, 0, 1024, 5)
+    qs.qs_buffer_append(cache, to_dev(torch, k[None]), to_dev(torch, v[None]))
+    oc.append(k[None], v[None])
+    both(VERIFY, synthetic.queries(w, 2, 5), "verify after flush")
+    both(DRAFT, synthetic.queries(w, 3, 1), "draft with pending")
+    qs.qs_buffer_rollback(cache, to_dev(torch, np.array([3], np.int32)))
+    oc.rollback([3])
+    assert_state_equal(cache, oc, "rollback")
+    both(DRAFT, synthetic.queries(w, 4, 1), "draft after rollback")
+    both(VERIFY, synthetic.queries(w, 5, 2), "verify after rollback")
+    assert np.all(qs.qs_get_errors(cache) == 0)
+
+
+# ------------------------------------------- injected state, edge cases
+
+def _oracle_state(rng, B, H, n_groups, fill, cap, k_scale=2.0):
+    oc = oracle.OracleCache(B, H, 128, 128, cap)
+    toks = {}
+
+    def tokens(b, t0, n):
+        key = (b, t0, n)
+        if key not in toks:
+            r = np.random.default_rng([int(rng.integers(1 << 30)), b, t0])
+            k = (r.standard_normal((H, n, 128)) * k_scale)
+            k[:, :, :3] *= 8
+            toks[key] = (k.astype(np.float16), r.standard_normal((H, n, 128)).astype(np.float16))
+        return toks[key]
+
+    oracle.prefill(oc, tokens, n_groups, fill)
+    return oc
+
+
+@pytest.mark.parametrize("n_groups,fill", [(0, 1), (0, 8), (0, 31), (1, 32), (1, 33), (2, 64),
+                                           (3, 65), (0, 127), (2, 128), (1, 200), (5, 255),
+                                           (4, 256)])
+@pytest.mark.parametrize("n_q", [1, 2, 5, 8])
+def test_attn_edge_cases(torch, n_groups, fill, n_q):
+    if n_q > fill:
+        pytest.skip("n_q > fill is the error case")
+    rng = np.random.default_rng(1000 * n_groups + fill + 7 * n_q)
+    B, H = 2, 3
+    oc = _oracle_state(rng, B, H, [n_groups, n_groups], [fill, fill], cap=max(n_groups, 1))
+    cache = qs.Cache(B, H, max(n_groups, 1))
+    layout.load_into(cache, oc)
+    q = h16(rng, (B, H, n_q, 128))
+    for mode in (DRAFT, VERIFY):
+        got, gl = run_attn(torch, cache, mode, q)
+        ref, rl = oc.attn(q, upper_only=(mode == DRAFT))
+        assert_close(got, ref, gl, rl, "mode %d" % mode)
+
+
+def test_attn_ragged_small(torch):
+    rng = np.random.default_rng(77)
+    ng = [0, 5, 1, 3, 0, 2, 7]
+    fl = [3, 256, 1, 129, 64, 33, 200]
+    B, H = len(ng), 3
+    oc = _oracle_state(rng, B, H, ng, fl, cap=8)
+    cache = qs.Cache(B, H, 8)
+    layout.load_into(cache, oc)
+    for n_q in (1, 3):
+        q = h16(rng, (B, H, n_q, 128))
+        for mode in (DRAFT, VERIFY):
+            got, gl = run_attn(torch, cache, mode, q)
+            ref, rl = oc.attn(q, upper_only=(mode == DRAFT))
+            assert_close(got, ref, gl, rl, "n_q %d mode %d" % (n_q, mode))
+    assert np.all(qs.qs_get_errors(cache) == 0)
+
+
+def test_attn_nq_greater_than_fill(torch):
+    rng = np.random.default_rng(3)
+    oc = _oracle_state(rng, 3, 2, [2, 0, 1], [4, 2, 40], cap=2)
+    cache = qs.Cache(3, 2, 2)
+    layout.load_into(cache, oc)
+    q = h16(rng, (3, 2, 3, 128))
+    got, gl = run_attn(torch, cache, VERIFY, q)
+    ref, rl = oc.attn(q, upper_only=False)
+    assert np.all(got[1] == 0) and np.all(np.isneginf(gl[1]))
+    assert_close(got, ref, gl, rl)
+    errs = qs.qs_get_errors(cache)
+    assert errs.tolist() == [0, qs.DEV_NQ_GT_FILL, 0]
+
+
+def test_draft_equals_verify_when_lower_is_eight(torch):
+    """Crafted codes with every C_L = 8: draft and verify must agree (the
+    oracle pins this exactly; on the device both take the same inputs to
+    the same kernels up to the code extraction)."""
+    rng = np.random.default_rng(9)
+    oc = _oracle_state(rng, 1, 2, [3], [20], cap=3)
+    oc.kq[:] = (oc.kq & 0xF0) | 8
+    oc.vq[:] = (oc.vq & 0xF0) | 8
+    cache = qs.Cache(1, 2, 3)
+    layout.load_into(cache, oc)
+    q = h16(rng, (1, 2, 4, 128))
+    gd, _ = run_attn(torch, cache, DRAFT, q)
+    gv, _ = run_attn(torch, cache, VERIFY, q)
+    ref, _ = oc.attn(q, upper_only=False)
+    assert_close(gd, ref)
+    assert_close(gv, ref)
+    assert np.abs(gd - gv).max() < 2e-3
+
+
+# ------------------------------------------------------------ full sizes
+
+def _sampled_oracle(w, bs, hs):
+    cap = max(w.n_groups[b] for b in bs) + 1
+    oc = oracle.OracleCache(len(bs), len(hs), w.D, w.G, cap)
+
+    def tokens(i, t0, n):
+        k, v = synthetic.kv_tokens(w, bs[i], t0, n)
+        return k[hs], v[hs]
+
+    oracle.prefill(oc, tokens, [w.n_groups[b] for b in bs], [w.fill[b] for b in bs])
+    return oc
+
+
+@pytest.mark.parametrize("cfg,bs,hs", [
+    ("32k", [0], list(range(32))),
+    ("128k", [0], [0, 7, 19, 31]),
+    ("batched32k", [0, 5, 7], [1, 30]),
+    ("ragged", [0, 3, 9, 15], [2, 17]),
+])
+def test_full_size_sampled(torch, cfg, bs, hs):
+    """Full-size workloads in the launch configuration the benchmark times;
+    the oracle recomputes the sampled (sequence, head) pairs."""
+    w = synthetic.CONFIGS[cfg]()
+    cap = max(w.n_groups) + 1
+    cache = qs.Cache(w.B, w.H, cap)
+    driver.prefill(cache, w)
+    oc = _sampled_oracle(w, bs, hs)
+    # quantized planes of the sampled heads, bit for bit
+    dev = layout.read_device(cache)
+    want = layout.device_arrays(oc)
+    for name in ("k_upper", "k_lower", "v_upper", "v_lower", "meta"):
+        g = dev[name][np.ix_(bs, hs)]
+        assert np.array_equal(g[:, :, :oc.cap], want[name]), name
+    assert np.array_equal(dev["state"][bs, :5], want["state"][:, :5])
+    for call, (mode, n_q) in enumerate(((DRAFT, 1), (VERIFY, 5))):
+        q = synthetic.queries(w, call, n_q)
+        got, gl = run_attn(torch, cache, mode, q)
+        ref, rl = oc.attn(np.ascontiguousarray(q[np.ix_(bs, hs)]), upper_only=(mode == DRAFT))
+        assert_close(got[np.ix_(bs, hs)], ref, gl[np.ix_(bs, hs)], rl, "%s mode %d" % (cfg, mode))
+    assert np.all(qs.qs_get_errors(cache) == 0)
