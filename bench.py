@@ -1,0 +1,502 @@
+"""Benchmark: QuantSpec decode attention over the hierarchical quantized KV
+cache on one GB300 (replicas over N GPUs, no collective on the data path).
+
+One step = one speculative round (gamma = 4) of the whole hot path on the
+Llama-2-7B-shaped 32k workload (batch 1, 32 heads, head_dim 128, G = 128,
+starting at 254 quantized groups + a full 256-token fp16 buffer = 32,768
+tokens):
+    need_flush + quantize-on-flush (128 tokens x 32 heads),
+    4 x (append 1 draft token + draft decode attention, 1 query, C_U only),
+    rollback of the 4 draft tokens, append 5 target tokens,
+    verify decode attention (5 queries, INT8), rollback of 4 - a (a seeded),
+then the counters are restored to the starting state (a device copy) so every
+step does the same work.  ``value`` is algorithmic bytes per step / step time
+(GB/s), summed over ranks.
+
+Per-call numbers (draft_us, verify_us, flush_us and the roofline object) time
+one call at a time with the L2 flushed (256 MB write) before each call.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode-attn µs/step & HBM GB/s (draft 4-bit / verify 8-bit) at 32k ctx"
+GAMMA = 4
+KB = 1024
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ---------------------------------------------------------------- bytes
+
+def attn_bytes(ng, fill, n_q, mode_draft, BH):
+    """Algorithmic bytes of one decode-attention call per the method: the
+    quantized planes it must read (draft: C_U + scales/zeros = 136 B per
+    token-head; verify: C_U + C_L + scales/zeros = 264 B), the fp16 buffer
+    tokens (512 B each), the queries and the outputs."""
+    grp = (8 * KB + 8 * KB + KB) if mode_draft else (4 * 8 * KB + KB)
+    return BH * (ng * grp + fill * 512 + n_q * 256 * 2)
+
+
+FLUSH_BYTES_PER_HEAD = 2 * 128 * 256 + 4 * 8 * KB + KB   # read both halves' rows, write planes + meta
+
+
+def append_bytes(n, BH):
+    return BH * n * 512 * 2
+
+
+# --------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples (100 ms) with host timestamps; read the ones that
+    fall inside the timed window."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.samples = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 7:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        inside = [p for (t, p) in self.samples if t0 <= t <= t1]
+        note = "inside timed region"
+        if not inside and self.samples:  # very short region: nearest samples after it started
+            inside = [p for (t, p) in self.samples if t >= t0][:3]
+            note = "timed region shorter than the sampling period; nearest samples"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(p[0]) for p in inside if num(p[0]) is not None]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for p in inside:
+            for n, v in zip(names, p[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": num(inside[0][1]), "reasons": sorted(reasons),
+                "power_w_max": max((num(p[2]) or 0) for p in inside),
+                "samples": len(inside), "note": note}
+
+
+# ------------------------------------------------------------ native arm
+
+class Round:
+    """Device state and inputs of the benchmark step on one GPU."""
+
+    def __init__(self, torch, w, seed):
+        from hierarchical_quantized_kv_gb300 import driver, qs, synthetic
+        self.torch, self.qs, self.w = torch, qs, w
+        dev = torch.device("cuda")
+        B, H, D = w.B, w.H, w.D
+        self.cache = qs.Cache(B, H, max(w.n_groups) + 2)
+        driver.prefill(self.cache, w)
+        torch.cuda.synchronize()
+        self.state0 = self.cache.state.clone()
+        rng = np.random.default_rng([seed, 77])
+        f16 = lambda *s: torch.from_numpy(rng.standard_normal(s).astype(np.float16)).to(dev)
+        self.kd = [f16(B, H, 1, D) for _ in range(GAMMA)]
+        self.vd = [f16(B, H, 1, D) for _ in range(GAMMA)]
+        self.kt, self.vt = f16(B, H, GAMMA + 1, D), f16(B, H, GAMMA + 1, D)
+        self.qd = [torch.from_numpy(synthetic.queries(w, i, 1)).to(dev) for i in range(GAMMA)]
+        self.qv = torch.from_numpy(synthetic.queries(w, GAMMA, GAMMA + 1)).to(dev)
+        self.od = [torch.empty_like(q) for q in self.qd]
+        self.ov = torch.empty_like(self.qv)
+        self.lse = torch.empty((B, H, GAMMA + 1), dtype=torch.float32, device=dev)
+        n_ws = max(qs.qs_attn_workspace_size(self.cache, 1), qs.qs_attn_workspace_size(self.cache, GAMMA + 1))
+        self.ws = torch.empty(n_ws, dtype=torch.uint8, device=dev)
+        self.mask = torch.zeros(B, dtype=torch.uint8, device=dev)
+        self.drop_draft = torch.full((B,), GAMMA, dtype=torch.int32, device=dev)
+        self.drops = [torch.from_numpy(GAMMA - synthetic.accepted_counts(w, s)).to(dev) for s in range(16)]
+        self.scale = 1.0 / np.sqrt(D)
+        # state after the step's flush: one more group, half the buffer
+        ng0, f0 = int(self.state0[0, 0]), int(self.state0[0, 1])
+        self.ng1, self.f1 = ng0 + 1, f0 - w.G
+        BH = B * H
+        self.bytes = {
+            "flush": FLUSH_BYTES_PER_HEAD * BH,
+            "draft": [attn_bytes(self.ng1, self.f1 + i + 1, 1, True, BH) for i in range(GAMMA)],
+            "verify": attn_bytes(self.ng1, self.f1 + GAMMA + 1, GAMMA + 1, False, BH),
+            "append": append_bytes(GAMMA, BH) + append_bytes(GAMMA + 1, BH),
+        }
+        self.step_bytes = (self.bytes["flush"] + sum(self.bytes["draft"]) + self.bytes["verify"]
+                           + self.bytes["append"])
+        self.launches_per_step = 2 + GAMMA * 3 + 1 + 1 + 2 + 1
+
+    def step(self, s, host=None):
+        qs, c = self.qs, self.cache
+        if host is not None:
+            host.h2d(self)
+        qs.qs_need_flush(c, GAMMA + 1, self.mask)
+        qs.qs_quantize_flush(c, self.mask)
+        for i in range(GAMMA):
+            qs.qs_buffer_append(c, self.kd[i], self.vd[i])
+            qs.qs_attn_decode(c, qs.QS_DRAFT_UPPER4, self.qd[i], self.scale, self.od[i], None, self.ws)
+        qs.qs_buffer_rollback(c, self.drop_draft)
+        qs.qs_buffer_append(c, self.kt, self.vt)
+        qs.qs_attn_decode(c, qs.QS_VERIFY_INT8, self.qv, self.scale, self.ov, self.lse, self.ws)
+        qs.qs_buffer_rollback(c, self.drops[s % len(self.drops)])
+        c.state.copy_(self.state0)
+        if host is not None:
+            host.d2h(self)
+
+    # states for single-call timing
+    def set_state(self, ng, fill):
+        st = self.state0.clone()
+        st[:, 0], st[:, 1], st[:, 2] = ng, fill, 0
+        self.cache.state.copy_(st)
+
+
+class HostIO:
+    """Pinned host buffers for the end-to-end number: every step copies its
+    inputs host -> device and its outputs device -> host."""
+
+    def __init__(self, torch, r):
+        pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t.cpu())
+        self.ins = [(pin(t), t) for t in r.kd + r.vd + [r.kt, r.vt] + r.qd + [r.qv]]
+        self.outs = [(t, torch.empty(t.shape, dtype=t.dtype, pin_memory=True)) for t in r.od + [r.ov, r.lse]]
+        self.h2d_bytes = sum(h.numel() * h.element_size() for h, _ in self.ins)
+        self.d2h_bytes = sum(h.numel() * h.element_size() for _, h in self.outs)
+
+    def h2d(self, r):
+        for h, d in self.ins:
+            d.copy_(h, non_blocking=True)
+
+    def d2h(self, r):
+        for d, h in self.outs:
+            h.copy_(d, non_blocking=True)
+
+
+def time_calls(torch, fn, setup, iters, l2_scratch):
+    """Mean device time of fn() over iters calls, L2 flushed before each."""
+    ts = []
+    for _ in range(iters):
+        setup()
+        l2_scratch.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        b.synchronize()
+        ts.append(a.elapsed_time(b) * 1e3)  # us
+    return statistics.mean(ts[1:]) if len(ts) > 1 else ts[0]
+
+
+def native(args):
+    import torch
+    import torch.distributed as dist
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    import __graft_entry__
+    if rank == 0 or world == 1:
+        __graft_entry__.build()
+    if world > 1:
+        dist.barrier()
+    from hierarchical_quantized_kv_gb300 import qs, synthetic
+    w = synthetic.CONFIGS[args.config](seed=rank)
+    r = Round(torch, w, seed=rank)
+    peak, peak_kind = load_peaks()
+
+    for s in range(args.warmup):
+        r.step(s)
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local)
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.time()
+    ev0.record()
+    for s in range(args.steps):
+        r.step(s)
+    ev1.record()
+    torch.cuda.synchronize()
+    t1 = time.time()
+    if world > 1:
+        dist.barrier()
+    sampler.stop()
+    ms = ev0.elapsed_time(ev1) / args.steps
+    clocks = sampler.summary(t0, t1)
+    if world > 1:
+        tt = torch.tensor([ms], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+
+    # per-call timing with L2 flushed (draft, verify, flush)
+    l2 = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    it = args.call_iters
+    draft_us = time_calls(torch, lambda: qs.qs_attn_decode(r.cache, qs.QS_DRAFT_UPPER4, r.qd[0], r.scale,
+                                                           r.od[0], None, r.ws),
+                          lambda: r.set_state(r.ng1, r.f1 + 1), it, l2)
+    verify_us = time_calls(torch, lambda: qs.qs_attn_decode(r.cache, qs.QS_VERIFY_INT8, r.qv, r.scale,
+                                                            r.ov, r.lse, r.ws),
+                           lambda: r.set_state(r.ng1, r.f1 + GAMMA + 1), it, l2)
+    flush_us = time_calls(torch, lambda: qs.qs_quantize_flush(r.cache, None),
+                          lambda: r.cache.state.copy_(r.state0), it, l2)
+    r.cache.state.copy_(r.state0)
+    draft_b, verify_b = r.bytes["draft"][0], r.bytes["verify"]
+    draft_gbs, verify_gbs = draft_b / draft_us / 1e3, verify_b / verify_us / 1e3
+    # dominant kernel by device time within a step
+    dominant = ("draft", draft_gbs, GAMMA * draft_us) if GAMMA * draft_us >= verify_us else \
+        ("verify", verify_gbs, verify_us)
+
+    # end to end through host buffers
+    host = HostIO(torch, r)
+    for s in range(3):
+        r.step(s, host)
+        torch.cuda.current_stream().synchronize()
+    e_steps = max(1, min(args.steps, 200))
+    te0 = time.perf_counter()
+    for s in range(e_steps):
+        r.step(s, host)
+        torch.cuda.current_stream().synchronize()  # the host reads the step's result
+    e2e_ms = (time.perf_counter() - te0) * 1e3 / e_steps
+    if world > 1:
+        tt = torch.tensor([e2e_ms], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+
+    errs = qs.qs_get_errors(r.cache)
+    assert np.all(errs == 0), errs
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, budget_s=args.cpu_budget)
+    if world > 1:
+        dist.destroy_process_group()
+    if rank != 0:
+        return
+    gbs = r.step_bytes * world / (ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": round(gbs, 1), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+        "us_per_step": round(ms * 1e3, 2), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16xf16->f32 (u4 / u8 codes)", "data": "synthetic",
+        "config": {"workload": w.name + " speculative round (gamma=4: flush, 4x(append 1 + draft 1q), "
+                               "rollback 4, append 5, verify 5q, rollback 4-a)",
+                   "B": w.B, "H": w.H, "D": w.D, "G": w.G, "context": w.context[0],
+                   "quantized_groups_at_attention": r.ng1, "bytes_per_step": r.step_bytes,
+                   "l2": "step: inputs larger than L2 (%.0f MB of planes per step); per-call numbers: "
+                         "256 MB L2 flush before each call" % (r.step_bytes / 1e6),
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "draft_us": round(draft_us, 2), "draft_gbs": round(draft_gbs, 1),
+        "verify_us": round(verify_us, 2), "verify_gbs": round(verify_gbs, 1),
+        "flush_us": round(flush_us, 2),
+        "roofline": {"bound": "hbm", "kernel": "qs_attn_decode %s (split + combine launch)" % dominant[0],
+                     "achieved": round(dominant[1], 1), "peak": peak,
+                     "peak_kind": "%s hbm_gbs (copy, burst)" % peak_kind, "unit": "GB/s",
+                     "frac": round(dominant[1] / peak, 4), "traffic": None},
+        "e2e": {"value": round(r.step_bytes * world / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": host.h2d_bytes,
+                "d2h_bytes_per_step": host.d2h_bytes},
+        "gpu_launches": r.launches_per_step * args.steps,
+        "clocks": clocks,
+    }
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------- CPU oracle arm
+
+def cpu_sample(w, heads):
+    """Oracle state for a sample of heads of sequence 0 at the step's start."""
+    import oracle
+    from hierarchical_quantized_kv_gb300 import synthetic
+    oc = oracle.OracleCache(1, len(heads), w.D, w.G, w.n_groups[0] + 2)
+
+    def tokens(b, t0, n):
+        k, v = synthetic.kv_tokens(w, 0, t0, n)
+        return k[heads], v[heads]
+
+    oracle.prefill(oc, tokens, [w.n_groups[0]], [w.fill[0]])
+    return oc
+
+
+def cpu_step(oc, w, s, rng):
+    """The benchmark step's work on the oracle (all of it, on the sampled heads)."""
+    from hierarchical_quantized_kv_gb300 import synthetic
+    H, D = oc.H, w.D
+    saved = [a.copy() for a in (oc.kq, oc.vq, oc.ks, oc.kz, oc.vs, oc.vz, oc.bk, oc.bv, oc.state)]
+    oc.flush(oc.need_flush(GAMMA + 1))
+    for i in range(GAMMA):
+        k = rng.standard_normal((1, H, 1, D)).astype(np.float16)
+        oc.append(k, k)
+        oc.attn(rng.standard_normal((1, H, 1, D)).astype(np.float16), upper_only=True)
+    oc.rollback([GAMMA])
+    k = rng.standard_normal((1, H, GAMMA + 1, D)).astype(np.float16)
+    oc.append(k, k)
+    oc.attn(rng.standard_normal((1, H, GAMMA + 1, D)).astype(np.float16), upper_only=False)
+    oc.rollback([GAMMA - int(synthetic.accepted_counts(w, s)[0])])
+    for a, b in zip((oc.kq, oc.vq, oc.ks, oc.kz, oc.vs, oc.vz, oc.bk, oc.bv, oc.state), saved):
+        a[:] = b
+
+
+def cpu_baseline(w, budget_s=15.0, heads=(0, 1, 2, 3)):
+    import oracle
+    heads = list(heads)
+    oc = cpu_sample(w, heads)
+    rng = np.random.default_rng(5)
+    BH = len(heads)
+    ng1, f1 = w.n_groups[0] + 1, w.fill[0] - w.G
+    step_bytes = (FLUSH_BYTES_PER_HEAD * BH
+                  + sum(attn_bytes(ng1, f1 + i + 1, 1, True, BH) for i in range(GAMMA))
+                  + attn_bytes(ng1, f1 + GAMMA + 1, GAMMA + 1, False, BH)
+                  + append_bytes(GAMMA, BH) + append_bytes(GAMMA + 1, BH))
+    n, t0 = 0, time.perf_counter()
+    while True:
+        cpu_step(oc, w, n, rng)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or n >= 20:
+            break
+    return {"value": round(step_bytes * n / el / 1e9, 4), "unit": "GB/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": "%d benchmark steps on %d of %d heads (sequence 0), %.1f s; fp64 attention"
+                      % (n, BH, w.H, el),
+            "s_per_step_sample": round(el / n, 4)}
+
+
+def reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    from hierarchical_quantized_kv_gb300 import synthetic
+    oracle.build.build()
+    w = synthetic.CONFIGS[args.config]()
+    heads = [0, 1]
+    oc = cpu_sample(w, heads)
+    rng = np.random.default_rng(5)
+    BH = len(heads)
+    ng1, f1 = w.n_groups[0] + 1, w.fill[0] - w.G
+    step_bytes = (FLUSH_BYTES_PER_HEAD * BH
+                  + sum(attn_bytes(ng1, f1 + i + 1, 1, True, BH) for i in range(GAMMA))
+                  + attn_bytes(ng1, f1 + GAMMA + 1, GAMMA + 1, False, BH)
+                  + append_bytes(GAMMA, BH) + append_bytes(GAMMA + 1, BH))
+    for s in range(args.warmup):
+        cpu_step(oc, w, s, rng)
+    t0 = time.perf_counter()
+    for s in range(args.steps):
+        cpu_step(oc, w, s, rng)
+    el = time.perf_counter() - t0
+    ms = el * 1e3 / args.steps
+    val = round(step_bytes / (ms * 1e-3) / 1e9, 4)
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": w.name + " speculative round (gamma=4), bounded CPU sample",
+                       "B": w.B, "H": w.H, "D": w.D, "G": w.G, "context": w.context[0],
+                       "sample_heads": BH},
+            "cpu_baseline": {"value": val, "unit": "GB/s", "cores": oracle.num_threads(),
+                             "kind": "oracle",
+                             "sample": "each step: the full step's work on %d of %d heads" % (BH, w.H)},
+            "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def profile(args):
+    """A short run for ncu: set up the workload, then ``--profile-calls``
+    calls of one kind (draft | verify | flush | step) and nothing else."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    from hierarchical_quantized_kv_gb300 import qs, synthetic
+    w = synthetic.CONFIGS[args.config]()
+    r = Round(torch, w, seed=0)
+    for i in range(args.profile_calls):
+        if args.profile == "draft":
+            r.set_state(r.ng1, r.f1 + 1)
+            qs.qs_attn_decode(r.cache, qs.QS_DRAFT_UPPER4, r.qd[0], r.scale, r.od[0], None, r.ws)
+        elif args.profile == "verify":
+            r.set_state(r.ng1, r.f1 + GAMMA + 1)
+            qs.qs_attn_decode(r.cache, qs.QS_VERIFY_INT8, r.qv, r.scale, r.ov, r.lse, r.ws)
+        elif args.profile == "flush":
+            r.cache.state.copy_(r.state0)
+            qs.qs_quantize_flush(r.cache, None)
+        else:
+            r.step(i)
+    torch.cuda.synchronize()
+    assert np.all(qs.qs_get_errors(r.cache) == 0)
+    print("profile run ok: %d %s calls on %s" % (args.profile_calls, args.profile, w.name))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--config", default="32k")
+    ap.add_argument("--call-iters", type=int, default=30)
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", choices=["draft", "verify", "flush", "step"])
+    ap.add_argument("--profile-calls", type=int, default=3)
+    args = ap.parse_args()
+    if args.profile:
+        profile(args)
+    elif args.impl == "reference":
+        if args.steps > 20:  # each oracle step is a bounded CPU sample (about a second)
+            args.steps = 20
+        args.warmup = min(args.warmup, 3)
+        reference(args)
+    else:
+        native(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -15,11 +15,13 @@
 //    head) segments are laid end to end as units (a quantized group of 128
 //    tokens, or a chunk of fp16 buffer tokens) and every CTA takes an equal
 //    contiguous range, so ragged batches balance without a host round trip.
-//  * Warp 4 is the producer: for each unit it issues bulk async copies
-//    (cp.async.bulk, TMA engine) of the unit's contiguous plane blocks into a
-//    ring of shared-memory stages guarded by mbarriers.  Draft units copy only
-//    the C_U planes (8 KB keys + 8 KB values + 1 KB scales/zeros).
-//  * Warps 0-3 are consumers, each on 32 tokens of a group: nibbles become
+//  * Each unit's contiguous plane blocks arrive by bulk async copies
+//    (cp.async.bulk, TMA engine) in a ring of shared-memory stages guarded by
+//    mbarriers; draft units copy only the C_U planes (8 KB keys + 8 KB values
+//    + 1 KB scales/zeros).  There is no producer warp: the last warp to finish
+//    with a stage (a shared-memory arrival counter) issues its refill, so all
+//    four warps compute and three CTAs fit on an SM.
+//  * The four warps each take 32 tokens of a group: nibbles become
 //    exact fp16 integers in registers (bit tricks, no conversion
 //    instructions), and the dense contractions q.K^T and P.V run on
 //    m16n8k16 tensor-core MMAs with fp32 accumulation.  Scales are folded:
@@ -35,7 +37,8 @@ namespace qs {
 namespace {
 
 constexpr int kConsumers = 4;
-constexpr int kThreads = (kConsumers + 1) * 32;
+constexpr int kThreads = kConsumers * 32;
+constexpr int kCtasPerSm = 3;
 constexpr int kTailRow = 272;  // padded fp16 row stride (bytes) of buffer tiles
 constexpr int kOffKU = 0, kOffVU = 8192, kOffMeta = 16384, kOffKL = 17408, kOffVL = 25600;
 
@@ -45,13 +48,13 @@ template <>
 struct Cfg<QS_DRAFT_UPPER4> {
   static constexpr int kGroupBytes = 8192 + 8192 + 1024;
   static constexpr int kTailTok = 32;
-  static constexpr int kStages = 6;
+  static constexpr int kStages = 4;
 };
 template <>
 struct Cfg<QS_VERIFY_INT8> {
   static constexpr int kGroupBytes = 4 * 8192 + 1024;
   static constexpr int kTailTok = 64;
-  static constexpr int kStages = 3;
+  static constexpr int kStages = 2;
 };
 
 template <int MODE>
@@ -59,8 +62,9 @@ struct Layout {
   static constexpr int kTailBytes = Cfg<MODE>::kTailTok * kTailRow * 2;
   static constexpr int kStageBytes =
       Cfg<MODE>::kGroupBytes > kTailBytes ? Cfg<MODE>::kGroupBytes : kTailBytes;
-  static constexpr int kBarOff = Cfg<MODE>::kStages * kStageBytes;
-  static constexpr int kZeroOff = kBarOff + 2 * Cfg<MODE>::kStages * 8;
+  static constexpr int kBarOff = Cfg<MODE>::kStages * kStageBytes;   // full barriers
+  static constexpr int kCntOff = kBarOff + 8 * Cfg<MODE>::kStages;    // release counters
+  static constexpr int kZeroOff = kCntOff + 16 * Cfg<MODE>::kStages;
   static constexpr int kTabOff = kZeroOff + 32;
   // per-sequence tables: n_groups, fill, half_base, segment length, base unit
   static constexpr int kSmemBytes = kTabOff + 5 * kMaxB * 4;
@@ -73,7 +77,7 @@ struct Params {
   float *lse;
   float *ws;
   int n_q;
-  int P;  // split-kernel grid size (number of contiguous unit ranges)
+  int P;      // split-kernel grid size (number of contiguous unit ranges)
   float sl2;  // softmax_scale * log2(e)
 };
 
@@ -155,25 +159,38 @@ struct Cursor {
   }
 };
 
-// ---- nibble / byte planes -> exact fp16 integers (one half2 per pair) -----
-// Pair p of a 32-bit word holds elements (p, p + 4) of its 8 nibbles; draft
-// returns 16 * C_U, verify the 8-bit code 16 * C_U + C_L.
+// ---- nibble / byte planes -> exact centred fp16 integers (half2 per pair) -
+// Pair p of a 32-bit word holds elements (p, p + 4) of its 8 nibbles.  Draft
+// returns 16 C_U - 128, verify the 8-bit code minus 128, C_INT8 - 128 =
+// 16 C_U + C_L - 128.  Centring keeps s * code close to k - (z + 128 s), the
+// middle of the group's range, so the fp16 rounding of q * s and p * s_V acts
+// on values of the size of the data instead of their distance to the group
+// minimum; the 128 s (draft: 136 s, the midpoint 8 included) goes into the
+// zero-point bias, computed in fp32.  Every subtraction below is exact.
 __device__ __forceinline__ void pairs_upper(uint32_t w, uint32_t (&e)[4]) {
   const uint32_t w8 = w >> 8;
-  e[0] = hsub2_u32((w & 0x000F000Fu) | 0x74007400u, 0x74007400u);
-  e[1] = hsub2_u32((w & 0x00F000F0u) | 0x64006400u, 0x64006400u);
-  e[2] = hsub2_u32((w8 & 0x000F000Fu) | 0x74007400u, 0x74007400u);
-  e[3] = hsub2_u32((w8 & 0x00F000F0u) | 0x64006400u, 0x64006400u);
+  // bits 0-3 under exponent 2^14: 16384 + 16 n; bits 4-7 under 2^10: 1024 + 16 n
+  e[0] = hsub2_u32((w & 0x000F000Fu) | 0x74007400u, 0x74087408u);   // - 16512
+  e[1] = hsub2_u32((w & 0x00F000F0u) | 0x64006400u, 0x64806480u);   // - 1152
+  e[2] = hsub2_u32((w8 & 0x000F000Fu) | 0x74007400u, 0x74087408u);
+  e[3] = hsub2_u32((w8 & 0x00F000F0u) | 0x64006400u, 0x64806480u);
 }
 
 __device__ __forceinline__ void pairs_int8(uint32_t wu, uint32_t wl, uint32_t (&e)[4]) {
   const uint32_t ev = (wl & 0x0F0F0F0Fu) | ((wu << 4) & 0xF0F0F0F0u);  // codes 0,2,4,6
   const uint32_t od = ((wl >> 4) & 0x0F0F0F0Fu) | (wu & 0xF0F0F0F0u);  // codes 1,3,5,7
-  e[0] = hsub2_u32(prmt(ev, 0x64646464u, 0x4240), 0x64006400u);
-  e[1] = hsub2_u32(prmt(od, 0x64646464u, 0x4240), 0x64006400u);
-  e[2] = hsub2_u32(prmt(ev, 0x64646464u, 0x4341), 0x64006400u);
-  e[3] = hsub2_u32(prmt(od, 0x64646464u, 0x4341), 0x64006400u);
+  // byte c under 0x64: 1024 + c, minus 1152
+  e[0] = hsub2_u32(prmt(ev, 0x64646464u, 0x4240), 0x64806480u);
+  e[1] = hsub2_u32(prmt(od, 0x64646464u, 0x4240), 0x64806480u);
+  e[2] = hsub2_u32(prmt(ev, 0x64646464u, 0x4341), 0x64806480u);
+  e[3] = hsub2_u32(prmt(od, 0x64646464u, 0x4341), 0x64806480u);
 }
+
+// Offset, in units of the scale, that centring moves into the zero-point term.
+template <int MODE>
+struct Centre {
+  static constexpr float kOff = (MODE == QS_DRAFT_UPPER4) ? 136.f : 128.f;
+};
 
 template <int MODE>
 __device__ __forceinline__ void pairs(uint32_t wu, uint32_t wl, uint32_t (&e)[4]) {
@@ -193,12 +210,13 @@ __device__ __forceinline__ uint4 lds128(uint32_t a) {
                : "r"(a));
   return v;
 }
-__device__ __forceinline__ uint16_t lds16(uint32_t a) {
-  uint16_t v;
-  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
-  return v;
-}
-__device__ __forceinline__ float h2f(uint16_t b) { return __half2float(__ushort_as_half(b)); }
+
+// Probabilities are taken as 2^(s - m + kExpShift): values up to 64 keep p * s_V
+// in the normal fp16 range for the tensor-core operand (far-down tokens of a
+// long, diffuse context would otherwise round as fp16 subnormals) while any
+// finite fp16 value scale (< 2^10) stays below the fp16 maximum.  The shift
+// cancels in O / l; partials store m - kExpShift.
+constexpr float kExpShift = 6.f;
 
 // Per-warp online-softmax state for its two queries (columns 2c, 2c+1).
 struct Softmax {
@@ -216,9 +234,10 @@ struct Softmax {
   // returns the offset to subtract (0 when nothing is visible yet).
   __device__ void update(float g0, float g1, float &u0, float &u1) {
     const float n0 = fmaxf(m[0], g0), n1 = fmaxf(m[1], g1);
-    u0 = (n0 == -INFINITY) ? 0.f : n0;
-    u1 = (n1 == -INFINITY) ? 0.f : n1;
-    const float a0 = fast_exp2(m[0] - u0), a1 = fast_exp2(m[1] - u1);
+    const float a0 = (n0 == -INFINITY) ? 1.f : fast_exp2(m[0] - n0);
+    const float a1 = (n1 == -INFINITY) ? 1.f : fast_exp2(m[1] - n1);
+    u0 = (n0 == -INFINITY) ? 0.f : n0 - kExpShift;
+    u1 = (n1 == -INFINITY) ? 0.f : n1 - kExpShift;
     m[0] = n0;
     m[1] = n1;
     if (a0 != 1.f || a1 != 1.f) {
@@ -261,29 +280,71 @@ __device__ __forceinline__ void load_q_pairs(const uint16_t *qrow, bool valid, i
 }
 
 // ------------------------------------------------------------ split kernel
+
+// Issue the bulk copies of one unit into a stage (called by one whole warp).
 template <int MODE>
-__global__ void __launch_bounds__(kThreads, 2) split_kernel(const Params prm) {
+__device__ __forceinline__ void issue_unit(const qs_cache &c, const Tables &T, const Cursor &cu,
+                                           uint32_t dst, uint32_t bar, int lane) {
+  using C = Cfg<MODE>;
+  constexpr int TT = C::kTailTok;
+  const size_t bh = (size_t)cu.b * c.H + cu.h;
+  const int ng = T.ng[cu.b];
+  if (cu.u < ng) {
+    if (lane == 0) {
+      const size_t grp = bh * c.cap_groups + cu.u;
+      mbar_arrive_expect_tx(bar, C::kGroupBytes);
+      bulk_g2s(dst + kOffKU, c.k_upper + grp * 8192, 8192, bar);
+      bulk_g2s(dst + kOffVU, c.v_upper + grp * 8192, 8192, bar);
+      bulk_g2s(dst + kOffMeta, c.meta + grp * 512, 1024, bar);
+      if (MODE == QS_VERIFY_INT8) {
+        bulk_g2s(dst + kOffKL, c.k_lower + grp * 8192, 8192, bar);
+        bulk_g2s(dst + kOffVL, c.v_lower + grp * 8192, 8192, bar);
+      }
+    }
+  } else {
+    const int i0 = (cu.u - ng) * TT;
+    const int rows = min(TT, T.fill[cu.b] - i0);
+    if (lane == 0) mbar_arrive_expect_tx(bar, rows * 2 * kD * 2);
+    __syncwarp();
+    const int slot0 = T.hb[cu.b] * kG + i0;  // chunks never straddle the ring end
+    for (int rr = lane; rr < 2 * rows; rr += 32) {
+      const bool isv = rr >= rows;
+      const int row = isv ? rr - rows : rr;
+      const int slot = (slot0 + row) & (kRing - 1);
+      const uint16_t *src = (isv ? c.buf_v : c.buf_k) + (bh * kRing + slot) * kD;
+      bulk_g2s(dst + (isv ? TT * kTailRow : 0) + row * kTailRow, src, kD * 2, bar);
+    }
+  }
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) split_kernel(const Params prm) {
   using C = Cfg<MODE>;
   using L = Layout<MODE>;
   constexpr int TT = C::kTailTok, S = C::kStages;
   extern __shared__ __align__(128) uint8_t smem[];
   const qs_cache &c = prm.c;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = lane >> 2, cq = lane & 3;
   const uint32_t sbase = smem_addr(smem);
-  const uint32_t full0 = sbase + L::kBarOff, empty0 = full0 + 8 * S;
-  const uint32_t zero_row = sbase + L::kZeroOff;
+  const uint32_t full0 = sbase + L::kBarOff, zero_row = sbase + L::kZeroOff;
+  int *cnt = reinterpret_cast<int *>(smem + L::kCntOff);
   Tables T = tables_at(smem, L::kTabOff);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(full0 + 8 * s, 1);
-      mbar_init(empty0 + 8 * s, kConsumers);
+      cnt[s] = 0;
     }
     fence_mbar_init();
   }
   if (threadIdx.x < 8) reinterpret_cast<uint32_t *>(smem + L::kZeroOff)[threadIdx.x] = 0;
   __shared__ long long s_total;
-  if (warp == 0) {
+  if (w == 0) {
     const long long tot = build_tables<TT>(c, prm.n_q, T, lane);
     if (lane == 0) s_total = tot;
   }
@@ -292,108 +353,65 @@ __global__ void __launch_bounds__(kThreads, 2) split_kernel(const Params prm) {
   const int p = blockIdx.x;
   const long long x0 = range_lo(p, U, prm.P), x1 = range_lo(p + 1, U, prm.P);
   if (x0 >= x1) return;
+  const long long n = x1 - x0;
 
-  if (warp == kConsumers) {
-    // ------------------------------------------------------- producer
-    Cursor cur;
-    cur.init(x0, T, c.B, c.H);
-    long long issued = 0;
-    for (long long x = x0; x < x1; ++x, ++issued) {
-      const int stage = (int)(issued % S);
-      const uint32_t par = (uint32_t)((issued / S) & 1);
-      if (!mbar_wait(empty0 + 8 * stage, par ^ 1u)) {
-        if (lane == 0) atomicOr(&c.state[(size_t)cur.b * QS_STATE_WORDS + QS_ST_ERR], QS_DEV_TIMEOUT);
-        break;
-      }
-      const uint32_t dst = sbase + stage * L::kStageBytes, bar = full0 + 8 * stage;
-      const size_t bh = (size_t)cur.b * c.H + cur.h;
-      const int ng = T.ng[cur.b];
-      if (cur.u < ng) {
-        if (lane == 0) {
-          const size_t grp = bh * c.cap_groups + cur.u;
-          mbar_arrive_expect_tx(bar, C::kGroupBytes);
-          bulk_g2s(dst + kOffKU, c.k_upper + grp * 8192, 8192, bar);
-          bulk_g2s(dst + kOffVU, c.v_upper + grp * 8192, 8192, bar);
-          bulk_g2s(dst + kOffMeta, c.meta + grp * 512, 1024, bar);
-          if (MODE == QS_VERIFY_INT8) {
-            bulk_g2s(dst + kOffKL, c.k_lower + grp * 8192, 8192, bar);
-            bulk_g2s(dst + kOffVL, c.v_lower + grp * 8192, 8192, bar);
-          }
-        }
-      } else {
-        const int i0 = (cur.u - ng) * TT;
-        const int rows = min(TT, T.fill[cur.b] - i0);
-        if (lane == 0) mbar_arrive_expect_tx(bar, rows * 2 * kD * 2);
-        __syncwarp();
-        const int slot0 = T.hb[cur.b] * kG + i0;  // chunks never straddle the ring end
-        for (int rr = lane; rr < 2 * rows; rr += 32) {
-          const bool isv = rr >= rows;
-          const int row = isv ? rr - rows : rr;
-          const int slot = (slot0 + row) & (kRing - 1);
-          const uint16_t *src = (isv ? c.buf_v : c.buf_k) + (bh * kRing + slot) * kD;
-          bulk_g2s(dst + (isv ? TT * kTailRow : 0) + row * kTailRow, src, kD * 2, bar);
-        }
-      }
-      cur.advance(T, c.B, c.H);
+  // units i and i + S share a stage; "ahead" walks S units in front
+  Cursor cur, ahead;
+  cur.init(x0, T, c.B, c.H);
+  ahead = cur;
+  if (w == 0) {  // prologue: the first S units
+    for (int k = 0; k < S && k < n; ++k) {
+      issue_unit<MODE>(c, T, ahead, sbase + k * L::kStageBytes, full0 + 8 * k, lane);
+      ahead.advance(T, c.B, c.H);
     }
-    // drain: no copy may still be in flight when this warp leaves
-    const long long first = issued > S ? issued - S : 0;
-    for (long long k = first; k < issued; ++k)
-      if (!mbar_wait(full0 + 8 * (int)(k % S), (uint32_t)((k / S) & 1))) break;
-    return;
+  } else {
+    for (int k = 0; k < S && k < n; ++k) ahead.advance(T, c.B, c.H);
   }
 
-  // --------------------------------------------------------- consumers
-  const int w = warp, r = lane >> 2, cq = lane & 3;
-  Cursor cur;
-  cur.init(x0, T, c.B, c.H);
   Softmax sm;
   sm.reset();
   uint32_t qp0[8], qp1[8];
   int fill = 0, ng = 0;
-  long long idx = 0;
-  for (long long x = x0; x < x1; ++x, ++idx) {
+  for (long long i = 0; i < n; ++i) {
     const size_t bh = (size_t)cur.b * c.H + cur.h;
-    if (x == x0 || cur.u == 0) {  // a new piece: this (sequence, head)
+    if (i == 0 || cur.u == 0) {  // a new piece: this (sequence, head)
       load_q_pairs(prm.q + (bh * prm.n_q + r) * kD, r < prm.n_q, cq, qp0, qp1);
       sm.reset();
       fill = T.fill[cur.b];
       ng = T.ng[cur.b];
     }
-    const int stage = (int)(idx % S);
-    const uint32_t par = (uint32_t)((idx / S) & 1);
-    if (!mbar_wait(full0 + 8 * stage, par)) {
+    const int stage = (int)(i % S);
+    if (!mbar_wait(full0 + 8 * stage, (uint32_t)((i / S) & 1))) {
       if (lane == 0) atomicOr(&c.state[(size_t)cur.b * QS_STATE_WORDS + QS_ST_ERR], QS_DEV_TIMEOUT);
+      // bounded drain of the copies still outstanding in the other stages
+      for (long long k = i + 1; k < i + S && k < n; ++k)
+        if (!mbar_wait(full0 + 8 * (int)(k % S), (uint32_t)((k / S) & 1))) break;
       return;
     }
     const uint32_t st = sbase + stage * L::kStageBytes;
 
     if (cur.u < ng) {
       // ================================================ quantized group
-      // per-group B = q * s_K (fp16) and key bias sum_d q_d (z_d [+ 8 s_d])
+      // B = q * s_K (fp16) per channel; bias from one MMA per k-block whose A
+      // rows 0-7 hold the zero-points and rows 8-15 the scales.  The meta rows
+      // are stored in fragment order: one 16-byte load gives k-blocks 2i, 2i+1.
       uint32_t bm0[8], bm1[8];
       float bacc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint4 sw = lds128(st + kOffMeta + QS_META_K_SCALE * 256 + 64 * cq + 16 * i);
-        const uint4 zw = lds128(st + kOffMeta + QS_META_K_ZERO * 256 + 64 * cq + 16 * i);
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          const int kb = 2 * i + t;
-          const uint32_t sa = t ? sw.y : sw.x, sb = t ? sw.w : sw.z;
-          const uint32_t za = t ? zw.y : zw.x, zb = t ? zw.w : zw.z;
-          const uint32_t sp0 = prmt(sa, sb, 0x5410), sp1 = prmt(sa, sb, 0x7632);
-          const uint32_t zp0 = prmt(za, zb, 0x5410), zp1 = prmt(za, zb, 0x7632);
-          bm0[kb] = hmul2_u32(qp0[kb], sp0);
-          bm1[kb] = hmul2_u32(qp1[kb], sp1);
-          // rows 0-7 of A = zero-points, rows 8-15 = scales: one MMA gives
-          // sum_d z_d q_d and sum_d s_d q_d for every query
-          mma16816(bacc, zp0, sp0, zp1, sp1, qp0[kb], qp1[kb]);
-        }
+      for (int i4 = 0; i4 < 4; ++i4) {
+        const uint4 sw = lds128(st + kOffMeta + QS_META_K_SCALE * 256 + 16 * (4 * i4 + cq));
+        const uint4 zw = lds128(st + kOffMeta + QS_META_K_ZERO * 256 + 16 * (4 * i4 + cq));
+        const int k0 = 2 * i4, k1 = 2 * i4 + 1;
+        bm0[k0] = hmul2_u32(qp0[k0], sw.x);
+        bm1[k0] = hmul2_u32(qp1[k0], sw.y);
+        bm0[k1] = hmul2_u32(qp0[k1], sw.z);
+        bm1[k1] = hmul2_u32(qp1[k1], sw.w);
+        mma16816(bacc, zw.x, sw.x, zw.y, sw.y, qp0[k0], qp1[k0]);
+        mma16816(bacc, zw.z, sw.z, zw.w, sw.w, qp0[k1], qp1[k1]);
       }
-      const float kb0 = (MODE == QS_DRAFT_UPPER4) ? bacc[0] + 8.f * bacc[2] : bacc[0];
-      const float kb1 = (MODE == QS_DRAFT_UPPER4) ? bacc[1] + 8.f * bacc[3] : bacc[1];
-      const float bk0 = kb0 * prm.sl2, bk1 = kb1 * prm.sl2;
+      // key dequant s (code - 128) + (z + kOff s): bias = sum_d q_d z_d + kOff sum_d q_d s_d
+      const float bk0 = fmaf(Centre<MODE>::kOff, bacc[2], bacc[0]) * prm.sl2;
+      const float bk1 = fmaf(Centre<MODE>::kOff, bacc[3], bacc[1]) * prm.sl2;
 
       // scores for the warp's 32 tokens: two m-tiles of 16
       float s[2][4];
@@ -411,34 +429,41 @@ __global__ void __launch_bounds__(kThreads, 2) split_kernel(const Params prm) {
         const uint32_t wu0[4] = {u0.x, u0.y, u0.z, u0.w}, wu1[4] = {u1.x, u1.y, u1.z, u1.w};
         const uint32_t wl0[4] = {l0.x, l0.y, l0.z, l0.w}, wl1[4] = {l1.x, l1.y, l1.z, l1.w};
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
+        for (int j = 0; j < 4; ++j) {
           uint32_t a[4], b8[4];
-          pairs<MODE>(wu0[i], wl0[i], a);
-          pairs<MODE>(wu1[i], wl1[i], b8);
-          mma16816(acc, a[0], b8[0], a[1], b8[1], bm0[2 * i], bm1[2 * i]);
-          mma16816(acc, a[2], b8[2], a[3], b8[3], bm0[2 * i + 1], bm1[2 * i + 1]);
+          pairs<MODE>(wu0[j], wl0[j], a);
+          pairs<MODE>(wu1[j], wl1[j], b8);
+          mma16816(acc, a[0], b8[0], a[1], b8[1], bm0[2 * j], bm1[2 * j]);
+          mma16816(acc, a[2], b8[2], a[3], b8[3], bm0[2 * j + 1], bm1[2 * j + 1]);
         }
         s[mt][0] = fmaf(acc[0], prm.sl2, bk0);
         s[mt][1] = fmaf(acc[1], prm.sl2, bk1);
         s[mt][2] = fmaf(acc[2], prm.sl2, bk0);
         s[mt][3] = fmaf(acc[3], prm.sl2, bk1);
       }
-      float g0 = fmaxf(fmaxf(s[0][0], s[0][2]), fmaxf(s[1][0], s[1][2]));
-      float g1 = fmaxf(fmaxf(s[0][1], s[0][3]), fmaxf(s[1][1], s[1][3]));
+      const float g0 = fmaxf(fmaxf(s[0][0], s[0][2]), fmaxf(s[1][0], s[1][2]));
+      const float g1 = fmaxf(fmaxf(s[0][1], s[0][3]), fmaxf(s[1][1], s[1][3]));
       float u0, u1;
       sm.update(warp_max8(g0), warp_max8(g1), u0, u1);
 
-      // probabilities, value scale folded in, value zero-point as a bias
+      // probabilities, value scale folded in, value zero-point as a bias; the
+      // value rows hold this lane's four tokens (r, r+8, r+16, r+24) together
+      const uint2 svw = *reinterpret_cast<const uint2 *>(smem + (st - sbase) + kOffMeta +
+                                                         QS_META_V_SCALE * 256 + 2 * (32 * w + 4 * r));
+      const uint2 zvw = *reinterpret_cast<const uint2 *>(smem + (st - sbase) + kOffMeta +
+                                                         QS_META_V_ZERO * 256 + 2 * (32 * w + 4 * r));
+      const float2 sv01 = __half22float2(u32_as_h2(svw.x)), sv23 = __half22float2(u32_as_h2(svw.y));
+      const float2 zv01 = __half22float2(u32_as_h2(zvw.x)), zv23 = __half22float2(u32_as_h2(zvw.y));
+      const float svs[4] = {sv01.x, sv01.y, sv23.x, sv23.y};
+      const float zvs[4] = {zv01.x, zv01.y, zv23.x, zv23.y};
       uint32_t bp0[2], bp1[2];
 #pragma unroll
       for (int mt = 0; mt < 2; ++mt) {
         float pv[4];
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
-          const int t = 32 * w + 16 * mt + r + 8 * hh;
-          const float sv = h2f(lds16(st + kOffMeta + QS_META_V_SCALE * 256 + 2 * t));
-          float zv = h2f(lds16(st + kOffMeta + QS_META_V_ZERO * 256 + 2 * t));
-          if (MODE == QS_DRAFT_UPPER4) zv = fmaf(8.f, sv, zv);
+          const float sv = svs[2 * mt + hh];
+          const float zv = fmaf(Centre<MODE>::kOff, sv, zvs[2 * mt + hh]);
           const float pa = fast_exp2(s[mt][2 * hh] - u0), pb = fast_exp2(s[mt][2 * hh + 1] - u1);
           sm.l[0] += pa;
           sm.l[1] += pb;
@@ -492,8 +517,7 @@ __global__ void __launch_bounds__(kThreads, 2) split_kernel(const Params prm) {
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const int tok = mr + r + 8 * (k >> 1);
-          const int j = k & 1;
-          const bool vis = tok < rows && (i0 + tok) <= lim0 + j;
+          const bool vis = tok < rows && (i0 + tok) <= lim0 + (k & 1);
           sv[k] = vis ? acc[k] * prm.sl2 : -INFINITY;
         }
         float u0, u1;
@@ -519,10 +543,22 @@ __global__ void __launch_bounds__(kThreads, 2) split_kernel(const Params prm) {
         }
       }
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(empty0 + 8 * stage);
 
-    if (x + 1 == x1 || cur.u + 1 == T.len[cur.b]) {
+    // release the stage; the last warp out issues the refill (unit i + S)
+    __syncwarp();
+    int last = 0;
+    if (lane == 0) last = (atomicAdd(&cnt[stage], 1) == kConsumers - 1);
+    last = __shfl_sync(0xffffffffu, last, 0);
+    if (last) {
+      if (lane == 0) cnt[stage] = 0;
+      if (i + S < n) {
+        fence_proxy_async_smem();
+        issue_unit<MODE>(c, T, ahead, st, full0 + 8 * stage, lane);
+      }
+    }
+    if (i + S < n) ahead.advance(T, c.B, c.H);
+
+    if (i + 1 == n || cur.u + 1 == T.len[cur.b]) {
       // ---- piece done: one partial per warp (unnormalized, log2 domain)
       const float l0 = warp_sum8(sm.l[0]), l1 = warp_sum8(sm.l[1]);
       const float v0 = warp_sum8(sm.bv[0]), v1 = warp_sum8(sm.bv[1]);
@@ -540,8 +576,10 @@ __global__ void __launch_bounds__(kThreads, 2) split_kernel(const Params prm) {
         }
       }
       if (r == 0) {
-        if (j0 < prm.n_q) { dst[prm.n_q * kD + j0] = sm.m[0]; dst[prm.n_q * kD + 8 + j0] = l0; }
-        if (j1 < prm.n_q) { dst[prm.n_q * kD + j1] = sm.m[1]; dst[prm.n_q * kD + 8 + j1] = l1; }
+        const float m0 = sm.m[0] == -INFINITY ? -INFINITY : sm.m[0] - kExpShift;
+        const float m1 = sm.m[1] == -INFINITY ? -INFINITY : sm.m[1] - kExpShift;
+        if (j0 < prm.n_q) { dst[prm.n_q * kD + j0] = m0; dst[prm.n_q * kD + 8 + j0] = l0; }
+        if (j1 < prm.n_q) { dst[prm.n_q * kD + j1] = m1; dst[prm.n_q * kD + 8 + j1] = l1; }
       }
     }
     cur.advance(T, c.B, c.H);
@@ -580,13 +618,18 @@ __global__ void __launch_bounds__(128) combine_kernel(const Params prm) {
   const int plo = cta_of(S0, U, prm.P), phi = cta_of(E0 - 1, U, prm.P);
   const long long seg = (long long)bh;
   const int stride = nq * kD + 16;
+  // CTAs between the first and last owner with an empty range (more CTAs
+  // than units) wrote nothing: skip them
+  auto owns = [&](int pp) { return range_lo(pp, U, prm.P) < range_lo(pp + 1, U, prm.P); };
   for (int j = 0; j < nq; ++j) {
     float M = -INFINITY;
     for (int pp = plo; pp <= phi; ++pp)
-      for (int w = 0; w < kConsumers; ++w)
-        M = fmaxf(M, prm.ws[((seg + pp) * kConsumers + w) * stride + nq * kD + j]);
+      if (owns(pp))
+        for (int w = 0; w < kConsumers; ++w)
+          M = fmaxf(M, prm.ws[((seg + pp) * kConsumers + w) * stride + nq * kD + j]);
     float Lsum = 0.f, acc = 0.f;
     for (int pp = plo; pp <= phi; ++pp)
+      if (owns(pp))
       for (int w = 0; w < kConsumers; ++w) {
         const float *part = prm.ws + ((seg + pp) * kConsumers + w) * stride;
         const float ms = part[nq * kD + j];

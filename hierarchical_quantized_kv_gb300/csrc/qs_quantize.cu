@@ -18,13 +18,18 @@ namespace qs {
 
 namespace {
 
+constexpr int kParts = 4;           // CTAs per (head, sequence)
+constexpr int kSlice = kD / kParts;  // key channels / value tokens per CTA
+
+// One CTA owns key channels [32p, 32p+32) (one 16-byte column of every key
+// row) and value tokens [32p, 32p+32) (value quarter p).
 struct FlushSmem {
-  __half k[kG][kD];      // oldest buffer half, keys  [token][channel]
-  __half v[kG][kD];      // values
-  uint8_t kc[kG][kD];    // 8-bit key codes   [token][channel]
-  uint8_t vc[kG][kD];    // 8-bit value codes [token][channel]
-  float kmin[2][kD], kmax[2][kD];
-  uint16_t ks[kD], kz[kD], vs[kG], vz[kG];
+  __half k[kG][kSlice];     // keys of the slice   [token][channel - 32p]
+  __half v[kSlice][kD];     // values of the slice [token - 32p][channel]
+  uint8_t kc[kG][kSlice];   // key codes
+  uint8_t vc[kSlice][kD];   // value codes
+  float kmin[8][kSlice], kmax[8][kSlice];
+  uint16_t ks[kSlice], kz[kSlice], vs[kSlice], vz[kSlice];
   int act, base, g;
 };
 
@@ -51,21 +56,36 @@ __device__ __forceinline__ int vperm(int p) {
   return 16 * ((p >> 1) & 1) + 8 * (p & 1) + 2 * (p >> 3) + ((p >> 2) & 1);
 }
 
+// Position of channel c in a key scale / zero row (inverse of the header's
+// map p -> 32((p>>3)&3) + 8(p>>5) + 2((p>>2)&1) + ((p>>1)&1) + 4(p&1)).
+__device__ __forceinline__ int kmeta_pos(int c) {
+  return ((c >> 2) & 1) | ((c & 1) << 1) | (((c >> 1) & 1) << 2) | (((c >> 5) & 3) << 3) |
+         (((c >> 3) & 3) << 5);
+}
+
+// Position of token t in a value scale / zero row (inverse of
+// p -> 32(p>>5) + ((p>>2)&7) + 16((p>>1)&1) + 8(p&1)).
+__device__ __forceinline__ int vmeta_pos(int t) {
+  return ((t >> 3) & 1) | (((t >> 4) & 1) << 1) | ((t & 7) << 2) | ((t >> 5) << 5);
+}
+
 }  // namespace
 
 __global__ void __launch_bounds__(256) flush_kernel(qs_cache c, const uint8_t *__restrict__ mask) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   FlushSmem &S = *reinterpret_cast<FlushSmem *>(smem_raw);
-  const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
+  const int part = blockIdx.x, h = blockIdx.y, b = blockIdx.z, tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
   int32_t *st = c.state + (size_t)b * QS_STATE_WORDS;
   if (tid == 0) {
     int act = mask ? (mask[b] != 0) : 1;
     const int fill = st[QS_ST_FILL], pending = st[QS_ST_PENDING], ng = st[QS_ST_N_GROUPS];
+    const bool lead = (h == 0 && part == 0);
     if (act && fill - pending < kG) {
-      if (h == 0) atomicOr(&st[QS_ST_ERR], QS_DEV_FLUSH_UNCOMMITTED);
+      if (lead) atomicOr(&st[QS_ST_ERR], QS_DEV_FLUSH_UNCOMMITTED);
       act = 0;
     } else if (act && (ng < 0 || ng >= c.cap_groups)) {
-      if (h == 0) atomicOr(&st[QS_ST_ERR], QS_DEV_CAPACITY);
+      if (lead) atomicOr(&st[QS_ST_ERR], QS_DEV_CAPACITY);
       act = 0;
     }
     S.act = act;
@@ -76,75 +96,75 @@ __global__ void __launch_bounds__(256) flush_kernel(qs_cache c, const uint8_t *_
   if (!S.act) return;
   const int base = S.base, g = S.g;
   const size_t bh = (size_t)b * c.H + h;
+  const __half *gk = reinterpret_cast<const __half *>(c.buf_k) + (bh * kRing + base * kG) * kD;
+  const __half *gv = reinterpret_cast<const __half *>(c.buf_v) + (bh * kRing + base * kG) * kD;
 
-  // 1. the oldest half: ring slots base*G .. base*G + G - 1 (contiguous)
-  {
-    const uint4 *gk = reinterpret_cast<const uint4 *>(c.buf_k + (bh * kRing + base * kG) * kD);
-    const uint4 *gv = reinterpret_cast<const uint4 *>(c.buf_v + (bh * kRing + base * kG) * kD);
-    uint4 *sk = reinterpret_cast<uint4 *>(&S.k[0][0]);
-    uint4 *sv = reinterpret_cast<uint4 *>(&S.v[0][0]);
-    for (int e = tid; e < kG * kD / 8; e += 256) {
-      sk[e] = gk[e];
-      sv[e] = gv[e];
-    }
+  // 1. loads: the key column slice (64 B of each of 128 rows), 32 value rows
+  for (int e = tid; e < kG * 4; e += 256) {  // 4 x 16 B per key row
+    const int t = e >> 2, q = e & 3;
+    reinterpret_cast<uint4 *>(&S.k[t][0])[q] =
+        reinterpret_cast<const uint4 *>(gk + (size_t)t * kD + part * kSlice)[q];
   }
+  for (int e = tid; e < kSlice * kD / 8; e += 256)
+    reinterpret_cast<uint4 *>(&S.v[0][0])[e] =
+        reinterpret_cast<const uint4 *>(gv + (size_t)part * kSlice * kD)[e];
   __syncthreads();
 
-  // 2. keys: min / max per channel over the G tokens (two halves of tokens)
+  // 2. keys: min / max per channel, warp w over tokens 16w..16w+15
   {
-    const int d = tid & (kD - 1), part = tid >> 7;
     float mn = INFINITY, mx = -INFINITY;
-    for (int t = part * 64; t < part * 64 + 64; ++t) {
-      const float x = __half2float(S.k[t][d]);
+    for (int t = 16 * warp; t < 16 * warp + 16; ++t) {
+      const float x = __half2float(S.k[t][lane]);
       mn = fminf(mn, x);
       mx = fmaxf(mx, x);
     }
-    S.kmin[part][d] = mn;
-    S.kmax[part][d] = mx;
+    S.kmin[warp][lane] = mn;
+    S.kmax[warp][lane] = mx;
   }
-  // 3. values: one warp per token, min / max over the D channels, then codes
-  {
-    const int warp = tid >> 5, lane = tid & 31;
-    for (int t = warp; t < kG; t += 8) {
-      const __half2 *row = reinterpret_cast<const __half2 *>(&S.v[t][4 * lane]);
-      const float2 a = __half22float2(row[0]), bb = __half22float2(row[1]);
-      float mn = fminf(fminf(a.x, a.y), fminf(bb.x, bb.y));
-      float mx = fmaxf(fmaxf(a.x, a.y), fmaxf(bb.x, bb.y));
-      for (int o = 16; o > 0; o >>= 1) {
-        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-      }
-      uint16_t sb, zb;
-      float sf, zf;
-      scale_zero(mn, mx, sb, zb, sf, zf);
-      if (lane == 0) {
-        S.vs[t] = sb;
-        S.vz[t] = zb;
-      }
-      const uint32_t q0 = code_of(a.x, zf, sf), q1 = code_of(a.y, zf, sf);
-      const uint32_t q2 = code_of(bb.x, zf, sf), q3 = code_of(bb.y, zf, sf);
-      *reinterpret_cast<uint32_t *>(&S.vc[t][4 * lane]) = q0 | (q1 << 8) | (q2 << 16) | (q3 << 24);
+  // 3. values: one warp per token, min / max over the 128 channels, codes
+  for (int t = warp; t < kSlice; t += 8) {
+    const __half2 *row = reinterpret_cast<const __half2 *>(&S.v[t][4 * lane]);
+    const float2 a = __half22float2(row[0]), bb = __half22float2(row[1]);
+    float mn = fminf(fminf(a.x, a.y), fminf(bb.x, bb.y));
+    float mx = fmaxf(fmaxf(a.x, a.y), fmaxf(bb.x, bb.y));
+    for (int o = 16; o > 0; o >>= 1) {
+      mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     }
-  }
-  __syncthreads();
-  if (tid < kD) {
     uint16_t sb, zb;
     float sf, zf;
-    scale_zero(fminf(S.kmin[0][tid], S.kmin[1][tid]), fmaxf(S.kmax[0][tid], S.kmax[1][tid]), sb,
-               zb, sf, zf);
+    scale_zero(mn, mx, sb, zb, sf, zf);
+    if (lane == 0) {
+      S.vs[t] = sb;
+      S.vz[t] = zb;
+    }
+    const uint32_t q0 = code_of(a.x, zf, sf), q1 = code_of(a.y, zf, sf);
+    const uint32_t q2 = code_of(bb.x, zf, sf), q3 = code_of(bb.y, zf, sf);
+    *reinterpret_cast<uint32_t *>(&S.vc[t][4 * lane]) = q0 | (q1 << 8) | (q2 << 16) | (q3 << 24);
+  }
+  __syncthreads();
+  if (tid < kSlice) {
+    float mn = S.kmin[0][tid], mx = S.kmax[0][tid];
+    for (int w = 1; w < 8; ++w) {
+      mn = fminf(mn, S.kmin[w][tid]);
+      mx = fmaxf(mx, S.kmax[w][tid]);
+    }
+    uint16_t sb, zb;
+    float sf, zf;
+    scale_zero(mn, mx, sb, zb, sf, zf);
     S.ks[tid] = sb;
     S.kz[tid] = zb;
   }
   __syncthreads();
 
-  // 4. key codes: thread = channel pair (2j, 2j+1) x a quarter of the tokens
+  // 4. key codes: thread = channel pair j (16 pairs) x 8 tokens
   {
-    const int j = tid & 63, tq = tid >> 6;
+    const int j = tid & 15, t0 = (tid >> 4) * 8;
     const float s0 = __half2float(__ushort_as_half(S.ks[2 * j]));
     const float s1 = __half2float(__ushort_as_half(S.ks[2 * j + 1]));
     const float z0 = __half2float(__ushort_as_half(S.kz[2 * j]));
     const float z1 = __half2float(__ushort_as_half(S.kz[2 * j + 1]));
-    for (int t = tq * 32; t < tq * 32 + 32; ++t) {
+    for (int t = t0; t < t0 + 8; ++t) {
       const float2 x = __half22float2(*reinterpret_cast<const __half2 *>(&S.k[t][2 * j]));
       const uint32_t q0 = code_of(x.x, z0, s0), q1 = code_of(x.y, z1, s1);
       *reinterpret_cast<uint16_t *>(&S.kc[t][2 * j]) = (uint16_t)(q0 | (q1 << 8));
@@ -153,49 +173,47 @@ __global__ void __launch_bounds__(256) flush_kernel(qs_cache c, const uint8_t *_
   __syncthreads();
 
   const size_t grp = bh * c.cap_groups + g;
-  // 5. key planes, token-major: byte i of a token = channels 2i (low), 2i+1
-  {
-    const int t = tid >> 1, hb = tid & 1;
-    uint8_t u[32], l[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const uint32_t c0 = S.kc[t][64 * hb + 2 * i], c1 = S.kc[t][64 * hb + 2 * i + 1];
-      u[i] = (uint8_t)((c0 >> 4) | (c1 & 0xF0u));
-      l[i] = (uint8_t)((c0 & 15u) | ((c1 & 15u) << 4));
-    }
-    uint4 *gu = reinterpret_cast<uint4 *>(c.k_upper + (grp * kG + t) * (kD / 2) + 32 * hb);
-    uint4 *gl = reinterpret_cast<uint4 *>(c.k_lower + (grp * kG + t) * (kD / 2) + 32 * hb);
-    gu[0] = *reinterpret_cast<uint4 *>(&u[0]);
-    gu[1] = *reinterpret_cast<uint4 *>(&u[16]);
-    gl[0] = *reinterpret_cast<uint4 *>(&l[0]);
-    gl[1] = *reinterpret_cast<uint4 *>(&l[16]);
-  }
-  // 6. value planes: [quarter][channel][16 B], nibble p holds token vperm(p)
-  for (int ri = tid; ri < 4 * kD; ri += 256) {
-    const int u4 = ri >> 7, d = ri & (kD - 1);
+  if (tid < kG) {
+    // 5. key planes: bytes [16p, 16p+16) of token row tid (channels 2i, 2i+1)
     uint32_t wu[4] = {0, 0, 0, 0}, wl[4] = {0, 0, 0, 0};
 #pragma unroll
-    for (int p = 0; p < 32; ++p) {
-      const uint32_t q = S.vc[32 * u4 + vperm(p)][d];
-      wu[p >> 3] |= (q >> 4) << (4 * (p & 7));
-      wl[p >> 3] |= (q & 15u) << (4 * (p & 7));
+    for (int i = 0; i < 16; ++i) {
+      const uint32_t c0 = S.kc[tid][2 * i], c1 = S.kc[tid][2 * i + 1];
+      wu[i >> 2] |= ((c0 >> 4) | (c1 & 0xF0u)) << (8 * (i & 3));
+      wl[i >> 2] |= ((c0 & 15u) | ((c1 & 15u) << 4)) << (8 * (i & 3));
     }
-    reinterpret_cast<uint4 *>(c.v_upper)[grp * 4 * kD + ri] = make_uint4(wu[0], wu[1], wu[2], wu[3]);
-    reinterpret_cast<uint4 *>(c.v_lower)[grp * 4 * kD + ri] = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+    reinterpret_cast<uint4 *>(c.k_upper + (grp * kG + tid) * (kD / 2))[part] =
+        make_uint4(wu[0], wu[1], wu[2], wu[3]);
+    reinterpret_cast<uint4 *>(c.k_lower + (grp * kG + tid) * (kD / 2))[part] =
+        make_uint4(wl[0], wl[1], wl[2], wl[3]);
+  } else {
+    // 6. value quarter p: row d = 16 bytes, nibble position q holds token vperm(q)
+    const int d = tid - kG;
+    uint32_t wu[4] = {0, 0, 0, 0}, wl[4] = {0, 0, 0, 0};
+#pragma unroll
+    for (int q = 0; q < 32; ++q) {
+      const uint32_t code = S.vc[vperm(q)][d];
+      wu[q >> 3] |= (code >> 4) << (4 * (q & 7));
+      wl[q >> 3] |= (code & 15u) << (4 * (q & 7));
+    }
+    const size_t row = (grp * 4 + part) * kD + d;
+    reinterpret_cast<uint4 *>(c.v_upper)[row] = make_uint4(wu[0], wu[1], wu[2], wu[3]);
+    reinterpret_cast<uint4 *>(c.v_lower)[row] = make_uint4(wl[0], wl[1], wl[2], wl[3]);
   }
-  // 7. metadata rows: key scale, key zero (per channel), value scale, zero
-  if (tid < 128) {
+  // 7. metadata: key scale / zero of the channel slice, value scale / zero of the quarter
+  if (tid < kSlice) {
     uint16_t *m = c.meta + grp * 4 * 128;
-    m[QS_META_K_SCALE * 128 + tid] = S.ks[tid];
-    m[QS_META_K_ZERO * 128 + tid] = S.kz[tid];
-    m[QS_META_V_SCALE * 128 + tid] = S.vs[tid];
-    m[QS_META_V_ZERO * 128 + tid] = S.vz[tid];
+    const int kp = kmeta_pos(part * kSlice + tid), vp = vmeta_pos(part * kSlice + tid);
+    m[QS_META_K_SCALE * 128 + kp] = S.ks[tid];
+    m[QS_META_K_ZERO * 128 + kp] = S.kz[tid];
+    m[QS_META_V_SCALE * 128 + vp] = S.vs[tid];
+    m[QS_META_V_ZERO * 128 + vp] = S.vz[tid];
   }
   __syncthreads();
   if (tid == 0) {
     __threadfence();
     const int ticket = atomicAdd(&st[QS_ST_TICKET], 1);
-    if (ticket == c.H - 1) {  // every head has read the old counters
+    if (ticket == kParts * c.H - 1) {  // every CTA of the sequence has read the old counters
       st[QS_ST_N_GROUPS] = g + 1;
       st[QS_ST_HALF_BASE] = base ^ 1;
       st[QS_ST_FILL] -= kG;
@@ -223,6 +241,6 @@ extern "C" qs_status qs_quantize_flush(const qs_cache *c, const uint8_t *d_mask,
       return QS_ERR_CUDA;
     if (dev < 32) __atomic_fetch_or(&configured_mask, 1 << dev, __ATOMIC_RELAXED);
   }
-  flush_kernel<<<dim3(c->H, c->B), 256, smem, (cudaStream_t)stream>>>(*c, d_mask);
+  flush_kernel<<<dim3(kParts, c->H, c->B), 256, smem, (cudaStream_t)stream>>>(*c, d_mask);
   return launch_status();
 }

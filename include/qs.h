@@ -115,7 +115,12 @@ enum { QS_META_K_SCALE = 0, QS_META_K_ZERO = 1, QS_META_V_SCALE = 2, QS_META_V_Z
  *      of the group.  This fixed permutation lets one 32-bit shared-memory
  *      word per lane feed tensor-core fragments without byte shuffles.
  *  meta  fp16 [B][H][cap][4][128]: per group, rows QS_META_*: key scale and
- *      zero per channel, value scale and zero per token.
+ *      zero per channel, value scale and zero per token, each row in a fixed
+ *      order matched to the tensor-core fragments:
+ *        key rows: position p holds channel
+ *          32*((p>>3)&3) + 8*(p>>5) + 2*((p>>2)&1) + ((p>>1)&1) + 4*(p&1);
+ *        value rows: position p holds token
+ *          32*(p>>5) + ((p>>2)&7) + 16*((p>>1)&1) + 8*(p&1).
  *  buf_k, buf_v  fp16 [B][H][2G][D]: the double full-precision buffer.
  *  state  int32 [B][QS_STATE_WORDS]: counters above; zero it (qs_state_reset)
  *      before first use.

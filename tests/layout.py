@@ -41,10 +41,23 @@ def unpack_k(upper, lower):
     return (u << 4 | l_).astype(np.uint8)
 
 
+def kmeta_perm(p):
+    """Channel stored at position p of a key scale / zero row."""
+    p = np.asarray(p)
+    return 32 * ((p >> 3) & 3) + 8 * (p >> 5) + 2 * ((p >> 2) & 1) + ((p >> 1) & 1) + 4 * (p & 1)
+
+
+def vmeta_perm(p):
+    """Token stored at position p of a value scale / zero row."""
+    p = np.asarray(p)
+    return 32 * (p >> 5) + ((p >> 2) & 7) + 16 * ((p >> 1) & 1) + 8 * (p & 1)
+
+
 def meta(ks, kz, vs, vz):
     """fp16 bit arrays [..., 128] x4 -> [..., 4, 128] (rows: K scale, K zero,
-    V scale, V zero)."""
-    return np.stack([ks, kz, vs, vz], axis=-2).astype(np.uint16)
+    V scale, V zero), each row in the header's position order."""
+    kp, vp = kmeta_perm(np.arange(128)), vmeta_perm(np.arange(128))
+    return np.stack([ks[..., kp], kz[..., kp], vs[..., vp], vz[..., vp]], axis=-2).astype(np.uint16)
 
 
 def device_arrays(oc: oracle.OracleCache):

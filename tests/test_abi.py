@@ -75,9 +75,10 @@ def test_host_validation_before_any_cuda_call(L):
         assert qs.status_string(s)
 
 
-def test_value_layout_permutation_is_a_bijection():
-    t = layout.vperm(np.arange(32))
-    assert sorted(t.tolist()) == list(range(32))
+def test_layout_permutations_are_bijections():
+    assert sorted(layout.vperm(np.arange(32)).tolist()) == list(range(32))
+    assert sorted(layout.kmeta_perm(np.arange(128)).tolist()) == list(range(128))
+    assert sorted(layout.vmeta_perm(np.arange(128)).tolist()) == list(range(128))
 
 
 def test_pack_unpack_roundtrip():

@@ -237,7 +237,9 @@ def test_attn_ragged_small(torch):
             got, gl = run_attn(torch, cache, mode, q)
             ref, rl = oc.attn(q, upper_only=(mode == DRAFT))
             assert_close(got, ref, gl, rl, "n_q %d mode %d" % (n_q, mode))
-    assert np.all(qs.qs_get_errors(cache) == 0)
+        # sequences with fill < n_q are flagged on both sides
+        assert np.array_equal(qs.qs_get_errors(cache), oc.state[:, oracle.ERR])
+        oc.state[:, oracle.ERR] = 0
 
 
 def test_attn_nq_greater_than_fill(torch):
@@ -276,7 +278,7 @@ def test_draft_equals_verify_when_lower_is_eight(torch):
 # ------------------------------------------------------------ full sizes
 
 def _sampled_oracle(w, bs, hs):
-    cap = max(w.n_groups[b] for b in bs) + 1
+    cap = max(w.n_groups) + 1
     oc = oracle.OracleCache(len(bs), len(hs), w.D, w.G, cap)
 
     def tokens(i, t0, n):
@@ -308,9 +310,41 @@ def test_full_size_sampled(torch, cfg, bs, hs):
         g = dev[name][np.ix_(bs, hs)]
         assert np.array_equal(g[:, :, :oc.cap], want[name]), name
     assert np.array_equal(dev["state"][bs, :5], want["state"][:, :5])
-    for call, (mode, n_q) in enumerate(((DRAFT, 1), (VERIFY, 5))):
+
+    def both(call, mode, n_q):
         q = synthetic.queries(w, call, n_q)
         got, gl = run_attn(torch, cache, mode, q)
         ref, rl = oc.attn(np.ascontiguousarray(q[np.ix_(bs, hs)]), upper_only=(mode == DRAFT))
         assert_close(got[np.ix_(bs, hs)], ref, gl[np.ix_(bs, hs)], rl, "%s mode %d" % (cfg, mode))
+
+    both(0, DRAFT, 1)
+    # a verify round: flush where the 5 target tokens would overflow, append
+    # them, then 5 causal queries (every sequence then has fill >= 5)
+    mask = torch.zeros(w.B, dtype=torch.uint8, device="cuda")
+    qs.qs_need_flush(cache, 5, mask)
+    qs.qs_quantize_flush(cache, mask)
+    m = oc.need_flush(5)
+    assert np.array_equal(mask.cpu().numpy()[bs], m)
+    oc.flush(m)
+    k = np.zeros((w.B, w.H, 5, w.D), np.float16)
+    v = np.zeros_like(k)
+    for b in range(w.B):
+        k[b], v[b] = synthetic.kv_tokens(w, b, w.context[b], 5)
+    qs.qs_buffer_append(cache, to_dev(torch, k), to_dev(torch, v))
+    oc.append(np.ascontiguousarray(k[np.ix_(bs, hs)]), np.ascontiguousarray(v[np.ix_(bs, hs)]))
+    dev = layout.read_device(cache)
+    want = layout.device_arrays(oc)
+    for name in ("k_upper", "v_lower", "meta"):
+        g = dev[name][np.ix_(bs, hs)]
+        assert np.array_equal(g[:, :, :want[name].shape[2]], want[name]), name
+    # the logical buffer tokens (ring slots past fill may hold different
+    # dropped tokens: the device prefill appended the batch-wide maximum fill)
+    for i, b in enumerate(bs):
+        st = dev["state"][b]
+        assert np.array_equal(st[:4], oc.state[i, :4])
+        slots = (st[3] * w.G + np.arange(st[1])) % (2 * w.G)
+        for name, ref in (("buf_k", oc.bk), ("buf_v", oc.bv)):
+            assert np.array_equal(dev[name][b][hs][:, slots], ref[i][:, slots]), name
+    both(1, VERIFY, 5)
+    both(2, DRAFT, 1)
     assert np.all(qs.qs_get_errors(cache) == 0)
