@@ -14,7 +14,8 @@ step does the same work.  ``value`` is algorithmic bytes per step / step time
 (GB/s), summed over ranks.
 
 Per-call numbers (draft_us, verify_us, flush_us and the roofline object) time
-one call at a time with the L2 flushed (256 MB write) before each call.
+one call at a time (CUDA-graph replay) with the L2 evicted before each call
+by reading a 256 MB buffer.
 """
 import argparse
 import json
@@ -213,15 +214,32 @@ class HostIO:
             h.copy_(d, non_blocking=True)
 
 
+def capture(torch, fn):
+    """fn's launches captured once as a CUDA graph (the calls are stream
+    ordered and allocate nothing, so replaying the graph repeats them)."""
+    fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    torch.cuda.synchronize()
+    return g
+
+
 def time_calls(torch, fn, setup, iters, l2_scratch):
-    """Mean device time of fn() over iters calls, L2 flushed before each."""
+    """Mean device time of one call (replayed from a CUDA graph) over iters
+    calls, L2 flushed before each by reading a buffer twice the L2 size (a
+    read leaves no dirty lines for the timed call to write back)."""
+    setup()
+    g = capture(torch, fn)
     ts = []
+    sink = torch.empty((), dtype=l2_scratch.dtype, device=l2_scratch.device)
     for _ in range(iters):
         setup()
-        l2_scratch.zero_()
+        torch.sum(l2_scratch, out=sink)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
-        fn()
+        g.replay()
         b.record()
         b.synchronize()
         ts.append(a.elapsed_time(b) * 1e3)  # us
@@ -250,6 +268,12 @@ def native(args):
     for s in range(args.warmup):
         r.step(s)
     torch.cuda.synchronize()
+    # one CUDA graph per distinct step (the seeded accepted counts cycle with
+    # period len(r.drops)); each replay launches the step's kernels
+    graphs = [capture(torch, lambda s=s: r.step(s)) for s in range(len(r.drops))]
+    for s in range(args.warmup):
+        graphs[s % len(graphs)].replay()
+    torch.cuda.synchronize()
 
     sampler = ClockSampler(local)
     time.sleep(0.3)
@@ -260,7 +284,7 @@ def native(args):
     t0 = time.time()
     ev0.record()
     for s in range(args.steps):
-        r.step(s)
+        graphs[s % len(graphs)].replay()
     ev1.record()
     torch.cuda.synchronize()
     t1 = time.time()
@@ -275,7 +299,7 @@ def native(args):
         ms = float(tt.item())
 
     # per-call timing with L2 flushed (draft, verify, flush)
-    l2 = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    l2 = torch.ones(64 << 20, dtype=torch.float32, device="cuda")  # 256 MB
     it = args.call_iters
     draft_us = time_calls(torch, lambda: qs.qs_attn_decode(r.cache, qs.QS_DRAFT_UPPER4, r.qd[0], r.scale,
                                                            r.od[0], None, r.ws),
@@ -292,15 +316,17 @@ def native(args):
     dominant = ("draft", draft_gbs, GAMMA * draft_us) if GAMMA * draft_us >= verify_us else \
         ("verify", verify_gbs, verify_us)
 
-    # end to end through host buffers
+    # end to end through host buffers: each step copies its inputs from pinned
+    # host memory, runs, copies its outputs back, and the host waits for them
     host = HostIO(torch, r)
+    egraphs = [capture(torch, lambda s=s: r.step(s, host)) for s in range(len(r.drops))]
     for s in range(3):
-        r.step(s, host)
+        egraphs[s % len(egraphs)].replay()
         torch.cuda.current_stream().synchronize()
-    e_steps = max(1, min(args.steps, 200))
+    e_steps = max(1, min(args.steps, 500))
     te0 = time.perf_counter()
     for s in range(e_steps):
-        r.step(s, host)
+        egraphs[s % len(egraphs)].replay()
         torch.cuda.current_stream().synchronize()  # the host reads the step's result
     e2e_ms = (time.perf_counter() - te0) * 1e3 / e_steps
     if world > 1:
@@ -328,7 +354,7 @@ def native(args):
                    "B": w.B, "H": w.H, "D": w.D, "G": w.G, "context": w.context[0],
                    "quantized_groups_at_attention": r.ng1, "bytes_per_step": r.step_bytes,
                    "l2": "step: inputs larger than L2 (%.0f MB of planes per step); per-call numbers: "
-                         "256 MB L2 flush before each call" % (r.step_bytes / 1e6),
+                         "L2 evicted before each call by a 256 MB read" % (r.step_bytes / 1e6),
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "draft_us": round(draft_us, 2), "draft_gbs": round(draft_gbs, 1),
         "verify_us": round(verify_us, 2), "verify_gbs": round(verify_gbs, 1),
@@ -341,6 +367,7 @@ def native(args):
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": host.h2d_bytes,
                 "d2h_bytes_per_step": host.d2h_bytes},
         "gpu_launches": r.launches_per_step * args.steps,
+        "launch": "CUDA graph replay of each step (one graph per distinct step)",
         "clocks": clocks,
     }
     if cpu is not None:
@@ -457,6 +484,8 @@ def profile(args):
     from hierarchical_quantized_kv_gb300 import qs, synthetic
     w = synthetic.CONFIGS[args.config]()
     r = Round(torch, w, seed=0)
+    for i in range(args.warmup if args.profile == "step" else 0):
+        r.step(i)
     for i in range(args.profile_calls):
         if args.profile == "draft":
             r.set_state(r.ng1, r.f1 + 1)

@@ -21,7 +21,9 @@
 //    + 1 KB scales/zeros).  There is no producer warp: the last warp to finish
 //    with a stage (a shared-memory arrival counter) issues its refill, so all
 //    four warps compute and three CTAs fit on an SM.
-//  * The four warps each take 32 tokens of a group: nibbles become
+//  * Units alternate between the CTA's two warp pairs; within a pair each
+//    warp takes 64 tokens of the group (so per-unit fixed costs amortize over
+//    64 tokens).  Nibbles become
 //    exact fp16 integers in registers (bit tricks, no conversion
 //    instructions), and the dense contractions q.K^T and P.V run on
 //    m16n8k16 tensor-core MMAs with fp32 accumulation.  Scales are folded:
@@ -230,23 +232,26 @@ struct Softmax {
 #pragma unroll
       for (int k = 0; k < 4; ++k) o[md][k] = 0.f;
   }
-  // New maximum from this step's warp-wide maxima; rescales the state and
-  // returns the offset to subtract (0 when nothing is visible yet).
-  __device__ void update(float g0, float g1, float &u0, float &u1) {
+  // New maximum from this step's warp-wide maxima: rescales l and the value
+  // bias, returns the factors a0, a1 for O (applied when the step's P.V is
+  // merged) and the offsets u0, u1 to subtract from the scores.
+  __device__ void update(float g0, float g1, float &u0, float &u1, float &a0, float &a1) {
     const float n0 = fmaxf(m[0], g0), n1 = fmaxf(m[1], g1);
-    const float a0 = (n0 == -INFINITY) ? 1.f : fast_exp2(m[0] - n0);
-    const float a1 = (n1 == -INFINITY) ? 1.f : fast_exp2(m[1] - n1);
+    a0 = (n0 == -INFINITY) ? 1.f : fast_exp2(m[0] - n0);
+    a1 = (n1 == -INFINITY) ? 1.f : fast_exp2(m[1] - n1);
     u0 = (n0 == -INFINITY) ? 0.f : n0 - kExpShift;
     u1 = (n1 == -INFINITY) ? 0.f : n1 - kExpShift;
     m[0] = n0;
     m[1] = n1;
-    if (a0 != 1.f || a1 != 1.f) {
-      l[0] *= a0; l[1] *= a1; bv[0] *= a0; bv[1] *= a1;
-#pragma unroll
-      for (int md = 0; md < 8; ++md) {
-        o[md][0] *= a0; o[md][1] *= a1; o[md][2] *= a0; o[md][3] *= a1;
-      }
-    }
+    l[0] *= a0; l[1] *= a1; bv[0] *= a0; bv[1] *= a1;
+  }
+  // O = a * O + D for one 16-channel tile: each step's P.V starts from a zero
+  // accumulator, so no tensor-core accumulation chain spans more than a group.
+  __device__ __forceinline__ void merge(int md, const float (&d)[4], float a0, float a1) {
+    o[md][0] = fmaf(o[md][0], a0, d[0]);
+    o[md][1] = fmaf(o[md][1], a1, d[1]);
+    o[md][2] = fmaf(o[md][2], a0, d[2]);
+    o[md][3] = fmaf(o[md][3], a1, d[3]);
   }
 };
 
@@ -326,9 +331,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) split_kernel(const Param
   using C = Cfg<MODE>;
   using L = Layout<MODE>;
   constexpr int TT = C::kTailTok, S = C::kStages;
+  constexpr int kTailTiles = TT / 32;  // 16-token tiles of a buffer chunk per warp
+  static_assert(S % 2 == 0, "the two warp pairs alternate over the stages");
   extern __shared__ __align__(128) uint8_t smem[];
   const qs_cache &c = prm.c;
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int pr = w >> 1, hw = w & 1;  // warp pair (units of that parity), half of a unit
   const int r = lane >> 2, cq = lane & 3;
   const uint32_t sbase = smem_addr(smem);
   const uint32_t full0 = sbase + L::kBarOff, zero_row = sbase + L::kZeroOff;
@@ -353,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) split_kernel(const Param
   const int p = blockIdx.x;
   const long long x0 = range_lo(p, U, prm.P), x1 = range_lo(p + 1, U, prm.P);
   if (x0 >= x1) return;
-  const long long n = x1 - x0;
+  const int n = (int)(x1 - x0);
 
   // units i and i + S share a stage; "ahead" walks S units in front
   Cursor cur, ahead;
@@ -372,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) split_kernel(const Param
   sm.reset();
   uint32_t qp0[8], qp1[8];
   int fill = 0, ng = 0;
-  for (long long i = 0; i < n; ++i) {
+  for (int i = 0; i < n; ++i) {
     const size_t bh = (size_t)cur.b * c.H + cur.h;
     if (i == 0 || cur.u == 0) {  // a new piece: this (sequence, head)
       load_q_pairs(prm.q + (bh * prm.n_q + r) * kD, r < prm.n_q, cq, qp0, qp1);
@@ -380,186 +388,237 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) split_kernel(const Param
       fill = T.fill[cur.b];
       ng = T.ng[cur.b];
     }
-    const int stage = (int)(i % S);
-    if (!mbar_wait(full0 + 8 * stage, (uint32_t)((i / S) & 1))) {
-      if (lane == 0) atomicOr(&c.state[(size_t)cur.b * QS_STATE_WORDS + QS_ST_ERR], QS_DEV_TIMEOUT);
-      // bounded drain of the copies still outstanding in the other stages
-      for (long long k = i + 1; k < i + S && k < n; ++k)
-        if (!mbar_wait(full0 + 8 * (int)(k % S), (uint32_t)((k / S) & 1))) break;
-      return;
-    }
-    const uint32_t st = sbase + stage * L::kStageBytes;
+    if ((i & 1) == pr) {
+      const int stage = i % S;
+      if (!mbar_wait(full0 + 8 * stage, (uint32_t)((i / S) & 1))) {
+        if (lane == 0)
+          atomicOr(&c.state[(size_t)cur.b * QS_STATE_WORDS + QS_ST_ERR], QS_DEV_TIMEOUT);
+        // bounded drain of the copies still outstanding in this pair's stages
+        for (int k = i + 2; k < i + S && k < n; k += 2)
+          if (!mbar_wait(full0 + 8 * (k % S), (uint32_t)((k / S) & 1))) break;
+        return;
+      }
+      const uint32_t st = sbase + stage * L::kStageBytes;
 
-    if (cur.u < ng) {
-      // ================================================ quantized group
-      // B = q * s_K (fp16) per channel; bias from one MMA per k-block whose A
-      // rows 0-7 hold the zero-points and rows 8-15 the scales.  The meta rows
-      // are stored in fragment order: one 16-byte load gives k-blocks 2i, 2i+1.
-      uint32_t bm0[8], bm1[8];
-      float bacc[4] = {0.f, 0.f, 0.f, 0.f};
+      if (cur.u < ng) {
+        // ============================================== quantized group
+        // This warp: tokens [64 hw, 64 hw + 64) of the group.  B = q * s_K per
+        // channel as an fp16 pair hi + lo (lo = the exactly-rounded residual
+        // of the fp16 product, one fused multiply-add): a dominant token's
+        // large score would otherwise carry the 2^-11 rounding of q * s.
+        // The key bias comes from one MMA per k-block whose A rows 0-7 hold
+        // the zero-points and rows 8-15 the scales.  The meta rows are stored
+        // in fragment order: one 16-byte load gives k-blocks 2i, 2i+1.
+        uint32_t bh0[8], bh1[8], bl0[8], bl1[8];
+        float bacc[4] = {0.f, 0.f, 0.f, 0.f}, bacc2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int i4 = 0; i4 < 4; ++i4) {
-        const uint4 sw = lds128(st + kOffMeta + QS_META_K_SCALE * 256 + 16 * (4 * i4 + cq));
-        const uint4 zw = lds128(st + kOffMeta + QS_META_K_ZERO * 256 + 16 * (4 * i4 + cq));
-        const int k0 = 2 * i4, k1 = 2 * i4 + 1;
-        bm0[k0] = hmul2_u32(qp0[k0], sw.x);
-        bm1[k0] = hmul2_u32(qp1[k0], sw.y);
-        bm0[k1] = hmul2_u32(qp0[k1], sw.z);
-        bm1[k1] = hmul2_u32(qp1[k1], sw.w);
-        mma16816(bacc, zw.x, sw.x, zw.y, sw.y, qp0[k0], qp1[k0]);
-        mma16816(bacc, zw.z, sw.z, zw.w, sw.w, qp0[k1], qp1[k1]);
-      }
-      // key dequant s (code - 128) + (z + kOff s): bias = sum_d q_d z_d + kOff sum_d q_d s_d
-      const float bk0 = fmaf(Centre<MODE>::kOff, bacc[2], bacc[0]) * prm.sl2;
-      const float bk1 = fmaf(Centre<MODE>::kOff, bacc[3], bacc[1]) * prm.sl2;
+        for (int i4 = 0; i4 < 4; ++i4) {
+          const uint4 sw = lds128(st + kOffMeta + QS_META_K_SCALE * 256 + 16 * (4 * i4 + cq));
+          const uint4 zw = lds128(st + kOffMeta + QS_META_K_ZERO * 256 + 16 * (4 * i4 + cq));
+          const int k0 = 2 * i4, k1 = 2 * i4 + 1;
+          bh0[k0] = hmul2_u32(qp0[k0], sw.x);
+          bh1[k0] = hmul2_u32(qp1[k0], sw.y);
+          bh0[k1] = hmul2_u32(qp0[k1], sw.z);
+          bh1[k1] = hmul2_u32(qp1[k1], sw.w);
+          bl0[k0] = hfma2_neg_u32(qp0[k0], sw.x, bh0[k0]);
+          bl1[k0] = hfma2_neg_u32(qp1[k0], sw.y, bh1[k0]);
+          bl0[k1] = hfma2_neg_u32(qp0[k1], sw.z, bh0[k1]);
+          bl1[k1] = hfma2_neg_u32(qp1[k1], sw.w, bh1[k1]);
+          mma16816(bacc, zw.x, sw.x, zw.y, sw.y, qp0[k0], qp1[k0]);
+          mma16816(bacc2, zw.z, sw.z, zw.w, sw.w, qp0[k1], qp1[k1]);
+        }
+        // key dequant s (code - 128) + (z + kOff s): bias = sum q z + kOff sum q s
+        const float bk0 =
+            fmaf(Centre<MODE>::kOff, bacc[2] + bacc2[2], bacc[0] + bacc2[0]) * prm.sl2;
+        const float bk1 =
+            fmaf(Centre<MODE>::kOff, bacc[3] + bacc2[3], bacc[1] + bacc2[1]) * prm.sl2;
 
-      // scores for the warp's 32 tokens: two m-tiles of 16
-      float s[2][4];
+        // scores: four m-tiles of 16 tokens
+        float s[4][4];
 #pragma unroll
-      for (int mt = 0; mt < 2; ++mt) {
-        const int t0 = 32 * w + 16 * mt + r;
-        const uint4 u0 = lds128(st + kOffKU + t0 * 64 + 16 * cq);
-        const uint4 u1 = lds128(st + kOffKU + (t0 + 8) * 64 + 16 * cq);
-        uint4 l0 = make_uint4(0, 0, 0, 0), l1 = l0;
-        if (MODE == QS_VERIFY_INT8) {
-          l0 = lds128(st + kOffKL + t0 * 64 + 16 * cq);
-          l1 = lds128(st + kOffKL + (t0 + 8) * 64 + 16 * cq);
-        }
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        const uint32_t wu0[4] = {u0.x, u0.y, u0.z, u0.w}, wu1[4] = {u1.x, u1.y, u1.z, u1.w};
-        const uint32_t wl0[4] = {l0.x, l0.y, l0.z, l0.w}, wl1[4] = {l1.x, l1.y, l1.z, l1.w};
+        for (int mt = 0; mt < 4; ++mt) {
+          const int t0 = 64 * hw + 16 * mt + r;
+          const uint4 u0 = lds128(st + kOffKU + t0 * 64 + 16 * cq);
+          const uint4 u1 = lds128(st + kOffKU + (t0 + 8) * 64 + 16 * cq);
+          uint4 l0 = make_uint4(0, 0, 0, 0), l1 = l0;
+          if (MODE == QS_VERIFY_INT8) {
+            l0 = lds128(st + kOffKL + t0 * 64 + 16 * cq);
+            l1 = lds128(st + kOffKL + (t0 + 8) * 64 + 16 * cq);
+          }
+          float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};
+          float acc3[4] = {0.f, 0.f, 0.f, 0.f};
+          const uint32_t wu0[4] = {u0.x, u0.y, u0.z, u0.w}, wu1[4] = {u1.x, u1.y, u1.z, u1.w};
+          const uint32_t wl0[4] = {l0.x, l0.y, l0.z, l0.w}, wl1[4] = {l1.x, l1.y, l1.z, l1.w};
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          uint32_t a[4], b8[4];
-          pairs<MODE>(wu0[j], wl0[j], a);
-          pairs<MODE>(wu1[j], wl1[j], b8);
-          mma16816(acc, a[0], b8[0], a[1], b8[1], bm0[2 * j], bm1[2 * j]);
-          mma16816(acc, a[2], b8[2], a[3], b8[3], bm0[2 * j + 1], bm1[2 * j + 1]);
+          for (int j = 0; j < 4; ++j) {  // independent MMA chains: hi even, hi odd, lo
+            uint32_t a[4], b8[4];
+            pairs<MODE>(wu0[j], wl0[j], a);
+            pairs<MODE>(wu1[j], wl1[j], b8);
+            mma16816(acc, a[0], b8[0], a[1], b8[1], bh0[2 * j], bh1[2 * j]);
+            mma16816(acc2, a[2], b8[2], a[3], b8[3], bh0[2 * j + 1], bh1[2 * j + 1]);
+            mma16816(acc3, a[0], b8[0], a[1], b8[1], bl0[2 * j], bl1[2 * j]);
+            mma16816(acc3, a[2], b8[2], a[3], b8[3], bl0[2 * j + 1], bl1[2 * j + 1]);
+          }
+          s[mt][0] = fmaf(acc[0] + acc2[0] + acc3[0], prm.sl2, bk0);
+          s[mt][1] = fmaf(acc[1] + acc2[1] + acc3[1], prm.sl2, bk1);
+          s[mt][2] = fmaf(acc[2] + acc2[2] + acc3[2], prm.sl2, bk0);
+          s[mt][3] = fmaf(acc[3] + acc2[3] + acc3[3], prm.sl2, bk1);
         }
-        s[mt][0] = fmaf(acc[0], prm.sl2, bk0);
-        s[mt][1] = fmaf(acc[1], prm.sl2, bk1);
-        s[mt][2] = fmaf(acc[2], prm.sl2, bk0);
-        s[mt][3] = fmaf(acc[3], prm.sl2, bk1);
-      }
-      const float g0 = fmaxf(fmaxf(s[0][0], s[0][2]), fmaxf(s[1][0], s[1][2]));
-      const float g1 = fmaxf(fmaxf(s[0][1], s[0][3]), fmaxf(s[1][1], s[1][3]));
-      float u0, u1;
-      sm.update(warp_max8(g0), warp_max8(g1), u0, u1);
+        float g0 = fmaxf(s[0][0], s[0][2]), g1 = fmaxf(s[0][1], s[0][3]);
+#pragma unroll
+        for (int mt = 1; mt < 4; ++mt) {
+          g0 = fmaxf(g0, fmaxf(s[mt][0], s[mt][2]));
+          g1 = fmaxf(g1, fmaxf(s[mt][1], s[mt][3]));
+        }
+        float u0, u1, a0, a1;
+        sm.update(warp_max8(g0), warp_max8(g1), u0, u1, a0, a1);
 
-      // probabilities, value scale folded in, value zero-point as a bias; the
-      // value rows hold this lane's four tokens (r, r+8, r+16, r+24) together
-      const uint2 svw = *reinterpret_cast<const uint2 *>(smem + (st - sbase) + kOffMeta +
-                                                         QS_META_V_SCALE * 256 + 2 * (32 * w + 4 * r));
-      const uint2 zvw = *reinterpret_cast<const uint2 *>(smem + (st - sbase) + kOffMeta +
-                                                         QS_META_V_ZERO * 256 + 2 * (32 * w + 4 * r));
-      const float2 sv01 = __half22float2(u32_as_h2(svw.x)), sv23 = __half22float2(u32_as_h2(svw.y));
-      const float2 zv01 = __half22float2(u32_as_h2(zvw.x)), zv23 = __half22float2(u32_as_h2(zvw.y));
-      const float svs[4] = {sv01.x, sv01.y, sv23.x, sv23.y};
-      const float zvs[4] = {zv01.x, zv01.y, zv23.x, zv23.y};
-      uint32_t bp0[2], bp1[2];
+        // probabilities with the value scale folded in, value zero-point as a
+        // bias; each value row holds a lane's four tokens of a quarter together
+        uint32_t bp0[4], bp1[4];
 #pragma unroll
-      for (int mt = 0; mt < 2; ++mt) {
-        float pv[4];
+        for (int qq = 0; qq < 2; ++qq) {
+          const int moff = kOffMeta + 2 * (32 * (2 * hw + qq) + 4 * r);
+          const uint2 svw =
+              *reinterpret_cast<const uint2 *>(smem + (st - sbase) + moff + QS_META_V_SCALE * 256);
+          const uint2 zvw =
+              *reinterpret_cast<const uint2 *>(smem + (st - sbase) + moff + QS_META_V_ZERO * 256);
+          const float2 sv01 = __half22float2(u32_as_h2(svw.x)), sv23 = __half22float2(u32_as_h2(svw.y));
+          const float2 zv01 = __half22float2(u32_as_h2(zvw.x)), zv23 = __half22float2(u32_as_h2(zvw.y));
+          const float svs[4] = {sv01.x, sv01.y, sv23.x, sv23.y};
+          const float zvs[4] = {zv01.x, zv01.y, zv23.x, zv23.y};
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const float sv = svs[2 * mt + hh];
-          const float zv = fmaf(Centre<MODE>::kOff, sv, zvs[2 * mt + hh]);
-          const float pa = fast_exp2(s[mt][2 * hh] - u0), pb = fast_exp2(s[mt][2 * hh + 1] - u1);
-          sm.l[0] += pa;
-          sm.l[1] += pb;
-          sm.bv[0] = fmaf(pa, zv, sm.bv[0]);
-          sm.bv[1] = fmaf(pb, zv, sm.bv[1]);
-          pv[2 * hh] = pa * sv;
-          pv[2 * hh + 1] = pb * sv;
+          for (int ml = 0; ml < 2; ++ml) {
+            const int mt = 2 * qq + ml;
+            float pv[4];
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+              const float sv = svs[2 * ml + hh];
+              const float zv = fmaf(Centre<MODE>::kOff, sv, zvs[2 * ml + hh]);
+              const float pa = fast_exp2(s[mt][2 * hh] - u0), pb = fast_exp2(s[mt][2 * hh + 1] - u1);
+              sm.l[0] += pa;
+              sm.l[1] += pb;
+              sm.bv[0] = fmaf(pa, zv, sm.bv[0]);
+              sm.bv[1] = fmaf(pb, zv, sm.bv[1]);
+              pv[2 * hh] = pa * sv;
+              pv[2 * hh + 1] = pb * sv;
+            }
+            bp0[mt] = movmatrix_trans(pack_half2(pv[0], pv[1]));
+            bp1[mt] = movmatrix_trans(pack_half2(pv[2], pv[3]));
+          }
         }
-        bp0[mt] = movmatrix_trans(pack_half2(pv[0], pv[1]));
-        bp1[mt] = movmatrix_trans(pack_half2(pv[2], pv[3]));
-      }
-      // O^T += V^T P'  (values: quarter w of the group, channel-major rows)
-#pragma unroll
-      for (int md = 0; md < 8; ++md) {
-        const uint32_t ra = st + kOffVU + (w * 128 + 16 * md + r) * 16 + 4 * cq;
-        const uint32_t vu0 = lds32(ra), vu1 = lds32(ra + 8 * 16);
-        uint32_t vl0 = 0, vl1 = 0;
-        if (MODE == QS_VERIFY_INT8) {
-          vl0 = lds32(ra - kOffVU + kOffVL);
-          vl1 = lds32(ra - kOffVU + kOffVL + 8 * 16);
-        }
-        uint32_t a[4], b8[4];
-        pairs<MODE>(vu0, vl0, a);
-        pairs<MODE>(vu1, vl1, b8);
-        mma16816(sm.o[md], a[0], b8[0], a[1], b8[1], bp0[0], bp1[0]);
-        mma16816(sm.o[md], a[2], b8[2], a[3], b8[3], bp0[1], bp1[1]);
-      }
-    } else {
-      // ================================================ fp16 buffer chunk
-      const int i0 = (cur.u - ng) * TT;
-      const int rows = min(TT, fill - i0);
-      const int mr = 16 * w;
-      if (mr < rows) {
-        // natural-order B pairs of q for query r
-        const uint32_t *qw = reinterpret_cast<const uint32_t *>(prm.q + (bh * prm.n_q + r) * kD);
-        const bool qv = r < prm.n_q;
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int kb = 0; kb < 8; ++kb) {
-          const uint32_t b0 = qv ? __ldg(qw + 8 * kb + cq) : 0u;
-          const uint32_t b1 = qv ? __ldg(qw + 8 * kb + cq + 4) : 0u;
-          const int row = mr + (lane & 7) + ((lane >> 3) & 1) * 8;
-          const int col = 16 * kb + (lane >> 4) * 8;
-          const uint32_t addr = row < rows ? st + row * kTailRow + col * 2 : zero_row;
-          uint32_t a0, a1, a2, a3;
-          ldmatrix_x4(addr, a0, a1, a2, a3);
-          mma16816(acc, a0, a1, a2, a3, b0, b1);
-        }
-        const int lim0 = fill - prm.n_q + 2 * cq;  // last visible buffer index, query 2c
-        float sv[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int tok = mr + r + 8 * (k >> 1);
-          const bool vis = tok < rows && (i0 + tok) <= lim0 + (k & 1);
-          sv[k] = vis ? acc[k] * prm.sl2 : -INFINITY;
-        }
-        float u0, u1;
-        sm.update(warp_max8(fmaxf(sv[0], sv[2])), warp_max8(fmaxf(sv[1], sv[3])), u0, u1);
-        float pv[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          pv[k] = fast_exp2(sv[k] - ((k & 1) ? u1 : u0));
-          sm.l[k & 1] += pv[k];
-        }
-        const uint32_t bq0 = movmatrix_trans(pack_half2(pv[0], pv[1]));
-        const uint32_t bq1 = movmatrix_trans(pack_half2(pv[2], pv[3]));
-        const uint32_t vbase = st + TT * kTailRow;
+        // O^T = a O^T + V^T P'  (values: quarters 2hw and 2hw+1, channel-major)
 #pragma unroll
         for (int md = 0; md < 8; ++md) {
-          const int mi = lane >> 3;
-          const int tok = mr + (lane & 7) + (mi >> 1) * 8;
-          const int ch = 16 * md + (mi & 1) * 8;
-          const uint32_t addr = tok < rows ? vbase + tok * kTailRow + ch * 2 : zero_row;
-          uint32_t a0, a1, a2, a3;
-          ldmatrix_x4_trans(addr, a0, a1, a2, a3);
-          mma16816(sm.o[md], a0, a1, a2, a3, bq0, bq1);
+          float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int qq = 0; qq < 2; ++qq) {
+            const uint32_t ra = st + kOffVU + ((2 * hw + qq) * 128 + 16 * md + r) * 16 + 4 * cq;
+            const uint32_t vu0 = lds32(ra), vu1 = lds32(ra + 8 * 16);
+            uint32_t vl0 = 0, vl1 = 0;
+            if (MODE == QS_VERIFY_INT8) {
+              vl0 = lds32(ra - kOffVU + kOffVL);
+              vl1 = lds32(ra - kOffVU + kOffVL + 8 * 16);
+            }
+            uint32_t a[4], b8[4];
+            pairs<MODE>(vu0, vl0, a);
+            pairs<MODE>(vu1, vl1, b8);
+            mma16816(d, a[0], b8[0], a[1], b8[1], bp0[2 * qq], bp1[2 * qq]);
+            mma16816(d, a[2], b8[2], a[3], b8[3], bp0[2 * qq + 1], bp1[2 * qq + 1]);
+          }
+          sm.merge(md, d, a0, a1);
+        }
+      } else {
+        // ============================================== fp16 buffer chunk
+        // This warp: 16-token tiles [hw * kTailTiles, (hw + 1) * kTailTiles).
+        const int i0 = (cur.u - ng) * TT;
+        const int rows = min(TT, fill - i0);
+        const int mr0 = 16 * kTailTiles * hw;
+        if (mr0 < rows) {
+          const uint32_t *qw = reinterpret_cast<const uint32_t *>(prm.q + (bh * prm.n_q + r) * kD);
+          const bool qv = r < prm.n_q;
+          uint32_t qb0[8], qb1[8];  // natural-order B pairs of q for query r
+#pragma unroll
+          for (int kb = 0; kb < 8; ++kb) {
+            qb0[kb] = qv ? __ldg(qw + 8 * kb + cq) : 0u;
+            qb1[kb] = qv ? __ldg(qw + 8 * kb + cq + 4) : 0u;
+          }
+          const int lim0 = fill - prm.n_q + 2 * cq;  // last visible buffer index, query 2c
+          float sv[kTailTiles][4];
+          float g0 = -INFINITY, g1 = -INFINITY;
+#pragma unroll
+          for (int tl = 0; tl < kTailTiles; ++tl) {
+            const int mr = mr0 + 16 * tl;
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int kb = 0; kb < 8; ++kb) {
+              const int row = mr + (lane & 7) + ((lane >> 3) & 1) * 8;
+              const int col = 16 * kb + (lane >> 4) * 8;
+              const uint32_t addr = row < rows ? st + row * kTailRow + col * 2 : zero_row;
+              uint32_t f0, f1, f2, f3;
+              ldmatrix_x4(addr, f0, f1, f2, f3);
+              mma16816(acc, f0, f1, f2, f3, qb0[kb], qb1[kb]);
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const int tok = mr + r + 8 * (k >> 1);
+              const bool vis = tok < rows && (i0 + tok) <= lim0 + (k & 1);
+              sv[tl][k] = vis ? acc[k] * prm.sl2 : -INFINITY;
+            }
+            g0 = fmaxf(g0, fmaxf(sv[tl][0], sv[tl][2]));
+            g1 = fmaxf(g1, fmaxf(sv[tl][1], sv[tl][3]));
+          }
+          float u0, u1, a0, a1;
+          sm.update(warp_max8(g0), warp_max8(g1), u0, u1, a0, a1);
+          uint32_t bq0[kTailTiles], bq1[kTailTiles];
+#pragma unroll
+          for (int tl = 0; tl < kTailTiles; ++tl) {
+            float pv[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              pv[k] = fast_exp2(sv[tl][k] - ((k & 1) ? u1 : u0));
+              sm.l[k & 1] += pv[k];
+            }
+            bq0[tl] = movmatrix_trans(pack_half2(pv[0], pv[1]));
+            bq1[tl] = movmatrix_trans(pack_half2(pv[2], pv[3]));
+          }
+          const uint32_t vbase = st + TT * kTailRow;
+#pragma unroll
+          for (int md = 0; md < 8; ++md) {
+            float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int tl = 0; tl < kTailTiles; ++tl) {
+              const int mi = lane >> 3;
+              const int tok = mr0 + 16 * tl + (lane & 7) + (mi >> 1) * 8;
+              const int ch = 16 * md + (mi & 1) * 8;
+              const uint32_t addr = tok < rows ? vbase + tok * kTailRow + ch * 2 : zero_row;
+              uint32_t f0, f1, f2, f3;
+              ldmatrix_x4_trans(addr, f0, f1, f2, f3);
+              mma16816(d, f0, f1, f2, f3, bq0[tl], bq1[tl]);
+            }
+            sm.merge(md, d, a0, a1);
+          }
         }
       }
-    }
 
-    // release the stage; the last warp out issues the refill (unit i + S)
-    __syncwarp();
-    int last = 0;
-    if (lane == 0) last = (atomicAdd(&cnt[stage], 1) == kConsumers - 1);
-    last = __shfl_sync(0xffffffffu, last, 0);
-    if (last) {
-      if (lane == 0) cnt[stage] = 0;
-      if (i + S < n) {
-        fence_proxy_async_smem();
-        issue_unit<MODE>(c, T, ahead, st, full0 + 8 * stage, lane);
+      // release the stage; the later of the pair issues the refill (unit i + S)
+      __syncwarp();
+      int last = 0;
+      if (lane == 0) last = (atomicAdd(&cnt[stage], 1) == 1);
+      last = __shfl_sync(0xffffffffu, last, 0);
+      if (last) {
+        if (lane == 0) cnt[stage] = 0;
+        if (i + S < n) {
+          fence_proxy_async_smem();
+          issue_unit<MODE>(c, T, ahead, st, full0 + 8 * stage, lane);
+        }
       }
     }
     if (i + S < n) ahead.advance(T, c.B, c.H);
 
     if (i + 1 == n || cur.u + 1 == T.len[cur.b]) {
-      // ---- piece done: one partial per warp (unnormalized, log2 domain)
+      // ---- piece done: one partial per warp (unnormalized, log2 domain);
+      // a warp that saw none of the piece writes an empty one (m = -inf)
       const float l0 = warp_sum8(sm.l[0]), l1 = warp_sum8(sm.l[1]);
       const float v0 = warp_sum8(sm.bv[0]), v1 = warp_sum8(sm.bv[1]);
       const int stride = prm.n_q * kD + 16;

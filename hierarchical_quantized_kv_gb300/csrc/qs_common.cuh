@@ -155,6 +155,10 @@ __device__ __forceinline__ uint32_t hsub2_u32(uint32_t a, uint32_t b) {
 __device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
   return h2_as_u32(__hmul2(u32_as_h2(a), u32_as_h2(b)));
 }
+// Exact residual of an fp16 product, rounded once: a * b - c (fused).
+__device__ __forceinline__ uint32_t hfma2_neg_u32(uint32_t a, uint32_t b, uint32_t c) {
+  return h2_as_u32(__hfma2(u32_as_h2(a), u32_as_h2(b), __hneg2(u32_as_h2(c))));
+}
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   return h2_as_u32(__floats2half2_rn(lo, hi));
 }

@@ -6,6 +6,8 @@ and error words.  Attention outputs: max-abs <= 1e-2 and relative RMS <=
 log-sum-exp within 5e-3 (bounded by the fp16 rounding of q * s_K, about
 2^-11 of sum_d |q_d k_d| * softmax_scale, far below this on these inputs).
 """
+import os
+
 import numpy as np
 import pytest
 
@@ -64,6 +66,11 @@ def assert_close(got, ref, got_lse=None, ref_lse=None, what=""):
     assert np.all(np.isfinite(got)), what
     err = np.abs(got - ref).max()
     rel = np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-30)
+    log = os.environ.get("QS_PARITY_LOG")
+    if log:
+        with open(log, "a") as f:
+            f.write("%s\t%s\tmax_abs=%.3g\trel_rms=%.3g\n"
+                    % (os.environ.get("PYTEST_CURRENT_TEST", "").split(" ")[0], what, err, rel))
     assert err <= ATOL and rel <= RRMS, "%s: max-abs %.3g rel-rms %.3g" % (what, err, rel)
     if got_lse is not None:
         fin = np.isfinite(ref_lse)
@@ -240,6 +247,31 @@ def test_attn_ragged_small(torch):
         # sequences with fill < n_q are flagged on both sides
         assert np.array_equal(qs.qs_get_errors(cache), oc.state[:, oracle.ERR])
         oc.state[:, oracle.ERR] = 0
+
+
+@pytest.mark.parametrize("mode", [DRAFT, VERIFY])
+def test_peaked_attention(torch, mode):
+    """One key far above the rest (a large score on a quantized token): the
+    softmax is dominated by it, so the score's own rounding shows directly
+    in the output."""
+    rng = np.random.default_rng(21)
+    B, H, ng, fill = 1, 2, 6, 40
+    oc = oracle.OracleCache(B, H, 128, 128, ng)
+    q = h16(rng, (B, H, 2, 128))
+
+    def tokens(b, t0, n):
+        k = rng.standard_normal((H, n, 128))
+        k[:, :, :3] *= 8
+        if t0 <= 300 < t0 + n:  # token 300: aligned with the queries
+            k[:, 300 - t0] = 2.5 * q[0, :, 0].astype(np.float64)
+        return k.astype(np.float16), rng.standard_normal((H, n, 128)).astype(np.float16)
+
+    oracle.prefill(oc, tokens, [ng], [fill])
+    cache = qs.Cache(B, H, ng)
+    layout.load_into(cache, oc)
+    got, gl = run_attn(torch, cache, mode, q)
+    ref, rl = oc.attn(q, upper_only=(mode == DRAFT))
+    assert_close(got, ref, gl, rl, "peaked mode %d" % mode)
 
 
 def test_attn_nq_greater_than_fill(torch):
