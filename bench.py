@@ -36,6 +36,35 @@ GAMMA = 4
 KB = 1024
 
 
+def kernel_source_hash():
+    """sha256 over the attention kernel sources (to tell whether a stored ncu
+    traffic figure still describes the kernel that runs)."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("qs_attn.cu", "qs_common.cuh"):
+        with open(os.path.join(ROOT, "hierarchical_quantized_kv_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def stored_traffic(kind):
+    """DRAM bytes per launch of the split kernel from the committed ncu
+    summary, or None when the kernel changed since it was captured."""
+    path = os.path.join(ROOT, "profiles", "split_kernel_traffic_32k.txt")
+    try:
+        kv = {}
+        with open(path) as f:
+            for line in f:
+                if ":" in line and not line.startswith("#"):
+                    k, v = line.split(":", 1)
+                    kv[k.strip()] = v.strip()
+        if kv.get("source_sha256") != kernel_source_hash():
+            return None
+        return int(kv["%s_dram_bytes_per_launch" % kind])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
 def load_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -236,7 +265,7 @@ def time_calls(torch, fn, setup, iters, l2_scratch):
     sink = torch.empty((), dtype=l2_scratch.dtype, device=l2_scratch.device)
     for _ in range(iters):
         setup()
-        torch.sum(l2_scratch, out=sink)
+        torch.sum(l2_scratch, dim=0, out=sink)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
         g.replay()
@@ -362,7 +391,7 @@ def native(args):
         "roofline": {"bound": "hbm", "kernel": "qs_attn_decode %s (split + combine launch)" % dominant[0],
                      "achieved": round(dominant[1], 1), "peak": peak,
                      "peak_kind": "%s hbm_gbs (copy, burst)" % peak_kind, "unit": "GB/s",
-                     "frac": round(dominant[1] / peak, 4), "traffic": None},
+                     "frac": round(dominant[1] / peak, 4), "traffic": stored_traffic(dominant[0])},
         "e2e": {"value": round(r.step_bytes * world / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": host.h2d_bytes,
                 "d2h_bytes_per_step": host.d2h_bytes},

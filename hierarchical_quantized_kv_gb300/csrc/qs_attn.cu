@@ -172,15 +172,15 @@ struct Cursor {
 __device__ __forceinline__ void pairs_upper(uint32_t w, uint32_t (&e)[4]) {
   const uint32_t w8 = w >> 8;
   // bits 0-3 under exponent 2^14: 16384 + 16 n; bits 4-7 under 2^10: 1024 + 16 n
-  e[0] = hsub2_u32((w & 0x000F000Fu) | 0x74007400u, 0x74087408u);   // - 16512
-  e[1] = hsub2_u32((w & 0x00F000F0u) | 0x64006400u, 0x64806480u);   // - 1152
-  e[2] = hsub2_u32((w8 & 0x000F000Fu) | 0x74007400u, 0x74087408u);
-  e[3] = hsub2_u32((w8 & 0x00F000F0u) | 0x64006400u, 0x64806480u);
+  e[0] = hsub2_u32(and_or(w, 0x000F000Fu, 0x74007400u), 0x74087408u);   // - 16512
+  e[1] = hsub2_u32(and_or(w, 0x00F000F0u, 0x64006400u), 0x64806480u);   // - 1152
+  e[2] = hsub2_u32(and_or(w8, 0x000F000Fu, 0x74007400u), 0x74087408u);
+  e[3] = hsub2_u32(and_or(w8, 0x00F000F0u, 0x64006400u), 0x64806480u);
 }
 
 __device__ __forceinline__ void pairs_int8(uint32_t wu, uint32_t wl, uint32_t (&e)[4]) {
-  const uint32_t ev = (wl & 0x0F0F0F0Fu) | ((wu << 4) & 0xF0F0F0F0u);  // codes 0,2,4,6
-  const uint32_t od = ((wl >> 4) & 0x0F0F0F0Fu) | (wu & 0xF0F0F0F0u);  // codes 1,3,5,7
+  const uint32_t ev = bitsel(wl, wu << 4, 0x0F0F0F0Fu);   // codes 0,2,4,6
+  const uint32_t od = bitsel(wl >> 4, wu, 0x0F0F0F0Fu);   // codes 1,3,5,7
   // byte c under 0x64: 1024 + c, minus 1152
   e[0] = hsub2_u32(prmt(ev, 0x64646464u, 0x4240), 0x64806480u);
   e[1] = hsub2_u32(prmt(od, 0x64646464u, 0x4240), 0x64806480u);
@@ -352,6 +352,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) split_kernel(const Param
   }
   if (threadIdx.x < 8) reinterpret_cast<uint32_t *>(smem + L::kZeroOff)[threadIdx.x] = 0;
   __shared__ long long s_total;
+  pdl_trigger();
+  pdl_wait();  // counters, cache and queries are written by earlier kernels
   if (w == 0) {
     const long long tot = build_tables<TT>(c, prm.n_q, T, lane);
     if (lane == 0) s_total = tot;
@@ -646,58 +648,99 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) split_kernel(const Param
 }
 
 // ----------------------------------------------------------- combine kernel
-// One CTA per (head, sequence), one thread per channel:
-// o = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s.
+// One CTA per (32-channel chunk, head, sequence):
+//   M_j = max_s m_sj,  L_j = sum_s 2^(m_sj - M_j) l_sj,
+//   o_jd = sum_s 2^(m_sj - M_j) O_sjd / L_j,   lse_j = (M_j + log2 L_j) ln 2.
+// Warp w takes every 8th partial slot of the segment, lane = channel; each
+// thread merges its slots online in registers (all loads independent, so one
+// memory round trip), then the eight warps merge through shared memory.
+constexpr int kCombineThreads = 256;
+constexpr int kCombineWarps = kCombineThreads / 32;
+constexpr int kChunks = kD / 32;
+
 template <int MODE>
-__global__ void __launch_bounds__(128) combine_kernel(const Params prm) {
+__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const Params prm) {
   constexpr int TT = Cfg<MODE>::kTailTok;
   __shared__ int tab[5 * kMaxB];
   __shared__ long long s_total;
+  __shared__ float sm_m[kCombineWarps][kMaxQ], sm_l[kCombineWarps][kMaxQ];
+  __shared__ float sm_o[kCombineWarps][kMaxQ][32];
   const qs_cache &c = prm.c;
   Tables T{tab, tab + kMaxB, tab + 2 * kMaxB, tab + 3 * kMaxB, tab + 4 * kMaxB};
-  const int h = blockIdx.x, b = blockIdx.y, d = threadIdx.x;
-  if (threadIdx.x < 32) {
-    const long long tot = build_tables<TT>(c, prm.n_q, T, threadIdx.x);
-    if (threadIdx.x == 0) s_total = tot;
+  const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z, tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  pdl_trigger();
+  pdl_wait();  // the split kernel's partials
+  if (warp == 0) {
+    const long long tot = build_tables<TT>(c, prm.n_q, T, lane);
+    if (lane == 0) s_total = tot;
   }
   __syncthreads();
   const size_t bh = (size_t)b * c.H + h;
-  const int nq = prm.n_q;
+  const int nq = prm.n_q, d = 32 * chunk + lane;
   if (T.len[b] == 0) {  // n_q > fill: nothing is visible
-    if (h == 0 && d == 0 && nq > T.fill[b])
+    if (h == 0 && chunk == 0 && tid == 0 && nq > T.fill[b])
       atomicOr(&c.state[(size_t)b * QS_STATE_WORDS + QS_ST_ERR], QS_DEV_NQ_GT_FILL);
-    for (int j = 0; j < nq; ++j) {
-      prm.out[(bh * nq + j) * kD + d] = 0;
-      if (prm.lse && d == 0) prm.lse[bh * nq + j] = -INFINITY;
-    }
+    if (warp < nq) prm.out[(bh * nq + warp) * kD + d] = 0;
+    if (prm.lse && chunk == 0 && tid < nq) prm.lse[bh * nq + tid] = -INFINITY;
     return;
   }
   const long long U = s_total;
   const long long S0 = T.base[b] + (long long)h * T.len[b], E0 = S0 + T.len[b];
   const int plo = cta_of(S0, U, prm.P), phi = cta_of(E0 - 1, U, prm.P);
-  const long long seg = (long long)bh;
+  const int nslots = (phi - plo + 1) * kConsumers;
   const int stride = nq * kD + 16;
-  // CTAs between the first and last owner with an empty range (more CTAs
-  // than units) wrote nothing: skip them
-  auto owns = [&](int pp) { return range_lo(pp, U, prm.P) < range_lo(pp + 1, U, prm.P); };
-  for (int j = 0; j < nq; ++j) {
-    float M = -INFINITY;
-    for (int pp = plo; pp <= phi; ++pp)
-      if (owns(pp))
-        for (int w = 0; w < kConsumers; ++w)
-          M = fmaxf(M, prm.ws[((seg + pp) * kConsumers + w) * stride + nq * kD + j]);
-    float Lsum = 0.f, acc = 0.f;
-    for (int pp = plo; pp <= phi; ++pp)
-      if (owns(pp))
-      for (int w = 0; w < kConsumers; ++w) {
-        const float *part = prm.ws + ((seg + pp) * kConsumers + w) * stride;
-        const float ms = part[nq * kD + j];
-        const float f = (ms == -INFINITY) ? 0.f : exp2f(ms - M);
-        Lsum = fmaf(f, part[nq * kD + 8 + j], Lsum);
-        acc = fmaf(f, part[j * kD + d], acc);
+
+  float M[kMaxQ], L[kMaxQ], A[kMaxQ];
+#pragma unroll
+  for (int j = 0; j < kMaxQ; ++j) { M[j] = -INFINITY; L[j] = 0.f; A[j] = 0.f; }
+#pragma unroll 4
+  for (int k = warp; k < nslots; k += kCombineWarps) {
+    const int pp = plo + k / kConsumers;
+    // CTAs between the first and last owner with an empty range (more CTAs
+    // than units) wrote nothing: their slot (still inside the workspace) is
+    // read but masked to -inf
+    const bool owned = range_lo(pp, U, prm.P) < range_lo(pp + 1, U, prm.P);
+    const float *part = prm.ws + ((size_t)(bh + pp) * kConsumers + (k % kConsumers)) * stride;
+#pragma unroll
+    for (int j = 0; j < kMaxQ; ++j) {
+      if (j < nq) {
+        const float msr = part[nq * kD + j], lsr = part[nq * kD + 8 + j], osr = part[j * kD + d];
+        const float ms = owned ? msr : -INFINITY;
+        const float ls = owned ? lsr : 0.f, os = owned ? osr : 0.f;  // never 0 * garbage
+        const float mn = fmaxf(M[j], ms);
+        const float a = (M[j] == -INFINITY) ? 0.f : exp2f(M[j] - mn);
+        const float f = (ms == -INFINITY) ? 0.f : exp2f(ms - mn);
+        L[j] = fmaf(L[j], a, f * ls);
+        A[j] = fmaf(A[j], a, f * os);
+        M[j] = mn;
       }
-    prm.out[(bh * nq + j) * kD + d] = __half_as_ushort(__float2half_rn(acc / Lsum));
-    if (prm.lse && d == 0) prm.lse[bh * nq + j] = (M + log2f(Lsum)) * 0.69314718055994531f;
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < kMaxQ; ++j) {
+    if (j < nq) {
+      sm_o[warp][j][lane] = A[j];
+      if (lane == 0) { sm_m[warp][j] = M[j]; sm_l[warp][j] = L[j]; }
+    }
+  }
+  __syncthreads();
+  // warp j < nq merges query j across the eight warps
+  if (warp < nq) {
+    const int j = warp;
+    float mx = -INFINITY;
+    for (int w = 0; w < kCombineWarps; ++w) mx = fmaxf(mx, sm_m[w][j]);
+    float l = 0.f, acc = 0.f;
+    for (int w = 0; w < kCombineWarps; ++w) {
+      const float mw = sm_m[w][j];
+      if (mw != -INFINITY) {
+        const float f = exp2f(mw - mx);
+        l = fmaf(f, sm_l[w][j], l);
+        acc = fmaf(f, sm_o[w][j][lane], acc);
+      }
+    }
+    prm.out[(bh * nq + j) * kD + d] = __half_as_ushort(__float2half_rn(acc / l));
+    if (prm.lse && chunk == 0 && lane == 0) prm.lse[bh * nq + j] = (mx + log2f(l)) * 0.69314718055994531f;
   }
 }
 
@@ -744,11 +787,11 @@ size_t ws_bytes(int P, int B, int H, int n_q) {
 
 template <int MODE>
 qs_status launch(const Params &prm, cudaStream_t s) {
-  split_kernel<MODE><<<prm.P, kThreads, Layout<MODE>::kSmemBytes, s>>>(prm);
-  qs_status st = launch_status();
+  qs_status st =
+      launch_pdl(split_kernel<MODE>, dim3(prm.P), dim3(kThreads), Layout<MODE>::kSmemBytes, s, prm);
   if (st != QS_OK) return st;
-  combine_kernel<MODE><<<dim3(prm.c.H, prm.c.B), 128, 0, s>>>(prm);
-  return launch_status();
+  return launch_pdl(combine_kernel<MODE>, dim3(kChunks, prm.c.H, prm.c.B), dim3(kCombineThreads), 0, s,
+                    prm);
 }
 
 }  // namespace

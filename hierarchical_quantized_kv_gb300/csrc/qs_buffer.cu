@@ -19,6 +19,8 @@ namespace qs {
 __global__ void __launch_bounds__(256) append_kernel(qs_cache c, const uint4 *__restrict__ k_new,
                                                      const uint4 *__restrict__ v_new, int n_new) {
   const int h = blockIdx.x, b = blockIdx.y;
+  pdl_trigger();
+  pdl_wait();
   int32_t *st = c.state + (size_t)b * QS_STATE_WORDS;
   __shared__ int s_fill, s_base;
   if (threadIdx.x == 0) {
@@ -57,6 +59,8 @@ __global__ void __launch_bounds__(256) append_kernel(qs_cache c, const uint4 *__
 }
 
 __global__ void rollback_kernel(qs_cache c, const int32_t *__restrict__ n_drop) {
+  pdl_trigger();
+  pdl_wait();
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= c.B) return;
   int32_t *st = c.state + (size_t)b * QS_STATE_WORDS;
@@ -70,6 +74,8 @@ __global__ void rollback_kernel(qs_cache c, const int32_t *__restrict__ n_drop) 
 }
 
 __global__ void need_flush_kernel(qs_cache c, int n_next, uint8_t *__restrict__ mask) {
+  pdl_trigger();
+  pdl_wait();
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= c.B) return;
   mask[b] = (c.state[(size_t)b * QS_STATE_WORDS + QS_ST_FILL] + n_next > kRing) ? 1 : 0;
@@ -121,25 +127,25 @@ qs_status qs_buffer_append(const qs_cache *c, const uint16_t *k_new, const uint1
   if (s != QS_OK) return s;
   if (!k_new || !v_new || n_new < 1 || n_new > kRing) return QS_ERR_ARG;
   if (!aligned16(k_new) || !aligned16(v_new)) return QS_ERR_ALIGN;
-  append_kernel<<<dim3(c->H, c->B), 256, 0, (cudaStream_t)stream>>>(
-      *c, reinterpret_cast<const uint4 *>(k_new), reinterpret_cast<const uint4 *>(v_new), n_new);
-  return launch_status();
+  return launch_pdl(append_kernel, dim3(c->H, c->B), dim3(256), 0, (cudaStream_t)stream, *c,
+                    reinterpret_cast<const uint4 *>(k_new), reinterpret_cast<const uint4 *>(v_new),
+                    (int)n_new);
 }
 
 qs_status qs_buffer_rollback(const qs_cache *c, const int32_t *d_n_drop, qs_stream_t stream) {
   qs_status s = check_cache(c);
   if (s != QS_OK) return s;
   if (!d_n_drop) return QS_ERR_ARG;
-  rollback_kernel<<<(c->B + 127) / 128, 128, 0, (cudaStream_t)stream>>>(*c, d_n_drop);
-  return launch_status();
+  return launch_pdl(rollback_kernel, dim3((c->B + 127) / 128), dim3(128), 0, (cudaStream_t)stream,
+                    *c, d_n_drop);
 }
 
 qs_status qs_need_flush(const qs_cache *c, int32_t n_next, uint8_t *d_mask, qs_stream_t stream) {
   qs_status s = check_cache(c);
   if (s != QS_OK) return s;
   if (!d_mask || n_next < 0) return QS_ERR_ARG;
-  need_flush_kernel<<<(c->B + 127) / 128, 128, 0, (cudaStream_t)stream>>>(*c, n_next, d_mask);
-  return launch_status();
+  return launch_pdl(need_flush_kernel, dim3((c->B + 127) / 128), dim3(128), 0,
+                    (cudaStream_t)stream, *c, (int)n_next, d_mask);
 }
 
 qs_status qs_get_errors(const qs_cache *c, int32_t *h_err, qs_stream_t stream) {

@@ -76,6 +76,8 @@ __global__ void __launch_bounds__(256) flush_kernel(qs_cache c, const uint8_t *_
   FlushSmem &S = *reinterpret_cast<FlushSmem *>(smem_raw);
   const int part = blockIdx.x, h = blockIdx.y, b = blockIdx.z, tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
+  pdl_trigger();
+  pdl_wait();
   int32_t *st = c.state + (size_t)b * QS_STATE_WORDS;
   if (tid == 0) {
     int act = mask ? (mask[b] != 0) : 1;
@@ -241,6 +243,6 @@ extern "C" qs_status qs_quantize_flush(const qs_cache *c, const uint8_t *d_mask,
       return QS_ERR_CUDA;
     if (dev < 32) __atomic_fetch_or(&configured_mask, 1 << dev, __ATOMIC_RELAXED);
   }
-  flush_kernel<<<dim3(kParts, c->H, c->B), 256, smem, (cudaStream_t)stream>>>(*c, d_mask);
-  return launch_status();
+  return launch_pdl(flush_kernel, dim3(kParts, c->H, c->B), dim3(256), smem, (cudaStream_t)stream,
+                    *c, d_mask);
 }
