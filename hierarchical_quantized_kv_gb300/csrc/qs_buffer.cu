@@ -96,6 +96,7 @@ const char *qs_status_string(qs_status s) {
     case QS_ERR_CUDA: return "CUDA error";
     case QS_ERR_UNSUPPORTED: return "unsupported size (v1: D = G = 128, B <= 256)";
     case QS_ERR_WORKSPACE: return "workspace missing or too small";
+    case QS_ERR_TOO_LARGE: return "problem exceeds the fixed scratch of qs_attn_decode_static_ws";
   }
   return "unknown status";
 }

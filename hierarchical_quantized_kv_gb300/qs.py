@@ -14,7 +14,9 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libqs.so")
 
 QS_DRAFT_UPPER4, QS_VERIFY_INT8 = 0, 1
-QS_OK, QS_ERR_ARG, QS_ERR_SHAPE, QS_ERR_ALIGN, QS_ERR_CUDA, QS_ERR_UNSUPPORTED, QS_ERR_WORKSPACE = range(7)
+(QS_OK, QS_ERR_ARG, QS_ERR_SHAPE, QS_ERR_ALIGN, QS_ERR_CUDA, QS_ERR_UNSUPPORTED, QS_ERR_WORKSPACE,
+ QS_ERR_TOO_LARGE) = range(8)
+QS_STATIC_WS_BYTES = 8 << 20
 DEV_OVERFLOW, DEV_OVER_ROLLBACK, DEV_FLUSH_UNCOMMITTED, DEV_CAPACITY, DEV_NQ_GT_FILL, DEV_TIMEOUT = (
     1, 2, 4, 8, 16, 32)
 ST_N_GROUPS, ST_FILL, ST_PENDING, ST_HALF_BASE, ST_ERR, ST_TICKET = range(6)

@@ -66,7 +66,8 @@ typedef enum {
   QS_ERR_ALIGN = 3,       /* a device pointer is not 16-byte aligned */
   QS_ERR_CUDA = 4,        /* a CUDA call or launch failed */
   QS_ERR_UNSUPPORTED = 5, /* D or G other than 128 */
-  QS_ERR_WORKSPACE = 6    /* workspace missing or smaller than required */
+  QS_ERR_WORKSPACE = 6,   /* workspace missing or smaller than required */
+  QS_ERR_TOO_LARGE = 7    /* problem needs more scratch than qs_attn_decode_static_ws has */
 } qs_status;
 
 typedef enum {
@@ -200,6 +201,32 @@ qs_status qs_attn_workspace_size(const qs_cache *c, int32_t n_q, size_t *bytes);
 qs_status qs_attn_decode(const qs_cache *c, qs_mode mode, const uint16_t *q, int32_t n_q,
                          float softmax_scale, uint16_t *out, float *lse, void *workspace,
                          size_t workspace_bytes, qs_stream_t stream);
+
+/* Size of the fixed scratch array behind qs_attn_decode_static_ws. */
+#define QS_STATIC_WS_BYTES (8u << 20)
+
+/* qs_attn_decode for callers that cannot allocate device memory.  No
+ * counterpart on the pages: it exists for callers that cannot allocate
+ * device memory -- a serving process whose device memory is fixed up front,
+ * a foreign runtime without a CUDA allocator, a plug-in handed only its input
+ * and output buffers.  Same arguments, results and errors as qs_attn_decode,
+ * minus the workspace: the split partials go to a fixed array of
+ * QS_STATIC_WS_BYTES (8 MiB) inside this library, which every GPU that loads
+ * libqs holds until the process exits.  The caller still passes q, out and
+ * lse.  The call allocates nothing (no cudaMalloc or cudaFree).  Limits and
+ * sharing:
+ *  - a problem whose qs_attn_workspace_size exceeds QS_STATIC_WS_BYTES returns
+ *    QS_ERR_TOO_LARGE before launching anything;
+ *  - the first call on a device looks up the array's device address (with
+ *    that device current) and caches it; make that first call before any
+ *    stream capture;
+ *  - every call on a device uses the same array: calls that overlap on the
+ *    GPU (other streams, other threads) race and corrupt each other's
+ *    results; order them on one stream.  The array needs no clearing: every
+ *    value a call reads is written earlier in the same call. */
+qs_status qs_attn_decode_static_ws(const qs_cache *c, qs_mode mode, const uint16_t *q,
+                                   int32_t n_q, float softmax_scale, uint16_t *out, float *lse,
+                                   qs_stream_t stream);
 
 /* Copy every sequence's error word to h_err (int32 [B], host memory) and
  * clear them on the device.  Synchronizes the stream. */

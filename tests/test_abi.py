@@ -71,7 +71,7 @@ def test_host_validation_before_any_cuda_call(L):
                             None) == qs.QS_ERR_ARG
     assert L.qs_attn_decode(ctypes.byref(c), 0, ctypes.c_void_p(0x20004), 1, ctypes.c_float(0.1),
                             p, None, p, 1 << 20, None) == qs.QS_ERR_ALIGN
-    for s in range(7):
+    for s in range(8):
         assert qs.status_string(s)
 
 
