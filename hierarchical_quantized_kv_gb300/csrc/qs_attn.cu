@@ -1,6 +1,6 @@
 // qs_attn.cu -- split-KV decode attention over the hierarchical quantized KV
 // cache (draft: C_U only; verify: INT8 = 16 C_U + C_L) plus the fp16 buffer,
-// and the log-sum-exp combine.
+// with the log-sum-exp combine of the splits in the same kernel.
 //
 // Sources: "QuantSpec Guide: Self-Speculative Decoding & Quantized KV",
 // "1. Hierarchical Two-Level Quantization with Bit-Sharing" (draft loads only
@@ -29,8 +29,11 @@
 //    m16n8k16 tensor-core MMAs with fp32 accumulation.  Scales are folded:
 //    B = q * s_K per channel, P' = p * s_V per token, zero-point terms as
 //    per-query biases, so the inner loops touch codes only.
-//  * Each consumer warp keeps its own online softmax and writes one partial
-//    per (piece of a segment); the combine kernel merges them.
+//  * Each warp keeps its own online softmax and writes one partial per piece
+//    of a segment it touches.  At the end of its range the CTA merges its
+//    four warps' partials (log-sum-exp); a segment split across CTAs is
+//    finished by whichever of them arrives last on the segment's counter,
+//    so the whole call is one kernel launch.
 #include <math.h>
 
 #include "qs_common.cuh"
@@ -52,24 +55,31 @@ struct Cfg<QS_DRAFT_UPPER4> {
   static constexpr int kTailTok = 32;
   static constexpr int kStages = 4;
 };
+#ifndef QS_VERIFY_STAGES
+#define QS_VERIFY_STAGES 2
+#endif
 template <>
 struct Cfg<QS_VERIFY_INT8> {
   static constexpr int kGroupBytes = 4 * 8192 + 1024;
   static constexpr int kTailTok = 64;
-  static constexpr int kStages = 2;
+  static constexpr int kStages = QS_VERIFY_STAGES;
 };
+
+constexpr int align16(int x) { return (x + 15) & ~15; }
 
 template <int MODE>
 struct Layout {
   static constexpr int kTailBytes = Cfg<MODE>::kTailTok * kTailRow * 2;
   static constexpr int kStageBytes =
       Cfg<MODE>::kGroupBytes > kTailBytes ? Cfg<MODE>::kGroupBytes : kTailBytes;
-  static constexpr int kBarOff = Cfg<MODE>::kStages * kStageBytes;   // full barriers
-  static constexpr int kCntOff = kBarOff + 8 * Cfg<MODE>::kStages;    // release counters
-  static constexpr int kZeroOff = kCntOff + 16 * Cfg<MODE>::kStages;
+  static constexpr int kBarOff = Cfg<MODE>::kStages * kStageBytes;               // full barriers
+  static constexpr int kCntOff = align16(kBarOff + 8 * Cfg<MODE>::kStages);      // release counters
+  static constexpr int kZeroOff = align16(kCntOff + 4 * Cfg<MODE>::kStages);     // zero row (ldmatrix)
   static constexpr int kTabOff = kZeroOff + 32;
   // per-sequence tables: n_groups, fill, half_base, segment length, base unit
   static constexpr int kSmemBytes = kTabOff + 5 * kMaxB * 4;
+  static_assert(kStageBytes % 16 == 0 && kBarOff % 16 == 0 && kZeroOff % 16 == 0,
+                "bulk copies and ldmatrix rows need 16-byte aligned shared memory");
 };
 
 struct Params {
@@ -326,13 +336,130 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-template <int MODE>
+// ------------------------------------------------------- log-sum-exp merge
+// CTA-wide (128 threads) merge of ns partials of one (sequence, head).
+// Partial k starts at src + k * kstride floats and holds, for each query
+// j < n_q, the unnormalized O_j[d] at j * 128 + d, then m_j (log2 domain) at
+// n_q * 128 + j and l_j at n_q * 128 + 8 + j:
+//   M_j = max_k m_kj,  L_j = sum_k 2^(m_kj - M_j) l_kj,
+//   O_j = sum_k 2^(m_kj - M_j) O_kj.
+// final: out_j = O_j / L_j (fp16) and lse_j = (M_j + log2 L_j) ln 2; else the
+// merged partial is written to dst (same layout; dst may be partial 0).
+// With fewer units than CTAs some CTAs own no unit and write no partial: when
+// `owners` is set, partial k belongs to CTA pbase + k and is skipped if that
+// CTA's range is empty.
+// Lanes hold four channels each; the four warps take four queries at a time,
+// or (one or two queries) split the partials into phases merged through `red`
+// (128 x 6 floats of shared memory).  Each thread loads its partials eight at
+// a time, all eight in flight before the first is used.
+struct MergeOut {
+  bool final;
+  uint16_t *out;  // final: fp16 [n_q][128] of this (sequence, head)
+  float *lse;     // final: [n_q] or null
+  float *dst;     // partial
+};
+
+__device__ void merge_partials(const float *src, size_t kstride, int ns, int n_q, bool owners,
+                               int pbase, long long U, int P, const MergeOut &mo, float *red) {
+  constexpr int kBatch = 8;  // partials whose loads are all in flight together
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int jpr = n_q == 1 ? 1 : (n_q == 2 ? 2 : 4);  // queries per round
+  const int ph = 4 / jpr, phase = w / jpr;
+  const int mo_off = n_q * kD;
+  for (int j0 = 0; j0 < n_q; j0 += jpr) {
+    const int j = j0 + w % jpr;
+    float M = -INFINITY, L = 0.f;
+    float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (j < n_q) {
+      for (int kb = phase; kb < ns; kb += kBatch * ph) {
+        float ms[kBatch], ls[kBatch];
+        float4 os[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          const int k = kb + u * ph;
+          ms[u] = -INFINITY;
+          ls[u] = 0.f;
+          os[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+          // an empty range's slot holds old data: never read into the sums
+          if (k < ns && (!owners || U >= P ||
+                         range_lo(pbase + k, U, P) < range_lo(pbase + k + 1, U, P))) {
+            const float *sk = src + k * kstride;
+            ms[u] = __ldcg(sk + mo_off + j);
+            ls[u] = __ldcg(sk + mo_off + 8 + j);
+            os[u] = __ldcg(reinterpret_cast<const float4 *>(sk + j * kD) + lane);
+          }
+        }
+        float mn = M;
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) mn = fmaxf(mn, ms[u]);
+        if (mn == -INFINITY) continue;  // nothing visible so far
+        const float a = (M == -INFINITY) ? 0.f : fast_exp2(M - mn);
+        L *= a;
+        A.x *= a; A.y *= a; A.z *= a; A.w *= a;
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          const float f = (ms[u] == -INFINITY) ? 0.f : fast_exp2(ms[u] - mn);
+          L = fmaf(f, ls[u], L);
+          A.x = fmaf(f, os[u].x, A.x);
+          A.y = fmaf(f, os[u].y, A.y);
+          A.z = fmaf(f, os[u].z, A.z);
+          A.w = fmaf(f, os[u].w, A.w);
+        }
+        M = mn;
+      }
+    }
+    if (ph > 1) {  // merge the phases (warps jpr apart) through shared memory
+      float *mine = red + 6 * threadIdx.x;
+      mine[0] = M; mine[1] = L; mine[2] = A.x; mine[3] = A.y; mine[4] = A.z; mine[5] = A.w;
+      __syncthreads();
+      if (phase == 0) {
+        for (int q = 1; q < ph; ++q) {
+          const float *o = red + 6 * (threadIdx.x + 32 * jpr * q);
+          const float ms = o[0];
+          const float mn = fmaxf(M, ms);
+          const float a = (M == -INFINITY) ? 0.f : fast_exp2(M - mn);
+          const float f = (ms == -INFINITY) ? 0.f : fast_exp2(ms - mn);
+          L = fmaf(L, a, f * o[1]);
+          A.x = fmaf(A.x, a, f * o[2]);
+          A.y = fmaf(A.y, a, f * o[3]);
+          A.z = fmaf(A.z, a, f * o[4]);
+          A.w = fmaf(A.w, a, f * o[5]);
+          M = mn;
+        }
+      }
+      __syncthreads();  // red is free again; every read of src is done
+    } else {
+      __syncwarp();  // the warp's reads of query j are done before dst is written
+    }
+    if (phase == 0 && j < n_q) {
+      if (mo.final) {
+        const float Ld = L > 0.f ? L : 1.f;  // L > 0 whenever a token is visible
+        uint2 h;
+        h.x = pack_half2(A.x / Ld, A.y / Ld);
+        h.y = pack_half2(A.z / Ld, A.w / Ld);
+        *reinterpret_cast<uint2 *>(mo.out + j * kD + 4 * lane) = h;
+        if (mo.lse && lane == 0) mo.lse[j] = (M + log2f(L)) * 0.69314718055994531f;
+      } else {
+        __stcg(reinterpret_cast<float4 *>(mo.dst + j * kD) + lane, A);
+        if (lane == 0) {
+          __stcg(mo.dst + mo_off + j, M);
+          __stcg(mo.dst + mo_off + 8 + j, L);
+        }
+      }
+    }
+  }
+}
+
+// PK (draft, one query): the MMA's eight query columns hold one real query,
+// so column 2j carries the hi part of B = q * s and column 2j + 1 the lo part
+// for query j = lane / 8 (thread column pair 2c, 2c + 1 = query c): one MMA
+// per k-block instead of two.
+template <int MODE, bool PK>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) split_kernel(const Params prm) {
   using C = Cfg<MODE>;
   using L = Layout<MODE>;
   constexpr int TT = C::kTailTok, S = C::kStages;
   constexpr int kTailTiles = TT / 32;  // 16-token tiles of a buffer chunk per warp
-  static_assert(S % 2 == 0, "the two warp pairs alternate over the stages");
   extern __shared__ __align__(128) uint8_t smem[];
   const qs_cache &c = prm.c;
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -352,15 +479,29 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) split_kernel(const Param
   }
   if (threadIdx.x < 8) reinterpret_cast<uint32_t *>(smem + L::kZeroOff)[threadIdx.x] = 0;
   __shared__ long long s_total;
+  __shared__ int s_abort, s_seg[2], s_need[2], s_last[2];
   pdl_trigger();
   pdl_wait();  // counters, cache and queries are written by earlier kernels
   if (w == 0) {
     const long long tot = build_tables<TT>(c, prm.n_q, T, lane);
-    if (lane == 0) s_total = tot;
+    if (lane == 0) { s_total = tot; s_abort = 0; }
   }
   __syncthreads();
   const long long U = s_total;
   const int p = blockIdx.x;
+  const int stride = prm.n_q * kD + 16;  // floats per partial
+
+  // sequences with n_q > fill see no token: zero outputs, lse = -inf, error
+  for (int b = p; b < c.B; b += prm.P) {
+    if (T.len[b] != 0) continue;
+    const size_t nh = (size_t)c.H * prm.n_q;
+    uint4 *o = reinterpret_cast<uint4 *>(prm.out + (size_t)b * nh * kD);
+    for (size_t i = threadIdx.x; i < nh * (kD / 8); i += kThreads) o[i] = make_uint4(0, 0, 0, 0);
+    if (prm.lse)
+      for (size_t i = threadIdx.x; i < nh; i += kThreads) prm.lse[(size_t)b * nh + i] = -INFINITY;
+    if (threadIdx.x == 0) atomicOr(&c.state[(size_t)b * QS_STATE_WORDS + QS_ST_ERR], QS_DEV_NQ_GT_FILL);
+  }
+
   const long long x0 = range_lo(p, U, prm.P), x1 = range_lo(p + 1, U, prm.P);
   if (x0 >= x1) return;
   const int n = (int)(x1 - x0);
@@ -385,7 +526,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) split_kernel(const Param
   for (int i = 0; i < n; ++i) {
     const size_t bh = (size_t)cur.b * c.H + cur.h;
     if (i == 0 || cur.u == 0) {  // a new piece: this (sequence, head)
-      load_q_pairs(prm.q + (bh * prm.n_q + r) * kD, r < prm.n_q, cq, qp0, qp1);
+      const int qi = PK ? (r >> 1) : r;  // the query in B column r
+      load_q_pairs(prm.q + (bh * prm.n_q + qi) * kD, qi < prm.n_q, cq, qp0, qp1);
       sm.reset();
       fill = T.fill[cur.b];
       ng = T.ng[cur.b];
@@ -393,12 +535,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) split_kernel(const Param
     if ((i & 1) == pr) {
       const int stage = i % S;
       if (!mbar_wait(full0 + 8 * stage, (uint32_t)((i / S) & 1))) {
-        if (lane == 0)
+        if (lane == 0) {
           atomicOr(&c.state[(size_t)cur.b * QS_STATE_WORDS + QS_ST_ERR], QS_DEV_TIMEOUT);
+          s_abort = 1;
+        }
         // bounded drain of the copies still outstanding in this pair's stages
+        // (stage i % S only ever serves units of this pair's parity)
         for (int k = i + 2; k < i + S && k < n; k += 2)
           if (!mbar_wait(full0 + 8 * (k % S), (uint32_t)((k / S) & 1))) break;
-        return;
+        break;  // to the merge, which then only keeps the arrival counts right
       }
       const uint32_t st = sbase + stage * L::kStageBytes;
 
@@ -426,6 +571,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) split_kernel(const Param
           bl1[k0] = hfma2_neg_u32(qp1[k0], sw.y, bh1[k0]);
           bl0[k1] = hfma2_neg_u32(qp0[k1], sw.z, bh0[k1]);
           bl1[k1] = hfma2_neg_u32(qp1[k1], sw.w, bh1[k1]);
+          if (PK && (r & 1)) {  // odd B columns carry the lo part
+            bh0[k0] = bl0[k0]; bh1[k0] = bl1[k0]; bh0[k1] = bl0[k1]; bh1[k1] = bl1[k1];
+          }
           mma16816(bacc, zw.x, sw.x, zw.y, sw.y, qp0[k0], qp1[k0]);
           mma16816(bacc2, zw.z, sw.z, zw.w, sw.w, qp0[k1], qp1[k1]);
         }
@@ -435,7 +583,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) split_kernel(const Param
         const float bk1 =
             fmaf(Centre<MODE>::kOff, bacc[3] + bacc2[3], bacc[1] + bacc2[1]) * prm.sl2;
 
-        // scores: four m-tiles of 16 tokens
+        // raw scores (q.k before scale and bias): four m-tiles of 16 tokens
         float s[4][4];
 #pragma unroll
         for (int mt = 0; mt < 4; ++mt) {
@@ -448,24 +596,30 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) split_kernel(const Param
             l1 = lds128(st + kOffKL + (t0 + 8) * 64 + 16 * cq);
           }
           float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};
-          float acc3[4] = {0.f, 0.f, 0.f, 0.f};
           const uint32_t wu0[4] = {u0.x, u0.y, u0.z, u0.w}, wu1[4] = {u1.x, u1.y, u1.z, u1.w};
           const uint32_t wl0[4] = {l0.x, l0.y, l0.z, l0.w}, wl1[4] = {l1.x, l1.y, l1.z, l1.w};
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {  // independent MMA chains: hi even, hi odd, lo
+          for (int j = 0; j < 4; ++j) {  // two independent MMA chains: even / odd k-blocks
             uint32_t a[4], b8[4];
             pairs<MODE>(wu0[j], wl0[j], a);
             pairs<MODE>(wu1[j], wl1[j], b8);
             mma16816(acc, a[0], b8[0], a[1], b8[1], bh0[2 * j], bh1[2 * j]);
             mma16816(acc2, a[2], b8[2], a[3], b8[3], bh0[2 * j + 1], bh1[2 * j + 1]);
-            mma16816(acc3, a[0], b8[0], a[1], b8[1], bl0[2 * j], bl1[2 * j]);
-            mma16816(acc3, a[2], b8[2], a[3], b8[3], bl0[2 * j + 1], bl1[2 * j + 1]);
+            if (!PK) {
+              mma16816(acc, a[0], b8[0], a[1], b8[1], bl0[2 * j], bl1[2 * j]);
+              mma16816(acc2, a[2], b8[2], a[3], b8[3], bl0[2 * j + 1], bl1[2 * j + 1]);
+            }
           }
-          s[mt][0] = fmaf(acc[0] + acc2[0] + acc3[0], prm.sl2, bk0);
-          s[mt][1] = fmaf(acc[1] + acc2[1] + acc3[1], prm.sl2, bk1);
-          s[mt][2] = fmaf(acc[2] + acc2[2] + acc3[2], prm.sl2, bk0);
-          s[mt][3] = fmaf(acc[3] + acc2[3] + acc3[3], prm.sl2, bk1);
+          if (PK) {  // query c: hi column + lo column, rows r and r + 8
+            s[mt][0] = (acc[0] + acc2[0]) + (acc[1] + acc2[1]);
+            s[mt][2] = (acc[2] + acc2[2]) + (acc[3] + acc2[3]);
+            s[mt][1] = s[mt][3] = -INFINITY;
+          } else {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) s[mt][k] = acc[k] + acc2[k];
+          }
         }
+        // max of scaled scores = max of raw scores * sl2 + bias (sl2 > 0)
         float g0 = fmaxf(s[0][0], s[0][2]), g1 = fmaxf(s[0][1], s[0][3]);
 #pragma unroll
         for (int mt = 1; mt < 4; ++mt) {
@@ -473,7 +627,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) split_kernel(const Param
           g1 = fmaxf(g1, fmaxf(s[mt][1], s[mt][3]));
         }
         float u0, u1, a0, a1;
-        sm.update(warp_max8(g0), warp_max8(g1), u0, u1, a0, a1);
+        sm.update(fmaf(warp_max8(g0), prm.sl2, bk0), fmaf(warp_max8(g1), prm.sl2, bk1), u0, u1, a0,
+                  a1);
+        const float c0 = bk0 - u0, c1 = bk1 - u1;  // p = 2^(raw * sl2 + c)
 
         // probabilities with the value scale folded in, value zero-point as a
         // bias; each value row holds a lane's four tokens of a quarter together
@@ -497,12 +653,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) split_kernel(const Param
             for (int hh = 0; hh < 2; ++hh) {
               const float sv = svs[2 * ml + hh];
               const float zv = fmaf(Centre<MODE>::kOff, sv, zvs[2 * ml + hh]);
-              const float pa = fast_exp2(s[mt][2 * hh] - u0), pb = fast_exp2(s[mt][2 * hh + 1] - u1);
+              const float pa = fast_exp2(fmaf(s[mt][2 * hh], prm.sl2, c0));
+              const float pb = PK ? 0.f : fast_exp2(fmaf(s[mt][2 * hh + 1], prm.sl2, c1));
               sm.l[0] += pa;
               sm.l[1] += pb;
               sm.bv[0] = fmaf(pa, zv, sm.bv[0]);
               sm.bv[1] = fmaf(pb, zv, sm.bv[1]);
-              pv[2 * hh] = pa * sv;
+              // PK: thread column pair (2c, 2c+1) = queries (2c, 2c+1) of the
+              // P' matrix; only c = 0 holds the one real query
+              pv[2 * hh] = (PK && cq != 0) ? 0.f : pa * sv;
               pv[2 * hh + 1] = pb * sv;
             }
             bp0[mt] = movmatrix_trans(pack_half2(pv[0], pv[1]));
@@ -537,34 +696,37 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) split_kernel(const Param
         const int rows = min(TT, fill - i0);
         const int mr0 = 16 * kTailTiles * hw;
         if (mr0 < rows) {
-          const uint32_t *qw = reinterpret_cast<const uint32_t *>(prm.q + (bh * prm.n_q + r) * kD);
-          const bool qv = r < prm.n_q;
-          uint32_t qb0[8], qb1[8];  // natural-order B pairs of q for query r
-#pragma unroll
-          for (int kb = 0; kb < 8; ++kb) {
-            qb0[kb] = qv ? __ldg(qw + 8 * kb + cq) : 0u;
-            qb1[kb] = qv ? __ldg(qw + 8 * kb + cq + 4) : 0u;
-          }
-          const int lim0 = fill - prm.n_q + 2 * cq;  // last visible buffer index, query 2c
+          // key fragments in the same permuted channel order as the quantized
+          // path, built from shared memory (16-byte loads + byte permutes), so
+          // the register-resident q pairs serve as B: no global loads here
+          // last visible buffer index of the thread's first query (2c; PK: c)
+          const int lim0 = fill - prm.n_q + (PK ? cq : 2 * cq);
           float sv[kTailTiles][4];
           float g0 = -INFINITY, g1 = -INFINITY;
 #pragma unroll
           for (int tl = 0; tl < kTailTiles; ++tl) {
             const int mr = mr0 + 16 * tl;
             float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            uint32_t w0[16], w1[16];  // channels 32c..32c+31 of rows mr+r, mr+r+8
+#pragma unroll
+            for (int i4 = 0; i4 < 4; ++i4) {
+              const int ra = mr + r, rb = mr + r + 8;
+              const uint4 x = ra < rows ? lds128(st + ra * kTailRow + 64 * cq + 16 * i4) : make_uint4(0, 0, 0, 0);
+              const uint4 y = rb < rows ? lds128(st + rb * kTailRow + 64 * cq + 16 * i4) : make_uint4(0, 0, 0, 0);
+              w0[4 * i4] = x.x; w0[4 * i4 + 1] = x.y; w0[4 * i4 + 2] = x.z; w0[4 * i4 + 3] = x.w;
+              w1[4 * i4] = y.x; w1[4 * i4 + 1] = y.y; w1[4 * i4 + 2] = y.z; w1[4 * i4 + 3] = y.w;
+            }
 #pragma unroll
             for (int kb = 0; kb < 8; ++kb) {
-              const int row = mr + (lane & 7) + ((lane >> 3) & 1) * 8;
-              const int col = 16 * kb + (lane >> 4) * 8;
-              const uint32_t addr = row < rows ? st + row * kTailRow + col * 2 : zero_row;
-              uint32_t f0, f1, f2, f3;
-              ldmatrix_x4(addr, f0, f1, f2, f3);
-              mma16816(acc, f0, f1, f2, f3, qb0[kb], qb1[kb]);
+              const int k0 = 4 * (kb >> 1) + (kb & 1);
+              mma16816(acc, prmt(w0[k0], w0[k0 + 2], 0x5410), prmt(w1[k0], w1[k0 + 2], 0x5410),
+                       prmt(w0[k0], w0[k0 + 2], 0x7632), prmt(w1[k0], w1[k0 + 2], 0x7632), qp0[kb],
+                       qp1[kb]);
             }
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
               const int tok = mr + r + 8 * (k >> 1);
-              const bool vis = tok < rows && (i0 + tok) <= lim0 + (k & 1);
+              const bool vis = tok < rows && (i0 + tok) <= lim0 + (k & 1) && !(PK && (k & 1));
               sv[tl][k] = vis ? acc[k] * prm.sl2 : -INFINITY;
             }
             g0 = fmaxf(g0, fmaxf(sv[tl][0], sv[tl][2]));
@@ -578,7 +740,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) split_kernel(const Param
             float pv[4];
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-              pv[k] = fast_exp2(sv[tl][k] - ((k & 1) ? u1 : u0));
+              pv[k] = (PK && cq != 0) ? 0.f : fast_exp2(sv[tl][k] - ((k & 1) ? u1 : u0));
               sm.l[k & 1] += pv[k];
             }
             bq0[tl] = movmatrix_trans(pack_half2(pv[0], pv[1]));
@@ -623,7 +785,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) split_kernel(const Param
       // a warp that saw none of the piece writes an empty one (m = -inf)
       const float l0 = warp_sum8(sm.l[0]), l1 = warp_sum8(sm.l[1]);
       const float v0 = warp_sum8(sm.bv[0]), v1 = warp_sum8(sm.bv[1]);
-      const int stride = prm.n_q * kD + 16;
       const long long seg = (long long)cur.b * c.H + cur.h;
       float *dst = prm.ws + ((seg + p) * kConsumers + w) * stride;
       const int j0 = 2 * cq, j1 = 2 * cq + 1;
@@ -645,152 +806,114 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) split_kernel(const Param
     }
     cur.advance(T, c.B, c.H);
   }
-}
 
-// ----------------------------------------------------------- combine kernel
-// One CTA per (32-channel chunk, head, sequence):
-//   M_j = max_s m_sj,  L_j = sum_s 2^(m_sj - M_j) l_sj,
-//   o_jd = sum_s 2^(m_sj - M_j) O_sjd / L_j,   lse_j = (M_j + log2 L_j) ln 2.
-// Warp w takes every 8th partial slot of the segment, lane = channel; each
-// thread merges its slots online in registers (all loads independent, so one
-// memory round trip), then the eight warps merge through shared memory.
-constexpr int kCombineThreads = 256;
-constexpr int kCombineWarps = kCombineThreads / 32;
-constexpr int kChunks = kD / 32;
-
-template <int MODE>
-__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const Params prm) {
-  constexpr int TT = Cfg<MODE>::kTailTok;
-  __shared__ int tab[5 * kMaxB];
-  __shared__ long long s_total;
-  __shared__ float sm_m[kCombineWarps][kMaxQ], sm_l[kCombineWarps][kMaxQ];
-  __shared__ float sm_o[kCombineWarps][kMaxQ][32];
-  const qs_cache &c = prm.c;
-  Tables T{tab, tab + kMaxB, tab + 2 * kMaxB, tab + 3 * kMaxB, tab + 4 * kMaxB};
-  const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z, tid = threadIdx.x;
-  const int warp = tid >> 5, lane = tid & 31;
-  pdl_trigger();
-  pdl_wait();  // the split kernel's partials
-  if (warp == 0) {
-    const long long tot = build_tables<TT>(c, prm.n_q, T, lane);
-    if (lane == 0) s_total = tot;
+  // ---- log-sum-exp merge.  Per piece of this CTA's range: merge the four
+  // warp partials; a segment that lies wholly in the range is final here.  A
+  // segment shared with other CTAs gets one CTA partial (in warp slot 0) and
+  // an arrival on its counter; the CTA that arrives last merges the CTA
+  // partials of the whole segment and resets the counter.  Only the first
+  // and the last piece of a range can be shared.
+  __syncthreads();  // every warp partial is written; the stages are idle
+  const bool aborted = s_abort != 0;
+  float *red = reinterpret_cast<float *>(smem);  // stage memory, free now
+  int n_arr = 0;
+  {
+    Cursor pc;
+    pc.init(x0, T, c.B, c.H);
+    long long x = x0;
+    while (x < x1) {
+      const int b = pc.b, h = pc.h, len = T.len[b];
+      const long long seg = (long long)b * c.H + h;
+      const long long S0 = T.base[b] + (long long)h * len, E0 = S0 + len;
+      const int plo = cta_of(S0, U, prm.P), phi = cta_of(E0 - 1, U, prm.P);
+      float *slots = prm.ws + (size_t)(seg + p) * kConsumers * stride;
+      MergeOut mo{plo == phi, prm.out + (size_t)seg * prm.n_q * kD,
+                  prm.lse ? prm.lse + (size_t)seg * prm.n_q : nullptr, slots};
+      if (!aborted) merge_partials(slots, stride, kConsumers, prm.n_q, false, 0, U, prm.P, mo, red);
+      if (plo != phi) {
+        if (threadIdx.x == 0) {
+          s_seg[n_arr] = (int)seg;
+          s_need[n_arr] = U >= prm.P ? phi - plo + 1 : len;  // one unit per CTA otherwise
+        }
+        ++n_arr;
+      }
+      x = E0 < x1 ? E0 : x1;
+      pc.u = len - 1;
+      pc.advance(T, c.B, c.H);
+    }
+  }
+  if (n_arr == 0) return;
+  __threadfence();  // this CTA's partials are visible before its arrival
+  __syncthreads();
+  if (threadIdx.x < n_arr) {
+    int *ctr = c.arrive + s_seg[threadIdx.x];
+    const int last = atomicAdd(ctr, 1) == s_need[threadIdx.x] - 1;
+    if (last) atomicExch(ctr, 0);  // every other arrival is in: ready for the next call
+    s_last[threadIdx.x] = last;
   }
   __syncthreads();
-  const size_t bh = (size_t)b * c.H + h;
-  const int nq = prm.n_q, d = 32 * chunk + lane;
-  if (T.len[b] == 0) {  // n_q > fill: nothing is visible
-    if (h == 0 && chunk == 0 && tid == 0 && nq > T.fill[b])
-      atomicOr(&c.state[(size_t)b * QS_STATE_WORDS + QS_ST_ERR], QS_DEV_NQ_GT_FILL);
-    if (warp < nq) prm.out[(bh * nq + warp) * kD + d] = 0;
-    if (prm.lse && chunk == 0 && tid < nq) prm.lse[bh * nq + tid] = -INFINITY;
-    return;
-  }
-  const long long U = s_total;
-  const long long S0 = T.base[b] + (long long)h * T.len[b], E0 = S0 + T.len[b];
-  const int plo = cta_of(S0, U, prm.P), phi = cta_of(E0 - 1, U, prm.P);
-  const int nslots = (phi - plo + 1) * kConsumers;
-  const int stride = nq * kD + 16;
-
-  float M[kMaxQ], L[kMaxQ], A[kMaxQ];
-#pragma unroll
-  for (int j = 0; j < kMaxQ; ++j) { M[j] = -INFINITY; L[j] = 0.f; A[j] = 0.f; }
-#pragma unroll 4
-  for (int k = warp; k < nslots; k += kCombineWarps) {
-    const int pp = plo + k / kConsumers;
-    // CTAs between the first and last owner with an empty range (more CTAs
-    // than units) wrote nothing: their slot (still inside the workspace) is
-    // read but masked to -inf
-    const bool owned = range_lo(pp, U, prm.P) < range_lo(pp + 1, U, prm.P);
-    const float *part = prm.ws + ((size_t)(bh + pp) * kConsumers + (k % kConsumers)) * stride;
-#pragma unroll
-    for (int j = 0; j < kMaxQ; ++j) {
-      if (j < nq) {
-        const float msr = part[nq * kD + j], lsr = part[nq * kD + 8 + j], osr = part[j * kD + d];
-        const float ms = owned ? msr : -INFINITY;
-        const float ls = owned ? lsr : 0.f, os = owned ? osr : 0.f;  // never 0 * garbage
-        const float mn = fmaxf(M[j], ms);
-        const float a = (M[j] == -INFINITY) ? 0.f : exp2f(M[j] - mn);
-        const float f = (ms == -INFINITY) ? 0.f : exp2f(ms - mn);
-        L[j] = fmaf(L[j], a, f * ls);
-        A[j] = fmaf(A[j], a, f * os);
-        M[j] = mn;
-      }
-    }
-  }
-#pragma unroll
-  for (int j = 0; j < kMaxQ; ++j) {
-    if (j < nq) {
-      sm_o[warp][j][lane] = A[j];
-      if (lane == 0) { sm_m[warp][j] = M[j]; sm_l[warp][j] = L[j]; }
-    }
-  }
-  __syncthreads();
-  // warp j < nq merges query j across the eight warps
-  if (warp < nq) {
-    const int j = warp;
-    float mx = -INFINITY;
-    for (int w = 0; w < kCombineWarps; ++w) mx = fmaxf(mx, sm_m[w][j]);
-    float l = 0.f, acc = 0.f;
-    for (int w = 0; w < kCombineWarps; ++w) {
-      const float mw = sm_m[w][j];
-      if (mw != -INFINITY) {
-        const float f = exp2f(mw - mx);
-        l = fmaf(f, sm_l[w][j], l);
-        acc = fmaf(f, sm_o[w][j][lane], acc);
-      }
-    }
-    prm.out[(bh * nq + j) * kD + d] = __half_as_ushort(__float2half_rn(acc / l));
-    if (prm.lse && chunk == 0 && lane == 0) prm.lse[bh * nq + j] = (mx + log2f(l)) * 0.69314718055994531f;
+  for (int a = 0; a < n_arr; ++a) {
+    if (!s_last[a] || aborted) continue;
+    __threadfence();
+    const long long seg = s_seg[a];
+    const int b = (int)(seg / c.H), h = (int)(seg % c.H), len = T.len[b];
+    const long long S0 = T.base[b] + (long long)h * len, E0 = S0 + len;
+    const int plo = cta_of(S0, U, prm.P), phi = cta_of(E0 - 1, U, prm.P);
+    MergeOut mo{true, prm.out + (size_t)seg * prm.n_q * kD,
+                prm.lse ? prm.lse + (size_t)seg * prm.n_q : nullptr, nullptr};
+    merge_partials(prm.ws + (size_t)(seg + plo) * kConsumers * stride, (size_t)kConsumers * stride,
+                   phi - plo + 1, prm.n_q, true, plo, U, prm.P, mo, red);
   }
 }
 
 // --------------------------------------------------------------- host side
 struct DevInfo {
-  int ready[2];
-  int grid[2];
+  int ready[4];
+  int grid[4];
 };
 DevInfo g_dev[64];
 
-template <int MODE>
+// Resident CTAs of one split-kernel variant on a device (set up once).
+template <int MODE, bool PK>
 qs_status grid_for_device(int dev, int &P) {
   DevInfo &di = g_dev[dev];
-  if (!__atomic_load_n(&di.ready[MODE], __ATOMIC_ACQUIRE)) {
+  constexpr int v = 2 * MODE + (PK ? 1 : 0);
+  if (!__atomic_load_n(&di.ready[v], __ATOMIC_ACQUIRE)) {
     const int smem = Layout<MODE>::kSmemBytes;
-    if (cudaFuncSetAttribute(split_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(split_kernel<MODE, PK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              smem) != cudaSuccess)
       return QS_ERR_CUDA;
     int sms = 0, occ = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       return QS_ERR_CUDA;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, split_kernel<MODE>, kThreads, smem) !=
-        cudaSuccess)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, split_kernel<MODE, PK>, kThreads,
+                                                      smem) != cudaSuccess)
       return QS_ERR_CUDA;
     if (occ < 1) return QS_ERR_CUDA;
-    di.grid[MODE] = sms * occ;
-    __atomic_store_n(&di.ready[MODE], 1, __ATOMIC_RELEASE);
+    di.grid[v] = sms * occ;
+    __atomic_store_n(&di.ready[v], 1, __ATOMIC_RELEASE);
   }
-  P = di.grid[MODE];
+  P = di.grid[v];
   return QS_OK;
 }
 
-qs_status grid_size(qs_mode mode, int &P) {
+qs_status grid_size(qs_mode mode, bool packed, int &P) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return QS_ERR_CUDA;
   if (dev < 0 || dev >= 64) return QS_ERR_UNSUPPORTED;
-  return mode == QS_DRAFT_UPPER4 ? grid_for_device<QS_DRAFT_UPPER4>(dev, P)
-                                 : grid_for_device<QS_VERIFY_INT8>(dev, P);
+  if (mode == QS_DRAFT_UPPER4)
+    return packed ? grid_for_device<QS_DRAFT_UPPER4, true>(dev, P)
+                  : grid_for_device<QS_DRAFT_UPPER4, false>(dev, P);
+  return grid_for_device<QS_VERIFY_INT8, false>(dev, P);
 }
 
 size_t ws_bytes(int P, int B, int H, int n_q) {
   return (size_t)(P + (size_t)B * H) * kConsumers * (size_t)(n_q * kD + 16) * sizeof(float);
 }
 
-template <int MODE>
+template <int MODE, bool PK>
 qs_status launch(const Params &prm, cudaStream_t s) {
-  qs_status st =
-      launch_pdl(split_kernel<MODE>, dim3(prm.P), dim3(kThreads), Layout<MODE>::kSmemBytes, s, prm);
-  if (st != QS_OK) return st;
-  return launch_pdl(combine_kernel<MODE>, dim3(kChunks, prm.c.H, prm.c.B), dim3(kCombineThreads), 0, s,
+  return launch_pdl(split_kernel<MODE, PK>, dim3(prm.P), dim3(kThreads), Layout<MODE>::kSmemBytes, s,
                     prm);
 }
 
@@ -805,10 +928,12 @@ qs_status qs_attn_workspace_size(const qs_cache *c, int32_t n_q, size_t *bytes) 
   qs_status s = check_cache(c);
   if (s != QS_OK) return s;
   if (!bytes || n_q < 1 || n_q > kMaxQ) return QS_ERR_ARG;
-  int P0 = 0, P1 = 0;
-  if ((s = grid_size(QS_DRAFT_UPPER4, P0)) != QS_OK) return s;
-  if ((s = grid_size(QS_VERIFY_INT8, P1)) != QS_OK) return s;
-  *bytes = ws_bytes(P0 > P1 ? P0 : P1, c->B, c->H, n_q);
+  int P0 = 0, P1 = 0, P2 = 0;
+  if ((s = grid_size(QS_DRAFT_UPPER4, false, P0)) != QS_OK) return s;
+  if ((s = grid_size(QS_DRAFT_UPPER4, true, P1)) != QS_OK) return s;
+  if ((s = grid_size(QS_VERIFY_INT8, false, P2)) != QS_OK) return s;
+  const int P = P0 > P1 ? (P0 > P2 ? P0 : P2) : (P1 > P2 ? P1 : P2);
+  *bytes = ws_bytes(P, c->B, c->H, n_q);
   return QS_OK;
 }
 
@@ -828,14 +953,15 @@ qs_status qs_attn_decode(const qs_cache *c, qs_mode mode, const uint16_t *q, int
   prm.lse = lse;
   prm.n_q = n_q;
   prm.sl2 = softmax_scale * 1.4426950408889634f;
-  if ((s = grid_size(mode, prm.P)) != QS_OK) return s;
+  const bool packed = (mode == QS_DRAFT_UPPER4 && n_q == 1);
+  if ((s = grid_size(mode, packed, prm.P)) != QS_OK) return s;
   if (!workspace || !aligned16(workspace) ||
       workspace_bytes < ws_bytes(prm.P, c->B, c->H, n_q))
     return QS_ERR_WORKSPACE;
   prm.ws = static_cast<float *>(workspace);
   cudaStream_t st = (cudaStream_t)stream;
-  return mode == QS_DRAFT_UPPER4 ? launch<QS_DRAFT_UPPER4>(prm, st)
-                                 : launch<QS_VERIFY_INT8>(prm, st);
+  if (mode == QS_VERIFY_INT8) return launch<QS_VERIFY_INT8, false>(prm, st);
+  return packed ? launch<QS_DRAFT_UPPER4, true>(prm, st) : launch<QS_DRAFT_UPPER4, false>(prm, st);
 }
 
 }  // extern "C"

@@ -111,6 +111,7 @@ qs_status qs_cache_bytes(int32_t B, int32_t H, int32_t D, int32_t G, int32_t cap
   out->meta = bh * cap * 4 * 128 * 2;
   out->buf_k = out->buf_v = bh * 2 * G * D * 2;
   out->state = (size_t)B * QS_STATE_WORDS * 4;
+  out->arrive = bh * 4;
   return QS_OK;
 }
 
@@ -119,6 +120,8 @@ qs_status qs_state_reset(const qs_cache *c, qs_stream_t stream) {
   if (s != QS_OK) return s;
   cudaError_t e = cudaMemsetAsync(c->state, 0, (size_t)c->B * QS_STATE_WORDS * 4,
                                   (cudaStream_t)stream);
+  if (e == cudaSuccess)
+    e = cudaMemsetAsync(c->arrive, 0, (size_t)c->B * c->H * 4, (cudaStream_t)stream);
   return e == cudaSuccess ? QS_OK : QS_ERR_CUDA;
 }
 

@@ -24,13 +24,13 @@ constexpr int kMaxQ = 8;        // queries per call (one n8 MMA tile)
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 inline qs_status check_cache(const qs_cache *c) {
-  if (!c || !c->state || !c->buf_k || !c->buf_v) return QS_ERR_ARG;
+  if (!c || !c->state || !c->arrive || !c->buf_k || !c->buf_v) return QS_ERR_ARG;
   if (c->B <= 0 || c->H <= 0 || c->cap_groups <= 0) return QS_ERR_SHAPE;
   if (c->D != kD || c->G != kG) return QS_ERR_UNSUPPORTED;
   if (c->B > kMaxB) return QS_ERR_UNSUPPORTED;
   if (!c->k_upper || !c->k_lower || !c->v_upper || !c->v_lower || !c->meta) return QS_ERR_ARG;
   const void *ps[] = {c->k_upper, c->k_lower, c->v_upper, c->v_lower,
-                      c->meta,    c->buf_k,   c->buf_v,   c->state};
+                      c->meta,    c->buf_k,   c->buf_v,   c->state, c->arrive};
   for (const void *p : ps)
     if (!aligned16(p)) return QS_ERR_ALIGN;
   return QS_OK;

@@ -30,12 +30,13 @@ _I32 = ctypes.c_int32
 class QsCacheStruct(ctypes.Structure):
     _fields_ = [("B", _I32), ("H", _I32), ("D", _I32), ("G", _I32), ("cap_groups", _I32),
                 ("k_upper", _P), ("k_lower", _P), ("v_upper", _P), ("v_lower", _P),
-                ("meta", _P), ("buf_k", _P), ("buf_v", _P), ("state", _P)]
+                ("meta", _P), ("buf_k", _P), ("buf_v", _P), ("state", _P), ("arrive", _P)]
 
 
 class QsCacheBytes(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in
-                ("k_upper", "k_lower", "v_upper", "v_lower", "meta", "buf_k", "buf_v", "state")]
+                ("k_upper", "k_lower", "v_upper", "v_lower", "meta", "buf_k", "buf_v", "state",
+                 "arrive")]
 
 
 class QsError(RuntimeError):
@@ -127,17 +128,19 @@ class Cache:
         self.buf_k = torch.zeros((B, H, 2 * G, D), **f16)
         self.buf_v = torch.zeros((B, H, 2 * G, D), **f16)
         self.state = torch.zeros((B, STATE_WORDS), dtype=torch.int32, device=device)
+        self.arrive = torch.zeros((B, H), dtype=torch.int32, device=device)
         self.struct = QsCacheStruct(B, H, D, G, cap_groups,
                                     self.k_upper.data_ptr(), self.k_lower.data_ptr(),
                                     self.v_upper.data_ptr(), self.v_lower.data_ptr(),
                                     self.meta.data_ptr(), self.buf_k.data_ptr(),
-                                    self.buf_v.data_ptr(), self.state.data_ptr())
+                                    self.buf_v.data_ptr(), self.state.data_ptr(),
+                                    self.arrive.data_ptr())
         self._ref = ctypes.byref(self.struct)
 
     def nbytes(self):
         return sum(t.numel() * t.element_size() for t in
                    (self.k_upper, self.k_lower, self.v_upper, self.v_lower, self.meta,
-                    self.buf_k, self.buf_v, self.state))
+                    self.buf_k, self.buf_v, self.state, self.arrive))
 
 
 def qs_state_reset(cache, stream=None):

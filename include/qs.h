@@ -125,6 +125,10 @@ enum { QS_META_K_SCALE = 0, QS_META_K_ZERO = 1, QS_META_V_SCALE = 2, QS_META_V_Z
  *  buf_k, buf_v  fp16 [B][H][2G][D]: the double full-precision buffer.
  *  state  int32 [B][QS_STATE_WORDS]: counters above; zero it (qs_state_reset)
  *      before first use.
+ *  arrive  int32 [B][H]: arrival counters of qs_attn_decode (the CTA that
+ *      finishes a head last merges its split partials).  Internal: zeroed by
+ *      qs_state_reset and left at zero by every completed attention call, so
+ *      at most one attention call may run on a cache at a time.
  */
 typedef struct {
   int32_t B, H, D, G, cap_groups;
@@ -132,10 +136,11 @@ typedef struct {
   uint16_t *meta;         /* fp16 bits */
   uint16_t *buf_k, *buf_v; /* fp16 bits */
   int32_t *state;
+  int32_t *arrive;
 } qs_cache;
 
 typedef struct {
-  size_t k_upper, k_lower, v_upper, v_lower, meta, buf_k, buf_v, state;
+  size_t k_upper, k_lower, v_upper, v_lower, meta, buf_k, buf_v, state, arrive;
 } qs_cache_bytes_t;
 
 /* Byte size of every cache array for the given dimensions.  Pure host
@@ -144,7 +149,8 @@ typedef struct {
 qs_status qs_cache_bytes(int32_t B, int32_t H, int32_t D, int32_t G, int32_t cap_groups,
                          qs_cache_bytes_t *out);
 
-/* Zero every sequence's counters (empty cache).  Asynchronous memset. */
+/* Zero every sequence's counters (empty cache) and the attention arrival
+ * counters.  Asynchronous memsets. */
 qs_status qs_state_reset(const qs_cache *c, qs_stream_t stream);
 
 /* Append n_new tokens per sequence to the fp16 buffer as pending tokens.

@@ -39,13 +39,14 @@ def test_cache_bytes_and_unsupported_sizes(L):
     assert b["meta"] == 2 * 3 * 5 * 4 * 128 * 2
     assert b["buf_k"] == 2 * 3 * 256 * 128 * 2
     assert b["state"] == 2 * 8 * 4
+    assert b["arrive"] == 2 * 3 * 4
     out = qs.QsCacheBytes()
     assert L.qs_cache_bytes(1, 1, 64, 128, 1, ctypes.byref(out)) == qs.QS_ERR_UNSUPPORTED
     assert L.qs_cache_bytes(0, 1, 128, 128, 1, ctypes.byref(out)) == qs.QS_ERR_ARG
 
 
 def _fake_cache(**kw):
-    c = qs.QsCacheStruct(1, 2, 128, 128, 4, *([0x10000] * 8))
+    c = qs.QsCacheStruct(1, 2, 128, 128, 4, *([0x10000] * 9))
     for k, v in kw.items():
         setattr(c, k, v)
     return c
@@ -55,6 +56,10 @@ def test_host_validation_before_any_cuda_call(L):
     assert L.qs_state_reset(None, None) == qs.QS_ERR_ARG
     c = _fake_cache(state=0x10008)
     assert L.qs_state_reset(ctypes.byref(c), None) == qs.QS_ERR_ALIGN
+    c = _fake_cache(arrive=0x10004)
+    assert L.qs_state_reset(ctypes.byref(c), None) == qs.QS_ERR_ALIGN
+    c = _fake_cache(arrive=None)
+    assert L.qs_state_reset(ctypes.byref(c), None) == qs.QS_ERR_ARG
     c = _fake_cache(D=96)
     assert L.qs_state_reset(ctypes.byref(c), None) == qs.QS_ERR_UNSUPPORTED
     c = _fake_cache(B=300)
