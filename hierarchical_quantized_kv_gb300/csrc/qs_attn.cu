@@ -140,13 +140,16 @@ __device__ long long build_tables(const qs_cache &c, int n_q, Tables T, int lane
   return (long long)__shfl_sync(0xffffffffu, incl, 31) * c.H;
 }
 
-// CTA p owns units [floor(p U / P), floor((p+1) U / P)).
+// CTA p owns units [range_lo(p), range_lo(p + 1)): floor(p U / P) onwards
+// when there are at least as many units as CTAs, else unit p alone (CTAs
+// p >= U idle).  Either way every CTA between a segment's first and last
+// owner owns part of it.
 __device__ __forceinline__ long long range_lo(int p, long long U, int P) {
-  return (long long)p * U / P;
+  return U >= P ? (long long)p * U / P : (p < U ? p : U);
 }
 // The CTA whose range holds unit x.
 __device__ __forceinline__ int cta_of(long long x, long long U, int P) {
-  return (int)(((x + 1) * P - 1) / U);
+  return U >= P ? (int)(((x + 1) * P - 1) / U) : (int)x;
 }
 
 struct Cursor {
@@ -345,13 +348,11 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 //   O_j = sum_k 2^(m_kj - M_j) O_kj.
 // final: out_j = O_j / L_j (fp16) and lse_j = (M_j + log2 L_j) ln 2; else the
 // merged partial is written to dst (same layout; dst may be partial 0).
-// With fewer units than CTAs some CTAs own no unit and write no partial: when
-// `owners` is set, partial k belongs to CTA pbase + k and is skipped if that
-// CTA's range is empty.
 // Lanes hold four channels each; the four warps take four queries at a time,
 // or (one or two queries) split the partials into phases merged through `red`
 // (128 x 6 floats of shared memory).  Each thread loads its partials eight at
-// a time, all eight in flight before the first is used.
+// a time, all eight in flight before the first is used.  SHARED: src is in
+// shared memory, else in global memory written by other CTAs (read from L2).
 struct MergeOut {
   bool final;
   uint16_t *out;  // final: fp16 [n_q][128] of this (sequence, head)
@@ -359,8 +360,18 @@ struct MergeOut {
   float *dst;     // partial
 };
 
-__device__ void merge_partials(const float *src, size_t kstride, int ns, int n_q, bool owners,
-                               int pbase, long long U, int P, const MergeOut &mo, float *red) {
+template <bool SHARED>
+__device__ __forceinline__ float ld_part(const float *p) {
+  return SHARED ? *p : __ldcg(p);
+}
+template <bool SHARED>
+__device__ __forceinline__ float4 ld_part4(const float *p) {
+  return SHARED ? *reinterpret_cast<const float4 *>(p) : __ldcg(reinterpret_cast<const float4 *>(p));
+}
+
+template <bool SHARED>
+__device__ void merge_partials(const float *src, int kstride, int ns, int n_q, const MergeOut &mo,
+                               float *red) {
   constexpr int kBatch = 8;  // partials whose loads are all in flight together
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int jpr = n_q == 1 ? 1 : (n_q == 2 ? 2 : 4);  // queries per round
@@ -380,13 +391,11 @@ __device__ void merge_partials(const float *src, size_t kstride, int ns, int n_q
           ms[u] = -INFINITY;
           ls[u] = 0.f;
           os[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-          // an empty range's slot holds old data: never read into the sums
-          if (k < ns && (!owners || U >= P ||
-                         range_lo(pbase + k, U, P) < range_lo(pbase + k + 1, U, P))) {
+          if (k < ns) {
             const float *sk = src + k * kstride;
-            ms[u] = __ldcg(sk + mo_off + j);
-            ls[u] = __ldcg(sk + mo_off + 8 + j);
-            os[u] = __ldcg(reinterpret_cast<const float4 *>(sk + j * kD) + lane);
+            ms[u] = ld_part<SHARED>(sk + mo_off + j);
+            ls[u] = ld_part<SHARED>(sk + mo_off + 8 + j);
+            os[u] = ld_part4<SHARED>(sk + j * kD + 4 * lane);
           }
         }
         float mn = M;
@@ -447,6 +456,31 @@ __device__ void merge_partials(const float *src, size_t kstride, int ns, int n_q
         }
       }
     }
+  }
+}
+
+// One warp's partial of a piece (unnormalized, log2 domain; m = -inf if the
+// warp saw no visible token) in the layout merge_partials reads; dst is in
+// global or shared memory.
+__device__ __forceinline__ void write_partial(const Softmax &sm, float *dst, int n_q, int lane) {
+  const int r = lane >> 2, cq = lane & 3;
+  const float l0 = warp_sum8(sm.l[0]), l1 = warp_sum8(sm.l[1]);
+  const float v0 = warp_sum8(sm.bv[0]), v1 = warp_sum8(sm.bv[1]);
+  const int j0 = 2 * cq, j1 = 2 * cq + 1;
+#pragma unroll
+  for (int md = 0; md < 8; ++md) {
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const int d = 16 * md + r + 8 * hh;
+      if (j0 < n_q) dst[j0 * kD + d] = sm.o[md][2 * hh] + v0;
+      if (j1 < n_q) dst[j1 * kD + d] = sm.o[md][2 * hh + 1] + v1;
+    }
+  }
+  if (r == 0) {
+    const float m0 = sm.m[0] == -INFINITY ? -INFINITY : sm.m[0] - kExpShift;
+    const float m1 = sm.m[1] == -INFINITY ? -INFINITY : sm.m[1] - kExpShift;
+    if (j0 < n_q) { dst[n_q * kD + j0] = m0; dst[n_q * kD + 8 + j0] = l0; }
+    if (j1 < n_q) { dst[n_q * kD + j1] = m1; dst[n_q * kD + 8 + j1] = l1; }
   }
 }
 
@@ -780,42 +814,27 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) split_kernel(const Param
     }
     if (i + S < n) ahead.advance(T, c.B, c.H);
 
-    if (i + 1 == n || cur.u + 1 == T.len[cur.b]) {
-      // ---- piece done: one partial per warp (unnormalized, log2 domain);
-      // a warp that saw none of the piece writes an empty one (m = -inf)
-      const float l0 = warp_sum8(sm.l[0]), l1 = warp_sum8(sm.l[1]);
-      const float v0 = warp_sum8(sm.bv[0]), v1 = warp_sum8(sm.bv[1]);
+    if (i + 1 < n && cur.u + 1 == T.len[cur.b]) {
+      // piece done before the range ends: this warp's partial to its slot
       const long long seg = (long long)cur.b * c.H + cur.h;
-      float *dst = prm.ws + ((seg + p) * kConsumers + w) * stride;
-      const int j0 = 2 * cq, j1 = 2 * cq + 1;
-#pragma unroll
-      for (int md = 0; md < 8; ++md) {
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const int d = 16 * md + r + 8 * hh;
-          if (j0 < prm.n_q) dst[j0 * kD + d] = sm.o[md][2 * hh] + v0;
-          if (j1 < prm.n_q) dst[j1 * kD + d] = sm.o[md][2 * hh + 1] + v1;
-        }
-      }
-      if (r == 0) {
-        const float m0 = sm.m[0] == -INFINITY ? -INFINITY : sm.m[0] - kExpShift;
-        const float m1 = sm.m[1] == -INFINITY ? -INFINITY : sm.m[1] - kExpShift;
-        if (j0 < prm.n_q) { dst[prm.n_q * kD + j0] = m0; dst[prm.n_q * kD + 8 + j0] = l0; }
-        if (j1 < prm.n_q) { dst[prm.n_q * kD + j1] = m1; dst[prm.n_q * kD + 8 + j1] = l1; }
-      }
+      write_partial(sm, prm.ws + ((seg + p) * kConsumers + w) * stride, prm.n_q, lane);
     }
     cur.advance(T, c.B, c.H);
   }
 
   // ---- log-sum-exp merge.  Per piece of this CTA's range: merge the four
-  // warp partials; a segment that lies wholly in the range is final here.  A
+  // warp partials (the last piece's straight from registers through shared
+  // memory); a segment that lies wholly in the range is final here.  A
   // segment shared with other CTAs gets one CTA partial (in warp slot 0) and
   // an arrival on its counter; the CTA that arrives last merges the CTA
   // partials of the whole segment and resets the counter.  Only the first
   // and the last piece of a range can be shared.
-  __syncthreads();  // every warp partial is written; the stages are idle
+  __syncthreads();  // the stages are idle
   const bool aborted = s_abort != 0;
-  float *red = reinterpret_cast<float *>(smem);  // stage memory, free now
+  float *red = reinterpret_cast<float *>(smem);                   // stage memory, free now
+  float *last_part = reinterpret_cast<float *>(smem + 4096);     // 4 partials
+  if (!aborted) write_partial(sm, last_part + w * stride, prm.n_q, lane);
+  __syncthreads();
   int n_arr = 0;
   {
     Cursor pc;
@@ -827,13 +846,16 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) split_kernel(const Param
       const long long S0 = T.base[b] + (long long)h * len, E0 = S0 + len;
       const int plo = cta_of(S0, U, prm.P), phi = cta_of(E0 - 1, U, prm.P);
       float *slots = prm.ws + (size_t)(seg + p) * kConsumers * stride;
-      MergeOut mo{plo == phi, prm.out + (size_t)seg * prm.n_q * kD,
-                  prm.lse ? prm.lse + (size_t)seg * prm.n_q : nullptr, slots};
-      if (!aborted) merge_partials(slots, stride, kConsumers, prm.n_q, false, 0, U, prm.P, mo, red);
+      const MergeOut mo{plo == phi, prm.out + (size_t)seg * prm.n_q * kD,
+                        prm.lse ? prm.lse + (size_t)seg * prm.n_q : nullptr, slots};
+      if (!aborted) {
+        if (E0 >= x1) merge_partials<true>(last_part, stride, kConsumers, prm.n_q, mo, red);
+        else merge_partials<false>(slots, stride, kConsumers, prm.n_q, mo, red);
+      }
       if (plo != phi) {
         if (threadIdx.x == 0) {
           s_seg[n_arr] = (int)seg;
-          s_need[n_arr] = U >= prm.P ? phi - plo + 1 : len;  // one unit per CTA otherwise
+          s_need[n_arr] = phi - plo + 1;
         }
         ++n_arr;
       }
@@ -843,26 +865,28 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) split_kernel(const Param
     }
   }
   if (n_arr == 0) return;
-  __threadfence();  // this CTA's partials are visible before its arrival
-  __syncthreads();
+  __syncthreads();  // this CTA's partials are written (made visible by the fence below)
   if (threadIdx.x < n_arr) {
     int *ctr = c.arrive + s_seg[threadIdx.x];
+    __threadfence();
     const int last = atomicAdd(ctr, 1) == s_need[threadIdx.x] - 1;
-    if (last) atomicExch(ctr, 0);  // every other arrival is in: ready for the next call
+    if (last) {
+      atomicExch(ctr, 0);  // every other arrival is in: ready for the next call
+      __threadfence();     // the other CTAs' partials are visible from here on
+    }
     s_last[threadIdx.x] = last;
   }
   __syncthreads();
   for (int a = 0; a < n_arr; ++a) {
     if (!s_last[a] || aborted) continue;
-    __threadfence();
     const long long seg = s_seg[a];
     const int b = (int)(seg / c.H), h = (int)(seg % c.H), len = T.len[b];
     const long long S0 = T.base[b] + (long long)h * len, E0 = S0 + len;
     const int plo = cta_of(S0, U, prm.P), phi = cta_of(E0 - 1, U, prm.P);
-    MergeOut mo{true, prm.out + (size_t)seg * prm.n_q * kD,
-                prm.lse ? prm.lse + (size_t)seg * prm.n_q : nullptr, nullptr};
-    merge_partials(prm.ws + (size_t)(seg + plo) * kConsumers * stride, (size_t)kConsumers * stride,
-                   phi - plo + 1, prm.n_q, true, plo, U, prm.P, mo, red);
+    const MergeOut mo{true, prm.out + (size_t)seg * prm.n_q * kD,
+                      prm.lse ? prm.lse + (size_t)seg * prm.n_q : nullptr, nullptr};
+    merge_partials<false>(prm.ws + (size_t)(seg + plo) * kConsumers * stride, kConsumers * stride,
+                          phi - plo + 1, prm.n_q, mo, red);
   }
 }
 
