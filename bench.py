@@ -92,6 +92,13 @@ def append_bytes(n, BH):
     return BH * n * 512 * 2
 
 
+def prefill_bytes(L, BH, G=128):
+    """qs_prefill of an L-token prompt: read K and V, write the groups
+    (both planes + meta, 33,792 B per group-head) and the buffer tokens."""
+    ng = 0 if L <= 2 * G else -(-(L - 2 * G) // G)
+    return BH * (L * 512 + ng * 33792 + (L - ng * G) * 512)
+
+
 # --------------------------------------------------------------- clocks
 
 class ClockSampler:
@@ -342,6 +349,21 @@ def native(args):
     flush_us = time_calls(torch, lambda: qs.qs_quantize_flush(r.cache, None),
                           lambda: r.cache.state.copy_(r.state0), it, l2)
     r.cache.state.copy_(r.state0)
+    # bulk prefill of the whole prompt (one sequence of the workload) into a
+    # second cache: one call quantizes every group and fills the buffer
+    prefill_us = prefill_gbs = None
+    if w.B == 1:
+        T = w.context[0]
+        kp, vp = synthetic.kv_tokens(w, 0, 0, T)
+        kp = torch.from_numpy(kp[None]).cuda()
+        vp = torch.from_numpy(vp[None]).cuda()
+        lens = torch.tensor([T], dtype=torch.int32, device="cuda")
+        pc = qs.Cache(1, w.H, r.cache.cap)
+        prefill_us = time_calls(torch, lambda: qs.qs_prefill(pc, kp, vp, lens),
+                                lambda: qs.qs_state_reset(pc), it, l2)
+        assert torch.equal(pc.state[0, :4].cpu(), r.state0[0, :4].cpu())
+        prefill_gbs = prefill_bytes(T, w.H) / prefill_us / 1e3
+        del kp, vp, pc
     draft_b, verify_b = r.bytes["draft"][0], r.bytes["verify"]
     draft_gbs, verify_gbs = draft_b / draft_us / 1e3, verify_b / verify_us / 1e3
     # dominant kernel by device time within a step
@@ -391,6 +413,8 @@ def native(args):
         "draft_us": round(draft_us, 2), "draft_gbs": round(draft_gbs, 1),
         "verify_us": round(verify_us, 2), "verify_gbs": round(verify_gbs, 1),
         "flush_us": round(flush_us, 2),
+        "prefill_us": None if prefill_us is None else round(prefill_us, 2),
+        "prefill_gbs": None if prefill_gbs is None else round(prefill_gbs, 1),
         "roofline": {"bound": "hbm", "kernel": "qs_attn_decode %s (split_kernel: split-KV attention + LSE merge, one launch)" % dominant[0],
                      "achieved": round(dominant[1], 1), "peak": peak,
                      "peak_kind": "%s hbm_gbs (copy, burst)" % peak_kind, "unit": "GB/s",

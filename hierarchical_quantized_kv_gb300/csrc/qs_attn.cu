@@ -41,9 +41,9 @@
 namespace qs {
 namespace {
 
-constexpr int kConsumers = 4;
-constexpr int kThreads = kConsumers * 32;
-constexpr int kCtasPerSm = 3;
+constexpr int kPairs = 6;               // warp pairs per CTA; a pair computes one unit
+constexpr int kWarps = 2 * kPairs;
+constexpr int kThreads = kWarps * 32;  // one CTA per SM
 constexpr int kTailRow = 272;  // padded fp16 row stride (bytes) of buffer tiles
 constexpr int kOffKU = 0, kOffVU = 8192, kOffMeta = 16384, kOffKL = 17408, kOffVL = 25600;
 
@@ -53,16 +53,13 @@ template <>
 struct Cfg<QS_DRAFT_UPPER4> {
   static constexpr int kGroupBytes = 8192 + 8192 + 1024;
   static constexpr int kTailTok = 32;
-  static constexpr int kStages = 4;
+  static constexpr int kStages = 2 * kPairs;  // a unit in compute and one in flight per pair
 };
-#ifndef QS_VERIFY_STAGES
-#define QS_VERIFY_STAGES 2
-#endif
 template <>
 struct Cfg<QS_VERIFY_INT8> {
   static constexpr int kGroupBytes = 4 * 8192 + 1024;
   static constexpr int kTailTok = 64;
-  static constexpr int kStages = QS_VERIFY_STAGES;
+  static constexpr int kStages = kPairs;
 };
 
 constexpr int align16(int x) { return (x + 15) & ~15; }
@@ -74,10 +71,13 @@ struct Layout {
       Cfg<MODE>::kGroupBytes > kTailBytes ? Cfg<MODE>::kGroupBytes : kTailBytes;
   static constexpr int kBarOff = Cfg<MODE>::kStages * kStageBytes;               // full barriers
   static constexpr int kCntOff = align16(kBarOff + 8 * Cfg<MODE>::kStages);      // release counters
-  static constexpr int kZeroOff = align16(kCntOff + 4 * Cfg<MODE>::kStages);     // zero row (ldmatrix)
+  static constexpr int kIssOff = align16(kCntOff + 4 * Cfg<MODE>::kStages);      // unit per stage
+  static constexpr int kClaimOff = align16(kIssOff + 4 * Cfg<MODE>::kStages);    // claimed units
+  static constexpr int kZeroOff = align16(kClaimOff + 4 * 2 * kPairs);          // zero row (ldmatrix)
   static constexpr int kTabOff = kZeroOff + 32;
-  // per-sequence tables: n_groups, fill, half_base, segment length, base unit
-  static constexpr int kSmemBytes = kTabOff + 5 * kMaxB * 4;
+  // per-sequence tables: n_groups, fill, half_base, segment length, base
+  // unit, first segment ordinal
+  static constexpr int kSmemBytes = kTabOff + 6 * kMaxB * 4;
   static_assert(kStageBytes % 16 == 0 && kBarOff % 16 == 0 && kZeroOff % 16 == 0,
                 "bulk copies and ldmatrix rows need 16-byte aligned shared memory");
 };
@@ -95,20 +95,23 @@ struct Params {
 
 struct Tables {
   int *ng, *fill, *hb, *len, *base;  // base in units, len in units per head
+  int *ord0;  // ordinal of (b, head 0) among the segments that have units
 };
 
 __device__ __forceinline__ Tables tables_at(uint8_t *smem, int off) {
   int *t = reinterpret_cast<int *>(smem + off);
-  return Tables{t, t + kMaxB, t + 2 * kMaxB, t + 3 * kMaxB, t + 4 * kMaxB};
+  return Tables{t, t + kMaxB, t + 2 * kMaxB, t + 3 * kMaxB, t + 4 * kMaxB, t + 5 * kMaxB};
 }
 
-// Warp-cooperative: read counters, segment lengths (units per head) and the
-// exclusive prefix of units (x H) into the tables.  Returns the total.
+// Warp-cooperative: read counters, segment lengths (units per head), the
+// exclusive prefix of units (x H) and the ordinal of each sequence's first
+// segment (segments of sequences without units are skipped) into the tables.
+// Returns the total number of units.
 template <int TT>
 __device__ long long build_tables(const qs_cache &c, int n_q, Tables T, int lane) {
   const int per = (c.B + 31) / 32;
   const int b0 = lane * per;
-  int local = 0;
+  int local = 0, local_ne = 0;
   for (int i = 0; i < per; ++i) {
     const int b = b0 + i;
     if (b < c.B) {
@@ -122,19 +125,24 @@ __device__ long long build_tables(const qs_cache &c, int n_q, Tables T, int lane
       const int len = (n_q <= fill) ? ng + (fill + TT - 1) / TT : 0;
       T.len[b] = len;
       local += len;
+      local_ne += len > 0;
     }
   }
-  int incl = local;
+  int incl = local, incl_ne = local_ne;
   for (int o = 1; o < 32; o <<= 1) {
     const int v = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += v;
+    const int v_ne = __shfl_up_sync(0xffffffffu, incl_ne, o);
+    if (lane >= o) { incl += v; incl_ne += v_ne; }
   }
   long long run = (long long)(incl - local) * c.H;
+  int run_ne = (incl_ne - local_ne) * c.H;
   for (int i = 0; i < per; ++i) {
     const int b = b0 + i;
     if (b < c.B) {
       T.base[b] = (int)run;
+      T.ord0[b] = run_ne;
       run += (long long)T.len[b] * c.H;
+      run_ne += T.len[b] > 0 ? c.H : 0;
     }
   }
   return (long long)__shfl_sync(0xffffffffu, incl, 31) * c.H;
@@ -149,28 +157,34 @@ __device__ __forceinline__ long long range_lo(int p, long long U, int P) {
 }
 // The CTA whose range holds unit x.
 __device__ __forceinline__ int cta_of(long long x, long long U, int P) {
-  return U >= P ? (int)(((x + 1) * P - 1) / U) : (int)x;
+  if (U < P) return (int)x;
+  if (U * P < (1ll << 32))  // 32-bit division
+    return (int)(((uint32_t)(x + 1) * (uint32_t)P - 1u) / (uint32_t)U);
+  return (int)(((x + 1) * P - 1) / U);
 }
 
-struct Cursor {
-  int b, h, u;
-  __device__ void init(long long x, const Tables &T, int B, int H) {
-    int lo = 0, hi = B - 1;  // largest b with base[b] <= x
+// Where unit x lies: sequence b, head h, unit u of the (b, h) segment, whose
+// first unit is s0 and whose ordinal among the segments with units is ord.
+// seek() costs a compare while x stays in the current segment.
+struct Seg {
+  int b = -1, h = 0, u = 0, s0 = 0, len = 0, ord = 0;
+  __device__ void seek(int x, const Tables &T, int B) {
+    if (b >= 0 && x >= s0 && x < s0 + len) {
+      u = x - s0;
+      return;
+    }
+    int lo = 0, hi = B - 1;  // largest b with base[b] <= x (that one has units)
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
       if (T.base[mid] <= x) lo = mid; else hi = mid - 1;
     }
     b = lo;
-    const long long off = x - T.base[b];
-    h = (int)(off / T.len[b]);
-    u = (int)(off % T.len[b]);
-  }
-  __device__ void advance(const Tables &T, int B, int H) {
-    if (++u < T.len[b]) return;
-    u = 0;
-    if (++h < H) return;
-    h = 0;
-    do { ++b; } while (b < B && T.len[b] == 0);
+    len = T.len[b];
+    const int off = x - T.base[b];
+    h = off / len;
+    s0 = T.base[b] + h * len;
+    u = x - s0;
+    ord = T.ord0[b] + h;
   }
 };
 
@@ -301,7 +315,7 @@ __device__ __forceinline__ void load_q_pairs(const uint16_t *qrow, bool valid, i
 
 // Issue the bulk copies of one unit into a stage (called by one whole warp).
 template <int MODE>
-__device__ __forceinline__ void issue_unit(const qs_cache &c, const Tables &T, const Cursor &cu,
+__device__ __forceinline__ void issue_unit(const qs_cache &c, const Tables &T, const Seg &cu,
                                            uint32_t dst, uint32_t bar, int lane) {
   using C = Cfg<MODE>;
   constexpr int TT = C::kTailTok;
@@ -348,11 +362,13 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 //   O_j = sum_k 2^(m_kj - M_j) O_kj.
 // final: out_j = O_j / L_j (fp16) and lse_j = (M_j + log2 L_j) ln 2; else the
 // merged partial is written to dst (same layout; dst may be partial 0).
-// Lanes hold four channels each; the four warps take four queries at a time,
-// or (one or two queries) split the partials into phases merged through `red`
-// (128 x 6 floats of shared memory).  Each thread loads its partials eight at
-// a time, all eight in flight before the first is used.  SHARED: src is in
-// shared memory, else in global memory written by other CTAs (read from L2).
+// Lanes hold four channels each.  The twelve warps take jpr queries at once
+// (the smallest divisor of twelve >= n_q) and split the partials into
+// 12 / jpr phases, merged at the end through `red` (384 x 6 floats of shared
+// memory).  Each thread loads its partials eight at a time, all eight in
+// flight before the first is used.  A partial with m = -inf is empty (its l
+// and O are not read into the sums; they may be stale).  src is a generic
+// address: shared memory, or global memory written by other CTAs.
 struct MergeOut {
   bool final;
   uint16_t *out;  // final: fp16 [n_q][128] of this (sequence, head)
@@ -360,28 +376,37 @@ struct MergeOut {
   float *dst;     // partial
 };
 
-template <bool SHARED>
+// Loads of partials through generic addresses (shared memory, or global
+// memory written by other CTAs: volatile, so never served from a stale L1 line).
 __device__ __forceinline__ float ld_part(const float *p) {
-  return SHARED ? *p : __ldcg(p);
+  float v;
+  asm volatile("ld.volatile.f32 %0, [%1];" : "=f"(v) : "l"(p));
+  return v;
 }
-template <bool SHARED>
 __device__ __forceinline__ float4 ld_part4(const float *p) {
-  return SHARED ? *reinterpret_cast<const float4 *>(p) : __ldcg(reinterpret_cast<const float4 *>(p));
+  float4 v;
+  asm volatile("ld.volatile.v4.f32 {%0,%1,%2,%3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "l"(p));
+  return v;
 }
 
-template <bool SHARED>
-__device__ void merge_partials(const float *src, int kstride, int ns, int n_q, const MergeOut &mo,
-                               float *red) {
-  constexpr int kBatch = 8;  // partials whose loads are all in flight together
+// Not inlined: it runs once per piece at the end of the kernel, when its
+// instructions are not in the instruction cache, so one small copy matters
+// more than call overhead.
+__device__ __noinline__ void merge_partials(const float *src, int kstride, int ns, int n_q,
+                                            const MergeOut &mo, float *red) {
+  constexpr int kBatch = 4;  // partials whose loads are all in flight together
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int jpr = n_q == 1 ? 1 : (n_q == 2 ? 2 : 4);  // queries per round
-  const int ph = 4 / jpr, phase = w / jpr;
+  const int jpr = n_q <= 4 ? n_q : (n_q <= 6 ? 6 : 12);  // queries at once
+  const int ph = kWarps / jpr, phase = w / jpr;
   const int mo_off = n_q * kD;
-  for (int j0 = 0; j0 < n_q; j0 += jpr) {
-    const int j = j0 + w % jpr;
-    float M = -INFINITY, L = 0.f;
-    float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
+  const int j = w % jpr;
+  float M = -INFINITY, L = 0.f;
+  float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
+  {
     if (j < n_q) {
+#pragma unroll 1
       for (int kb = phase; kb < ns; kb += kBatch * ph) {
         float ms[kBatch], ls[kBatch];
         float4 os[kBatch];
@@ -393,14 +418,21 @@ __device__ void merge_partials(const float *src, int kstride, int ns, int n_q, c
           os[u] = make_float4(0.f, 0.f, 0.f, 0.f);
           if (k < ns) {
             const float *sk = src + k * kstride;
-            ms[u] = ld_part<SHARED>(sk + mo_off + j);
-            ls[u] = ld_part<SHARED>(sk + mo_off + 8 + j);
-            os[u] = ld_part4<SHARED>(sk + j * kD + 4 * lane);
+            ms[u] = ld_part(sk + mo_off + j);
+            ls[u] = ld_part(sk + mo_off + 8 + j);
+            os[u] = ld_part4(sk + j * kD + 4 * lane);
           }
         }
         float mn = M;
 #pragma unroll
-        for (int u = 0; u < kBatch; ++u) mn = fmaxf(mn, ms[u]);
+        for (int u = 0; u < kBatch; ++u) {
+          if (!(ms[u] > -INFINITY)) {  // empty partial: stale l and O stay out
+            ms[u] = -INFINITY;
+            ls[u] = 0.f;
+            os[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+          mn = fmaxf(mn, ms[u]);
+        }
         if (mn == -INFINITY) continue;  // nothing visible so far
         const float a = (M == -INFINITY) ? 0.f : fast_exp2(M - mn);
         L *= a;
@@ -484,12 +516,34 @@ __device__ __forceinline__ void write_partial(const Softmax &sm, float *dst, int
   }
 }
 
+// An empty partial (the warp saw none of the piece): m = -inf, l = 0.
+__device__ __forceinline__ void write_empty(float *dst, int n_q, int lane) {
+  if (lane < n_q) {
+    dst[n_q * kD + lane] = -INFINITY;
+    dst[n_q * kD + 8 + lane] = 0.f;
+  }
+}
+
+// Barrier of the two warps of pair `id - 1` (named barrier `id`, 64 threads).
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Wait (bounded) until a stage's copy of unit i has been issued.
+__device__ __forceinline__ bool wait_issued(volatile int *issued, int i) {
+  if (*issued == i) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (*issued != i)
+    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+  return true;
+}
+
 // PK (draft, one query): the MMA's eight query columns hold one real query,
 // so column 2j carries the hi part of B = q * s and column 2j + 1 the lo part
 // for query j = lane / 8 (thread column pair 2c, 2c + 1 = query c): one MMA
 // per k-block instead of two.
 template <int MODE, bool PK>
-__global__ void __launch_bounds__(kThreads, kCtasPerSm) split_kernel(const Params prm) {
+__global__ void __launch_bounds__(kThreads, 1) split_kernel(const Params prm) {
   using C = Cfg<MODE>;
   using L = Layout<MODE>;
   constexpr int TT = C::kTailTok, S = C::kStages;
@@ -497,28 +551,33 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) split_kernel(const Param
   extern __shared__ __align__(128) uint8_t smem[];
   const qs_cache &c = prm.c;
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int pr = w >> 1, hw = w & 1;  // warp pair (units of that parity), half of a unit
+  const int pr = w >> 1, hw = w & 1;  // warp pair, half of a unit
   const int r = lane >> 2, cq = lane & 3;
   const uint32_t sbase = smem_addr(smem);
   const uint32_t full0 = sbase + L::kBarOff, zero_row = sbase + L::kZeroOff;
-  int *cnt = reinterpret_cast<int *>(smem + L::kCntOff);
+  int *cnt = reinterpret_cast<int *>(smem + L::kCntOff);            // releases per stage
+  volatile int *issued = reinterpret_cast<int *>(smem + L::kIssOff);  // unit copied into a stage
+  volatile int *claim = reinterpret_cast<int *>(smem + L::kClaimOff); // [pair][2] claimed unit
   Tables T = tables_at(smem, L::kTabOff);
+  __shared__ long long s_total;
+  __shared__ int s_abort, s_next, s_seg[2], s_ord[2], s_need[2], s_last[2];
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(full0 + 8 * s, 1);
       cnt[s] = 0;
+      issued[s] = -1;
     }
     fence_mbar_init();
+    s_next = 0;
+    s_abort = 0;
   }
   if (threadIdx.x < 8) reinterpret_cast<uint32_t *>(smem + L::kZeroOff)[threadIdx.x] = 0;
-  __shared__ long long s_total;
-  __shared__ int s_abort, s_seg[2], s_need[2], s_last[2];
   pdl_trigger();
   pdl_wait();  // counters, cache and queries are written by earlier kernels
   if (w == 0) {
     const long long tot = build_tables<TT>(c, prm.n_q, T, lane);
-    if (lane == 0) { s_total = tot; s_abort = 0; }
+    if (lane == 0) s_total = tot;
   }
   __syncthreads();
   const long long U = s_total;
@@ -536,49 +595,69 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) split_kernel(const Param
     if (threadIdx.x == 0) atomicOr(&c.state[(size_t)b * QS_STATE_WORDS + QS_ST_ERR], QS_DEV_NQ_GT_FILL);
   }
 
-  const long long x0 = range_lo(p, U, prm.P), x1 = range_lo(p + 1, U, prm.P);
+  const int x0 = (int)range_lo(p, U, prm.P), x1 = (int)range_lo(p + 1, U, prm.P);
   if (x0 >= x1) return;
-  const int n = (int)(x1 - x0);
+  const int n = x1 - x0;
+  Seg first, lastseg;
+  first.seek(x0, T, c.B);
+  lastseg.seek(x1 - 1, T, c.B);
+  const int ord_first = first.ord, ord_last = lastseg.ord;
+  // partial slot of warp ww for the piece of segment ordinal o
+  auto slot = [&](int o, int ww) { return prm.ws + ((size_t)(o + p) * kWarps + ww) * stride; };
 
-  // units i and i + S share a stage; "ahead" walks S units in front
-  Cursor cur, ahead;
-  cur.init(x0, T, c.B, c.H);
-  ahead = cur;
-  if (w == 0) {  // prologue: the first S units
+  // units i and i + S share stage i % S; warp 0 issues the first S
+  if (w == 0) {
+    Seg a;
     for (int k = 0; k < S && k < n; ++k) {
-      issue_unit<MODE>(c, T, ahead, sbase + k * L::kStageBytes, full0 + 8 * k, lane);
-      ahead.advance(T, c.B, c.H);
+      a.seek(x0 + k, T, c.B);
+      if (lane == 0) issued[k] = k;
+      issue_unit<MODE>(c, T, a, sbase + k * L::kStageBytes, full0 + 8 * k, lane);
     }
-  } else {
-    for (int k = 0; k < S && k < n; ++k) ahead.advance(T, c.B, c.H);
   }
 
   Softmax sm;
   sm.reset();
   uint32_t qp0[8], qp1[8];
   int fill = 0, ng = 0;
-  for (int i = 0; i < n; ++i) {
-    const size_t bh = (size_t)cur.b * c.H + cur.h;
-    if (i == 0 || cur.u == 0) {  // a new piece: this (sequence, head)
+  int cur_ord = -1;  // segment ordinal of this warp's softmax state (-1: none yet)
+  Seg cur, ahead;
+  for (int k = 0;; ++k) {
+    // the pair's leader claims the next unit; both warps take it after the
+    // pair barrier (claims alternate between two slots)
+    if (hw == 0 && lane == 0) {
+      int i = *reinterpret_cast<volatile int *>(&s_abort) ? n : atomicAdd(&s_next, 1);
+      claim[2 * pr + (k & 1)] = i < n ? i : n;
+    }
+    named_bar_sync(1 + pr, 64);
+    const int i = claim[2 * pr + (k & 1)];
+    if (i >= n) break;
+    cur.seek(x0 + i, T, c.B);
+    if (cur.ord != cur_ord) {
+      // a new piece: the finished one's partial (empty ones for pieces this
+      // warp skipped), then fresh state and this head's queries
+      if (cur_ord >= 0) write_partial(sm, slot(cur_ord, w), prm.n_q, lane);
+      for (int o = cur_ord >= 0 ? cur_ord + 1 : ord_first; o < cur.ord; ++o)
+        write_empty(slot(o, w), prm.n_q, lane);
+      cur_ord = cur.ord;
+      const size_t bh = (size_t)cur.b * c.H + cur.h;
       const int qi = PK ? (r >> 1) : r;  // the query in B column r
       load_q_pairs(prm.q + (bh * prm.n_q + qi) * kD, qi < prm.n_q, cq, qp0, qp1);
       sm.reset();
       fill = T.fill[cur.b];
       ng = T.ng[cur.b];
     }
-    if ((i & 1) == pr) {
-      const int stage = i % S;
-      if (!mbar_wait(full0 + 8 * stage, (uint32_t)((i / S) & 1))) {
-        if (lane == 0) {
-          atomicOr(&c.state[(size_t)cur.b * QS_STATE_WORDS + QS_ST_ERR], QS_DEV_TIMEOUT);
-          s_abort = 1;
-        }
-        // bounded drain of the copies still outstanding in this pair's stages
-        // (stage i % S only ever serves units of this pair's parity)
-        for (int k = i + 2; k < i + S && k < n; k += 2)
-          if (!mbar_wait(full0 + 8 * (k % S), (uint32_t)((k / S) & 1))) break;
-        break;  // to the merge, which then only keeps the arrival counts right
+    const int stage = i % S;
+    // the stage must hold unit i's copy (not the unit S before it) before its
+    // barrier parity means anything
+    bool ok = wait_issued(issued + stage, i);
+    if (ok) ok = mbar_wait(full0 + 8 * stage, (uint32_t)((i / S) & 1));
+    ok = __all_sync(0xffffffffu, ok);  // the tensor-core code below needs the whole warp
+    if (!ok) {
+      if (lane == 0) {
+        atomicOr(&c.state[(size_t)cur.b * QS_STATE_WORDS + QS_ST_ERR], QS_DEV_TIMEOUT);
+        s_abort = 1;
       }
+    } else {
       const uint32_t st = sbase + stage * L::kStageBytes;
 
       if (cur.u < ng) {
@@ -799,69 +878,83 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) split_kernel(const Param
         }
       }
 
-      // release the stage; the later of the pair issues the refill (unit i + S)
-      __syncwarp();
-      int last = 0;
-      if (lane == 0) last = (atomicAdd(&cnt[stage], 1) == 1);
-      last = __shfl_sync(0xffffffffu, last, 0);
-      if (last) {
-        if (lane == 0) cnt[stage] = 0;
-        if (i + S < n) {
-          fence_proxy_async_smem();
-          issue_unit<MODE>(c, T, ahead, st, full0 + 8 * stage, lane);
-        }
+    }
+
+    // release the stage; the later warp of the pair issues the refill
+    // (unit i + S) unless its own wait failed
+    __syncwarp();
+    int last = 0;
+    if (lane == 0) last = (atomicAdd(&cnt[stage], 1) == 1);
+    last = __shfl_sync(0xffffffffu, last, 0);
+    if (last) {
+      if (lane == 0) cnt[stage] = 0;
+      if (ok && i + S < n) {
+        ahead.seek(x0 + i + S, T, c.B);
+        fence_proxy_async_smem();
+        if (lane == 0) issued[stage] = i + S;
+        __syncwarp();
+        issue_unit<MODE>(c, T, ahead, sbase + stage * L::kStageBytes, full0 + 8 * stage, lane);
       }
     }
-    if (i + S < n) ahead.advance(T, c.B, c.H);
-
-    if (i + 1 < n && cur.u + 1 == T.len[cur.b]) {
-      // piece done before the range ends: this warp's partial to its slot
-      const long long seg = (long long)cur.b * c.H + cur.h;
-      write_partial(sm, prm.ws + ((seg + p) * kConsumers + w) * stride, prm.n_q, lane);
-    }
-    cur.advance(T, c.B, c.H);
   }
+  // this warp's partials for the pieces after its last unit's piece are empty
+  // (all but the range's last piece go to the workspace)
+  if (cur_ord >= 0 && cur_ord < ord_last) write_partial(sm, slot(cur_ord, w), prm.n_q, lane);
+  for (int o = cur_ord >= 0 ? cur_ord + 1 : ord_first; o < ord_last; ++o)
+    write_empty(slot(o, w), prm.n_q, lane);
 
-  // ---- log-sum-exp merge.  Per piece of this CTA's range: merge the four
+  __syncthreads();
+  // no copy may still be landing in the stage memory reused below: after a
+  // timeout, wait for each stage's last copy (otherwise every issued copy
+  // has been waited for by the pair that claimed its unit)
+  if (w == 0 && s_abort) {
+    const unsigned long long deadline = globaltimer_ns() + kWaitLimitNs;
+    for (int s = lane; s < S; s += 32) {
+      const int j = issued[s];
+      if (j >= 0)
+        while (!mbar_try_wait(full0 + 8 * s, (uint32_t)((j / S) & 1)) && globaltimer_ns() < deadline) {
+        }
+    }
+  }
+  __syncthreads();
+
+  // ---- log-sum-exp merge.  Per piece of this CTA's range: merge the twelve
   // warp partials (the last piece's straight from registers through shared
   // memory); a segment that lies wholly in the range is final here.  A
   // segment shared with other CTAs gets one CTA partial (in warp slot 0) and
   // an arrival on its counter; the CTA that arrives last merges the CTA
   // partials of the whole segment and resets the counter.  Only the first
   // and the last piece of a range can be shared.
-  __syncthreads();  // the stages are idle
   const bool aborted = s_abort != 0;
-  float *red = reinterpret_cast<float *>(smem);                   // stage memory, free now
-  float *last_part = reinterpret_cast<float *>(smem + 4096);     // 4 partials
-  if (!aborted) write_partial(sm, last_part + w * stride, prm.n_q, lane);
+  float *red = reinterpret_cast<float *>(smem);                 // stage memory, free now
+  float *last_part = reinterpret_cast<float *>(smem + 16384);  // kWarps partials
+  if (cur_ord == ord_last) write_partial(sm, last_part + w * stride, prm.n_q, lane);
+  else write_empty(last_part + w * stride, prm.n_q, lane);
   __syncthreads();
   int n_arr = 0;
   {
-    Cursor pc;
-    pc.init(x0, T, c.B, c.H);
-    long long x = x0;
+    Seg pc;
+    int x = x0;
     while (x < x1) {
-      const int b = pc.b, h = pc.h, len = T.len[b];
-      const long long seg = (long long)b * c.H + h;
-      const long long S0 = T.base[b] + (long long)h * len, E0 = S0 + len;
+      pc.seek(x, T, c.B);
+      const long long seg = (long long)pc.b * c.H + pc.h;
+      const int S0 = pc.s0, E0 = pc.s0 + pc.len;
       const int plo = cta_of(S0, U, prm.P), phi = cta_of(E0 - 1, U, prm.P);
-      float *slots = prm.ws + (size_t)(seg + p) * kConsumers * stride;
       const MergeOut mo{plo == phi, prm.out + (size_t)seg * prm.n_q * kD,
-                        prm.lse ? prm.lse + (size_t)seg * prm.n_q : nullptr, slots};
+                        prm.lse ? prm.lse + (size_t)seg * prm.n_q : nullptr, slot(pc.ord, 0)};
       if (!aborted) {
-        if (E0 >= x1) merge_partials<true>(last_part, stride, kConsumers, prm.n_q, mo, red);
-        else merge_partials<false>(slots, stride, kConsumers, prm.n_q, mo, red);
+        merge_partials(pc.ord == ord_last ? last_part : slot(pc.ord, 0), stride, kWarps, prm.n_q, mo,
+                       red);
       }
       if (plo != phi) {
         if (threadIdx.x == 0) {
           s_seg[n_arr] = (int)seg;
+          s_ord[n_arr] = pc.ord;
           s_need[n_arr] = phi - plo + 1;
         }
         ++n_arr;
       }
-      x = E0 < x1 ? E0 : x1;
-      pc.u = len - 1;
-      pc.advance(T, c.B, c.H);
+      x = E0;
     }
   }
   if (n_arr == 0) return;
@@ -880,13 +973,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) split_kernel(const Param
   for (int a = 0; a < n_arr; ++a) {
     if (!s_last[a] || aborted) continue;
     const long long seg = s_seg[a];
-    const int b = (int)(seg / c.H), h = (int)(seg % c.H), len = T.len[b];
-    const long long S0 = T.base[b] + (long long)h * len, E0 = S0 + len;
+    const int b = (int)(seg / c.H), len = T.len[b];
+    const int S0 = T.base[b] + (int)(seg % c.H) * len, E0 = S0 + len;
     const int plo = cta_of(S0, U, prm.P), phi = cta_of(E0 - 1, U, prm.P);
     const MergeOut mo{true, prm.out + (size_t)seg * prm.n_q * kD,
                       prm.lse ? prm.lse + (size_t)seg * prm.n_q : nullptr, nullptr};
-    merge_partials<false>(prm.ws + (size_t)(seg + plo) * kConsumers * stride, kConsumers * stride,
-                          phi - plo + 1, prm.n_q, mo, red);
+    // CTA pp's partial of this segment is in its warp slot 0
+    merge_partials(prm.ws + ((size_t)(s_ord[a] + plo) * kWarps) * stride, kWarps * stride,
+                   phi - plo + 1, prm.n_q, mo, red);
   }
 }
 
@@ -932,7 +1026,7 @@ qs_status grid_size(qs_mode mode, bool packed, int &P) {
 }
 
 size_t ws_bytes(int P, int B, int H, int n_q) {
-  return (size_t)(P + (size_t)B * H) * kConsumers * (size_t)(n_q * kD + 16) * sizeof(float);
+  return (size_t)(P + (size_t)B * H) * kWarps * (size_t)(n_q * kD + 16) * sizeof(float);
 }
 
 template <int MODE, bool PK>

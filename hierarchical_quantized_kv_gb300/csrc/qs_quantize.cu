@@ -69,38 +69,13 @@ __device__ __forceinline__ int vmeta_pos(int t) {
   return ((t >> 3) & 1) | (((t >> 4) & 1) << 1) | ((t & 7) << 2) | ((t >> 5) << 5);
 }
 
-}  // namespace
-
-__global__ void __launch_bounds__(256) flush_kernel(qs_cache c, const uint8_t *__restrict__ mask) {
-  extern __shared__ __align__(128) uint8_t smem_raw[];
-  FlushSmem &S = *reinterpret_cast<FlushSmem *>(smem_raw);
-  const int part = blockIdx.x, h = blockIdx.y, b = blockIdx.z, tid = threadIdx.x;
+// One CTA's share of quantizing a group of G tokens whose fp16 key and value
+// rows (D channels each, row stride D) start at gk and gv: key channels
+// [32 part, 32 part + 32) and value tokens [32 part, 32 part + 32), written
+// as group `grp` (index into the [B][H][cap] group arrays).  256 threads.
+__device__ void quantize_part(FlushSmem &S, const __half *gk, const __half *gv, const qs_cache &c,
+                              size_t grp, int part, int tid) {
   const int warp = tid >> 5, lane = tid & 31;
-  pdl_trigger();
-  pdl_wait();
-  int32_t *st = c.state + (size_t)b * QS_STATE_WORDS;
-  if (tid == 0) {
-    int act = mask ? (mask[b] != 0) : 1;
-    const int fill = st[QS_ST_FILL], pending = st[QS_ST_PENDING], ng = st[QS_ST_N_GROUPS];
-    const bool lead = (h == 0 && part == 0);
-    if (act && fill - pending < kG) {
-      if (lead) atomicOr(&st[QS_ST_ERR], QS_DEV_FLUSH_UNCOMMITTED);
-      act = 0;
-    } else if (act && (ng < 0 || ng >= c.cap_groups)) {
-      if (lead) atomicOr(&st[QS_ST_ERR], QS_DEV_CAPACITY);
-      act = 0;
-    }
-    S.act = act;
-    S.base = st[QS_ST_HALF_BASE] & 1;
-    S.g = ng;
-  }
-  __syncthreads();
-  if (!S.act) return;
-  const int base = S.base, g = S.g;
-  const size_t bh = (size_t)b * c.H + h;
-  const __half *gk = reinterpret_cast<const __half *>(c.buf_k) + (bh * kRing + base * kG) * kD;
-  const __half *gv = reinterpret_cast<const __half *>(c.buf_v) + (bh * kRing + base * kG) * kD;
-
   // 1. loads: the key column slice (64 B of each of 128 rows), 32 value rows
   for (int e = tid; e < kG * 4; e += 256) {  // 4 x 16 B per key row
     const int t = e >> 2, q = e & 3;
@@ -174,7 +149,6 @@ __global__ void __launch_bounds__(256) flush_kernel(qs_cache c, const uint8_t *_
   }
   __syncthreads();
 
-  const size_t grp = bh * c.cap_groups + g;
   if (tid < kG) {
     // 5. key planes: bytes [16p, 16p+16) of token row tid (channels 2i, 2i+1)
     uint32_t wu[4] = {0, 0, 0, 0}, wl[4] = {0, 0, 0, 0};
@@ -211,6 +185,40 @@ __global__ void __launch_bounds__(256) flush_kernel(qs_cache c, const uint8_t *_
     m[QS_META_V_SCALE * 128 + vp] = S.vs[tid];
     m[QS_META_V_ZERO * 128 + vp] = S.vz[tid];
   }
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(256) flush_kernel(qs_cache c, const uint8_t *__restrict__ mask) {
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  FlushSmem &S = *reinterpret_cast<FlushSmem *>(smem_raw);
+  const int part = blockIdx.x, h = blockIdx.y, b = blockIdx.z, tid = threadIdx.x;
+  pdl_trigger();
+  pdl_wait();
+  int32_t *st = c.state + (size_t)b * QS_STATE_WORDS;
+  if (tid == 0) {
+    int act = mask ? (mask[b] != 0) : 1;
+    const int fill = st[QS_ST_FILL], pending = st[QS_ST_PENDING], ng = st[QS_ST_N_GROUPS];
+    const bool lead = (h == 0 && part == 0);
+    if (act && fill - pending < kG) {
+      if (lead) atomicOr(&st[QS_ST_ERR], QS_DEV_FLUSH_UNCOMMITTED);
+      act = 0;
+    } else if (act && (ng < 0 || ng >= c.cap_groups)) {
+      if (lead) atomicOr(&st[QS_ST_ERR], QS_DEV_CAPACITY);
+      act = 0;
+    }
+    S.act = act;
+    S.base = st[QS_ST_HALF_BASE] & 1;
+    S.g = ng;
+  }
+  __syncthreads();
+  if (!S.act) return;
+  const int base = S.base, g = S.g;
+  const size_t bh = (size_t)b * c.H + h;
+  const __half *gk = reinterpret_cast<const __half *>(c.buf_k) + (bh * kRing + base * kG) * kD;
+  const __half *gv = reinterpret_cast<const __half *>(c.buf_v) + (bh * kRing + base * kG) * kD;
+
+  quantize_part(S, gk, gv, c, bh * c.cap_groups + g, part, tid);
   __syncthreads();
   if (tid == 0) {
     __threadfence();
@@ -225,24 +233,116 @@ __global__ void __launch_bounds__(256) flush_kernel(qs_cache c, const uint8_t *_
   }
 }
 
+// Bulk prefill of empty caches from a prompt (k, v: fp16 [B][H][T][D]).
+// Grid (4 gmax + 2, H, B): block x < 4 gmax quantizes part x % 4 of group
+// x / 4 (if the sequence has that group); the last two blocks copy buffer
+// halves 0 and 1.  The CTA that arrives last on the sequence's ticket writes
+// the counters, so every CTA reads the old (empty) ones first.
+__global__ void __launch_bounds__(256) prefill_kernel(qs_cache c, const uint16_t *__restrict__ k,
+                                                     const uint16_t *__restrict__ v, int T,
+                                                     const int32_t *__restrict__ len, int gmax) {
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  FlushSmem &S = *reinterpret_cast<FlushSmem *>(smem_raw);
+  const int x = blockIdx.x, h = blockIdx.y, b = blockIdx.z, tid = threadIdx.x;
+  pdl_trigger();
+  pdl_wait();
+  int32_t *st = c.state + (size_t)b * QS_STATE_WORDS;
+  if (tid == 0) {
+    const int L = len[b];
+    const bool lead = (h == 0 && x == 0);
+    int act = 1, ng = 0;
+    if (st[QS_ST_N_GROUPS] != 0 || st[QS_ST_FILL] != 0 || st[QS_ST_PENDING] != 0 || L < 0 ||
+        L > T) {
+      if (lead) atomicOr(&st[QS_ST_ERR], QS_DEV_PREFILL);
+      act = 0;
+    } else {
+      ng = L > 2 * kG ? (L - 2 * kG + kG - 1) / kG : 0;
+      if (ng > c.cap_groups) {
+        if (lead) atomicOr(&st[QS_ST_ERR], QS_DEV_CAPACITY);
+        act = 0;
+      }
+    }
+    S.act = act;
+    S.g = ng;
+    S.base = act ? L - ng * kG : 0;  // fill
+  }
+  __syncthreads();
+  if (!S.act) return;
+  const int ng = S.g, fill = S.base;
+  const size_t bh = (size_t)b * c.H + h;
+  const uint16_t *kp = k + bh * T * kD, *vp = v + bh * T * kD;
+  if (x < 4 * gmax) {
+    const int g = x >> 2, part = x & 3;
+    if (g < ng)
+      quantize_part(S, reinterpret_cast<const __half *>(kp) + (size_t)g * kG * kD,
+                    reinterpret_cast<const __half *>(vp) + (size_t)g * kG * kD, c,
+                    bh * c.cap_groups + g, part, tid);
+  } else {
+    // buffer half x - 4 gmax: tokens i in [G half, G half + G) that are < fill
+    const int i0 = (x - 4 * gmax) * kG, i1 = min(i0 + kG, fill);
+    const uint4 *ks = reinterpret_cast<const uint4 *>(kp + (size_t)ng * kG * kD);
+    const uint4 *vs = reinterpret_cast<const uint4 *>(vp + (size_t)ng * kG * kD);
+    uint4 *kd = reinterpret_cast<uint4 *>(c.buf_k + bh * kRing * kD);
+    uint4 *vd = reinterpret_cast<uint4 *>(c.buf_v + bh * kRing * kD);
+    for (int e = i0 * (kD / 8) + tid; e < i1 * (kD / 8); e += 256) {
+      kd[e] = ks[e];
+      vd[e] = vs[e];
+    }
+  }
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    const int ticket = atomicAdd(&st[QS_ST_TICKET], 1);
+    if (ticket == (int)gridDim.x * c.H - 1) {
+      st[QS_ST_N_GROUPS] = ng;
+      st[QS_ST_FILL] = fill;
+      st[QS_ST_PENDING] = 0;
+      st[QS_ST_HALF_BASE] = 0;
+      st[QS_ST_TICKET] = 0;
+      __threadfence();
+    }
+  }
+}
+
 }  // namespace qs
 
 using namespace qs;
+
+namespace {
+// Opt the kernels into their dynamic shared memory once per device.
+qs_status set_smem_once(const void *kernel, int smem, int *mask) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return QS_ERR_CUDA;
+  if (dev >= 32 || !(__atomic_load_n(mask, __ATOMIC_ACQUIRE) & (1 << dev))) {
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+        cudaSuccess)
+      return QS_ERR_CUDA;
+    if (dev < 32) __atomic_fetch_or(mask, 1 << dev, __ATOMIC_RELEASE);
+  }
+  return QS_OK;
+}
+int g_flush_ready = 0, g_prefill_ready = 0;  // one bit per device ordinal below 32
+}  // namespace
+
+extern "C" qs_status qs_prefill(const qs_cache *c, const uint16_t *k, const uint16_t *v, int32_t T,
+                                const int32_t *d_len, qs_stream_t stream) {
+  qs_status s = check_cache(c);
+  if (s != QS_OK) return s;
+  if (!k || !v || !d_len || T < 0 || T > (1 << 26)) return QS_ERR_ARG;
+  if (!aligned16(k) || !aligned16(v)) return QS_ERR_ALIGN;
+  const int smem = (int)sizeof(FlushSmem);
+  if ((s = set_smem_once((const void *)prefill_kernel, smem, &g_prefill_ready)) != QS_OK) return s;
+  const int gmax = T > 2 * kG ? (T - 2 * kG + kG - 1) / kG : 0;
+  return launch_pdl(prefill_kernel, dim3(4 * gmax + 2, c->H, c->B), dim3(256), smem,
+                    (cudaStream_t)stream, *c, k, v, (int)T, d_len, gmax);
+}
 
 extern "C" qs_status qs_quantize_flush(const qs_cache *c, const uint8_t *d_mask,
                                        qs_stream_t stream) {
   qs_status s = check_cache(c);
   if (s != QS_OK) return s;
   const int smem = (int)sizeof(FlushSmem);
-  static int configured_mask = 0;  // one bit per device ordinal below 32
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return QS_ERR_CUDA;
-  if (dev >= 32 || !(configured_mask & (1 << dev))) {
-    if (cudaFuncSetAttribute(flush_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-        cudaSuccess)
-      return QS_ERR_CUDA;
-    if (dev < 32) __atomic_fetch_or(&configured_mask, 1 << dev, __ATOMIC_RELAXED);
-  }
+  if ((s = set_smem_once((const void *)flush_kernel, smem, &g_flush_ready)) != QS_OK) return s;
   return launch_pdl(flush_kernel, dim3(kParts, c->H, c->B), dim3(256), smem, (cudaStream_t)stream,
                     *c, d_mask);
 }

@@ -19,6 +19,7 @@ QS_DRAFT_UPPER4, QS_VERIFY_INT8 = 0, 1
 QS_STATIC_WS_BYTES = 8 << 20
 DEV_OVERFLOW, DEV_OVER_ROLLBACK, DEV_FLUSH_UNCOMMITTED, DEV_CAPACITY, DEV_NQ_GT_FILL, DEV_TIMEOUT = (
     1, 2, 4, 8, 16, 32)
+DEV_PREFILL = 64
 ST_N_GROUPS, ST_FILL, ST_PENDING, ST_HALF_BASE, ST_ERR, ST_TICKET = range(6)
 STATE_WORDS = 8
 META_K_SCALE, META_K_ZERO, META_V_SCALE, META_V_ZERO = range(4)
@@ -59,6 +60,7 @@ _SIGS = {
     "qs_attn_decode": [ctypes.POINTER(QsCacheStruct), ctypes.c_int, _P, _I32, ctypes.c_float, _P,
                        _P, _P, ctypes.c_size_t, _P],
     "qs_get_errors": [ctypes.POINTER(QsCacheStruct), _P, _P],
+    "qs_prefill": [ctypes.POINTER(QsCacheStruct), _P, _P, _I32, _P, _P],
 }
 
 
@@ -168,6 +170,14 @@ def qs_need_flush(cache, n_next, mask, stream=None):
 def qs_quantize_flush(cache, mask=None, stream=None):
     """mask: uint8 [B] device tensor or None (every sequence)."""
     _check("qs_quantize_flush", lib().qs_quantize_flush(cache._ref, _ptr(mask), _stream(stream)))
+
+
+def qs_prefill(cache, k, v, lens, stream=None):
+    """k, v: fp16 [B, H, T, D] contiguous device tensors; lens: int32 [B]
+    device tensor of prompt lengths."""
+    assert k.is_contiguous() and v.is_contiguous() and k.shape == v.shape
+    _check("qs_prefill", lib().qs_prefill(cache._ref, _ptr(k), _ptr(v), int(k.shape[2]), _ptr(lens),
+                                          _stream(stream)))
 
 
 def qs_attn_workspace_size(cache, n_q):

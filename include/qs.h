@@ -82,8 +82,10 @@ enum {
   QS_DEV_FLUSH_UNCOMMITTED = 4,  /* flush with fewer than G committed tokens */
   QS_DEV_CAPACITY = 8,           /* flush with n_groups == cap_groups */
   QS_DEV_NQ_GT_FILL = 16,        /* attention with n_q > buffered tokens */
-  QS_DEV_TIMEOUT = 32            /* a pipeline wait ran out of time (never
+  QS_DEV_TIMEOUT = 32,           /* a pipeline wait ran out of time (never
                                     expected; the call's results are invalid) */
+  QS_DEV_PREFILL = 64            /* prefill of a non-empty cache, or a prompt
+                                    length outside [0, T] */
 };
 
 /* Per-sequence counters: int32 state[B][QS_STATE_WORDS]. */
@@ -182,6 +184,28 @@ qs_status qs_need_flush(const qs_cache *c, int32_t n_next, uint8_t *d_mask, qs_s
  * no-op.  Source: Pith review page, "What carries the argument", Figure 7 and
  * Appendix D; "QuantSpec Guide", "Periodic Group Quantization". */
 qs_status qs_quantize_flush(const qs_cache *c, const uint8_t *d_mask, qs_stream_t stream);
+
+/* Bulk prefill: fill empty caches from a prompt in one call.  k, v: fp16
+ * [B][H][T][D] device arrays (token t of head h of sequence b at
+ * [b][h][t]); d_len: int32 [B] device array, the prompt length of each
+ * sequence.  With L = d_len[b]: the first n_groups * G tokens become groups
+ * 0..n_groups-1 (G tokens each, in order, convention QS-RN-v1 as in
+ * qs_quantize_flush) and the remaining fill tokens become committed buffer
+ * tokens 0..fill-1 in ring slots 0..fill-1, where
+ *   n_groups = L > 2G ? ceil((L - 2G) / G) : 0,   fill = L - G * n_groups,
+ * pending = 0 and half_base = 0.  These are the groups and the logical buffer
+ * that appending the prompt in pieces of at most G tokens (qs_buffer_append,
+ * commit, qs_quantize_flush whenever qs_need_flush asks) would leave.
+ * Per sequence: a cache that is not empty (n_groups, fill or pending non-zero)
+ * or L outside [0, T] gives QS_DEV_PREFILL, n_groups > cap_groups gives
+ * QS_DEV_CAPACITY; either leaves the sequence unchanged.  Host errors:
+ * QS_ERR_ARG (null pointers, T < 0 or T > 2^26), QS_ERR_ALIGN.  Ownership:
+ * all arrays are the caller's; the call only reads k, v and d_len.
+ * Source: "QuantSpec Guide", core architectural blueprint (the prefill
+ * context is quantized once into the hierarchical cache); Pith review page,
+ * "What carries the argument" (groups of G tokens, two buffer halves). */
+qs_status qs_prefill(const qs_cache *c, const uint16_t *k, const uint16_t *v, int32_t T,
+                     const int32_t *d_len, qs_stream_t stream);
 
 /* Bytes of device workspace qs_attn_decode needs for n_q queries (1..8) on
  * the current device.  Pure host function (reads device attributes). */

@@ -29,6 +29,7 @@ from . import build as _build
 N_GROUPS, FILL, PENDING, HALF_BASE, ERR = 0, 1, 2, 3, 4
 STATE_WORDS = 8
 DEV_OVERFLOW, DEV_OVER_ROLLBACK, DEV_FLUSH_UNCOMMITTED, DEV_CAPACITY, DEV_NQ_GT_FILL = 1, 2, 4, 8, 16
+DEV_PREFILL = 64
 
 _lib = None
 
@@ -64,6 +65,7 @@ def lib():
         L.qso_split_code.argtypes = [ctypes.c_uint8, P, P]
         for name, args in (("qso_append", [P, P, P, I]), ("qso_rollback", [P, P]),
                            ("qso_need_flush", [P, I, P]), ("qso_flush", [P, P]),
+                           ("qso_prefill", [P, P, P, I, P]),
                            ("qso_attn", [P, I, P, I, D_, P, P])):
             f = getattr(L, name)
             f.restype = None
@@ -178,6 +180,15 @@ class OracleCache:
         else:
             m = np.ascontiguousarray(np.asarray(mask, np.uint8))
             lib().qso_flush(ctypes.byref(c), _ptr(m))
+
+    def prefill(self, k, v, lens):
+        """Fill empty caches from a prompt: k, v [B, H, T, D] fp16, lens [B]."""
+        kb = _as_half_bits(k)
+        vb = _as_half_bits(v)
+        assert kb.shape == vb.shape and kb.shape[:2] == (self.B, self.H) and kb.shape[3] == self.D
+        n = np.ascontiguousarray(np.broadcast_to(np.asarray(lens, np.int32), (self.B,)))
+        c = self._c()
+        lib().qso_prefill(ctypes.byref(c), _ptr(kb), _ptr(vb), kb.shape[2], _ptr(n))
 
     def attn(self, q, upper_only, scale=None):
         """Decode attention in fp64: q [B, H, n_q, D] fp16 ->

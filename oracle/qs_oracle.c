@@ -57,6 +57,7 @@
 #define QSO_DEV_FLUSH_UNCOMMITTED 4
 #define QSO_DEV_CAPACITY 8
 #define QSO_DEV_NQ_GT_FILL 16
+#define QSO_DEV_PREFILL 64
 
 /* ------------------------------------------------------------------ fp16 */
 
@@ -248,6 +249,22 @@ void qso_need_flush(const qso_cache *c, int n_next, uint8_t *mask) {
     mask[b] = (uint8_t)(st(c, b)[QSO_FILL] + n_next > 2 * c->G);
 }
 
+/* Quantize G tokens (kt, vt: [G][D] fp16, token-major) of head h of
+ * sequence b into group g: keys per channel over the G tokens, values per
+ * token over the D (= G) channels.  [P3] Figure 7 / Appendix D. */
+static void quantize_block(qso_cache *c, int b, int h, int g, const uint16_t *kt,
+                           const uint16_t *vt) {
+  int G = c->G, D = c->D;
+  long grp = bh(c, b, h) * c->cap + g;
+  uint8_t *kq = c->kq + grp * G * D, *vq = c->vq + grp * G * D;
+  for (int d = 0; d < D; ++d) /* keys: one group per channel */
+    qso_quantize_group(kt + d, D, G, c->ks + grp * D + d, c->kz + grp * D + d,
+                       kq + d, D);
+  for (int t = 0; t < G; ++t) /* values: one group per token */
+    qso_quantize_group(vt + (long)t * D, 1, D, c->vs + grp * G + t,
+                       c->vz + grp * G + t, vq + (long)t * D, 1);
+}
+
 /* Quantize the oldest buffer half (G committed tokens) of every masked
  * sequence into group n_groups: keys per channel over the G tokens, values
  * per token over the D (= G) channels.  Then toggle the half and drop G.
@@ -276,20 +293,59 @@ void qso_flush(qso_cache *c, const uint8_t *mask) {
         memcpy(kt + (long)i * D, c->bk + src, sizeof(uint16_t) * D);
         memcpy(vt + (long)i * D, c->bv + src, sizeof(uint16_t) * D);
       }
-      long grp = bh(c, b, h) * c->cap + g;
-      uint8_t *kq = c->kq + grp * G * D, *vq = c->vq + grp * G * D;
-      for (int d = 0; d < D; ++d) /* keys: one group per channel */
-        qso_quantize_group(kt + d, D, G, c->ks + grp * D + d,
-                           c->kz + grp * D + d, kq + d, D);
-      for (int t = 0; t < G; ++t) /* values: one group per token */
-        qso_quantize_group(vt + (long)t * D, 1, D, c->vs + grp * G + t,
-                           c->vz + grp * G + t, vq + (long)t * D, 1);
+      quantize_block(c, b, h, g, kt, vt);
     }
     free(kt);
     free(vt);
     s[QSO_N_GROUPS] = g + 1;
     s[QSO_HALF_BASE] ^= 1;
     s[QSO_FILL] -= G;
+  }
+}
+
+/* Fill empty caches from a prompt in one step.  k, v: [B][H][T][D] fp16;
+ * sequence b has len[b] prompt tokens.  The first n_groups * G tokens become
+ * groups 0..n_groups-1 (G at a time, in order) and the other fill tokens
+ * become committed buffer tokens 0..fill-1 in slots 0..fill-1 (half_base 0),
+ * with n_groups = len > 2G ? ceil((len - 2G) / G) : 0, fill = len - G n_groups
+ * (so fill is in (G, 2G] once len > 2G).  These are the groups and the logical
+ * buffer that appending the prompt in pieces of at most G tokens, with a
+ * flush before every append that would overflow 2G, leaves behind.  A
+ * sequence whose cache is not empty (n_groups, fill or pending non-zero) or
+ * whose length is outside [0, T] gets QSO_DEV_PREFILL and is left unchanged;
+ * one that needs more than cap groups gets QSO_DEV_CAPACITY and is left
+ * unchanged.  [P1] architectural blueprint (the prefill context is quantized
+ * once into the hierarchical cache); [P3] "What carries the argument". */
+void qso_prefill(qso_cache *c, const uint16_t *k, const uint16_t *v, int T,
+                 const int32_t *len) {
+  int G = c->G, D = c->D;
+  for (int b = 0; b < c->B; ++b) {
+    int32_t *s = st(c, b);
+    int L = len[b];
+    if (s[QSO_N_GROUPS] != 0 || s[QSO_FILL] != 0 || s[QSO_PENDING] != 0 || L < 0 ||
+        L > T) {
+      s[QSO_ERR] |= QSO_DEV_PREFILL;
+      continue;
+    }
+    int ng = L > 2 * G ? (L - 2 * G + G - 1) / G : 0;
+    if (ng > c->cap) {
+      s[QSO_ERR] |= QSO_DEV_CAPACITY;
+      continue;
+    }
+    for (int h = 0; h < c->H; ++h) {
+      const uint16_t *kp = k + bh(c, b, h) * T * D, *vp = v + bh(c, b, h) * T * D;
+      for (int g = 0; g < ng; ++g)
+        quantize_block(c, b, h, g, kp + (long)g * G * D, vp + (long)g * G * D);
+      for (int i = 0; i < L - ng * G; ++i) {
+        long dst = (bh(c, b, h) * 2 * G + i) * D, src = (long)(ng * G + i) * D;
+        memcpy(c->bk + dst, kp + src, sizeof(uint16_t) * D);
+        memcpy(c->bv + dst, vp + src, sizeof(uint16_t) * D);
+      }
+    }
+    s[QSO_N_GROUPS] = ng;
+    s[QSO_FILL] = L - ng * G;
+    s[QSO_PENDING] = 0;
+    s[QSO_HALF_BASE] = 0;
   }
 }
 

@@ -307,6 +307,95 @@ def test_draft_equals_verify_when_lower_is_eight(torch):
     assert np.abs(gd - gv).max() < 2e-3
 
 
+# ------------------------------------------------------------- bulk prefill
+
+def _prompt(rng, B, H, T):
+    return h16(rng, (B, H, T, 128), 2.0), h16(rng, (B, H, T, 128))
+
+
+def test_prefill_bit_exact_then_decode(torch):
+    """qs_prefill against the oracle's prefill (itself pinned to the append /
+    flush path): every array bit for bit for prompt lengths around the group
+    and buffer boundaries; then attention, a flush and an append on top."""
+    rng = np.random.default_rng(31)
+    B, H, T, cap = 6, 2, 700, 5
+    lens = np.array([0, 1, 256, 257, 385, 700], np.int32)
+    k, v = _prompt(rng, B, H, T)
+    cache = qs.Cache(B, H, cap)
+    qs.qs_prefill(cache, to_dev(torch, k), to_dev(torch, v), to_dev(torch, lens))
+    oc = oracle.OracleCache(B, H, 128, 128, cap)
+    oc.prefill(k, v, lens)
+    assert_state_equal(cache, oc, "prefill")
+    assert np.all(qs.qs_get_errors(cache) == 0) and np.all(oc.state[:, oracle.ERR] == 0)
+    for mode, n_q in ((DRAFT, 1), (VERIFY, 5)):
+        q = h16(rng, (B, H, n_q, 128))
+        got, gl = run_attn(torch, cache, mode, q)
+        ref, rl = oc.attn(q, upper_only=(mode == DRAFT))
+        assert_close(got, ref, gl, rl, "after prefill, mode %d" % mode)
+    assert np.array_equal(qs.qs_get_errors(cache), oc.state[:, oracle.ERR])
+    oc.state[:, oracle.ERR] = 0
+    mask = torch.zeros(B, dtype=torch.uint8, device="cuda")
+    qs.qs_need_flush(cache, 5, mask)
+    qs.qs_quantize_flush(cache, mask)
+    oc.flush(oc.need_flush(5))
+    k5, v5 = _prompt(rng, B, H, 5)
+    qs.qs_buffer_append(cache, to_dev(torch, k5), to_dev(torch, v5))
+    oc.append(k5, v5)
+    assert_state_equal(cache, oc, "flush + append after prefill")
+    assert np.all(qs.qs_get_errors(cache) == 0)
+
+
+def test_prefill_error_paths(torch):
+    rng = np.random.default_rng(7)
+    H, T = 1, 400
+    k, v = _prompt(rng, 4, H, T)
+    cache = qs.Cache(4, H, 1)
+    oc = oracle.OracleCache(4, H, 128, 128, 1)
+    lens = np.array([200, 400, 401, -1], np.int32)  # ok / needs 2 groups / > T / < 0
+    qs.qs_prefill(cache, to_dev(torch, k), to_dev(torch, v), to_dev(torch, lens))
+    oc.prefill(k, v, lens)
+    assert_state_equal(cache, oc, "errors")
+    errs = qs.qs_get_errors(cache)
+    assert np.array_equal(errs, oc.state[:, oracle.ERR])
+    assert list(errs) == [0, qs.DEV_CAPACITY, qs.DEV_PREFILL, qs.DEV_PREFILL]
+    oc.state[:, oracle.ERR] = 0
+    lens2 = np.array([300, 0, 0, 0], np.int32)  # sequence 0 is no longer empty
+    qs.qs_prefill(cache, to_dev(torch, k), to_dev(torch, v), to_dev(torch, lens2))
+    oc.prefill(k, v, lens2)
+    assert_state_equal(cache, oc, "non-empty")
+    assert list(qs.qs_get_errors(cache)) == [qs.DEV_PREFILL, 0, 0, 0]
+    with pytest.raises(qs.QsError) as e:
+        qs.qs_prefill(cache, to_dev(torch, k[:, :, :0]), to_dev(torch, v[:, :, :0]), None)
+    assert e.value.status == qs.QS_ERR_ARG
+
+
+def test_prefill_full_size_32k(torch):
+    """The 32k workload's whole prompt in one call (254 groups + 256 buffer
+    tokens per head, 32 heads) equals the oracle bit for bit, and equals the
+    state the append / flush path builds (logical content)."""
+    w = synthetic.llama_32k()
+    T = w.context[0]
+    k, v = synthetic.kv_tokens(w, 0, 0, T)
+    cap = w.n_groups[0] + 1
+    cache = qs.Cache(1, w.H, cap)
+    qs.qs_prefill(cache, to_dev(torch, k[None]), to_dev(torch, v[None]),
+                  to_dev(torch, np.array([T], np.int32)))
+    oc = oracle.OracleCache(1, w.H, w.D, w.G, cap)
+    oc.prefill(k[None], v[None], [T])
+    assert oc.counters(0)["n_groups"] == w.n_groups[0] and oc.counters(0)["fill"] == w.fill[0]
+    assert_state_equal(cache, oc, "32k prefill")
+    ref = qs.Cache(1, w.H, cap)
+    driver.prefill(ref, w)
+    a, b = layout.read_device(cache), layout.read_device(ref)
+    for name in ("k_upper", "k_lower", "v_upper", "v_lower", "meta"):
+        assert np.array_equal(a[name], b[name]), name
+    assert np.array_equal(a["state"][0, :3], b["state"][0, :3])
+    hb = int(b["state"][0, 3])
+    slots = (hb * w.G + np.arange(w.fill[0])) % (2 * w.G)
+    assert np.array_equal(a["buf_k"][0][:, :w.fill[0]], b["buf_k"][0][:, slots])
+    assert np.all(qs.qs_get_errors(cache) == 0)
+
+
 # ------------------------------------------------------------ full sizes
 
 def _sampled_oracle(w, bs, hs):

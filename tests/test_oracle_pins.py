@@ -427,3 +427,75 @@ def test_quantized_attention_error_is_bounded_by_dequant_error():
         e8 = np.abs(o8[0, hh, 0] - ref).max()
         eU = np.abs(oU[0, hh, 0] - ref).max()
         assert e8 < 0.02 and e8 < eU
+
+
+# --------------------------------------------------------------- bulk prefill
+
+def _appended_prompt(rng, K, V, L, cap):
+    """The state-machine path for a prompt: append its first L tokens in
+    pieces of 1..G, committing each, with a flush before every append that
+    would overflow the 2G buffer."""
+    H, D = K.shape[1], K.shape[3]
+    c = oracle.OracleCache(1, H, D, 128, cap)
+    t = 0
+    while t < L:
+        n = min(int(rng.integers(1, 129)), L - t)
+        if c.need_flush(n)[0]:
+            c.flush()
+        c.append(np.ascontiguousarray(K[:, :, t:t + n]), np.ascontiguousarray(V[:, :, t:t + n]))
+        c.rollback([0])
+        t += n
+    return c
+
+
+@pytest.mark.parametrize("L", [0, 1, 127, 128, 255, 256, 257, 383, 384, 385, 700, 1000])
+def test_prefill_equals_appending_the_prompt(L):
+    """A one-step prefill leaves the same groups, counters and logical buffer
+    as appending the prompt piece by piece through the state machine (whose
+    groups are pinned to QS-RN-v1 of the committed stream above)."""
+    rng = np.random.default_rng(500 + L)
+    H, G = 2, 128
+    K, V = _stream(rng, H, L + 7)  # the prompt array is longer than the prompt
+    ref = _appended_prompt(rng, K, V, L, cap=8)
+    pre = oracle.OracleCache(1, H, 128, G, cap=8)
+    pre.prefill(K, V, [L])
+    cr, cp = ref.counters(0), pre.counters(0)
+    assert cp["err"] == 0 and cr["err"] == 0 and cp["half_base"] == 0
+    ng = 0 if L <= 2 * G else -(-(L - 2 * G) // G)
+    assert cp["n_groups"] == cr["n_groups"] == ng
+    assert cp["fill"] == cr["fill"] == L - ng * G and cp["pending"] == cr["pending"] == 0
+    if L > 2 * G:
+        assert G < cp["fill"] <= 2 * G
+    for name in ("kq", "vq", "ks", "kz", "vs", "vz"):
+        a, b = getattr(ref, name), getattr(pre, name)
+        assert np.array_equal(a[:, :, :ng], b[:, :, :ng]), name
+        assert not b[:, :, ng:].any(), name  # groups past n_groups untouched
+    for hh in range(H):
+        for x, y in zip(ref.buffer_tokens(0, hh), pre.buffer_tokens(0, hh)):
+            assert np.array_equal(x, y)
+        # slots 0..fill-1 in order (half_base 0)
+        assert np.array_equal(pre.bk[0, hh, :cp["fill"]], K[0, hh, ng * G:L].view(np.uint16))
+
+
+def test_prefill_error_paths_are_flagged_and_no_ops():
+    rng = np.random.default_rng(7)
+    H, T = 1, 400
+    k1, v1 = _stream(rng, H, T)
+    K, V = np.concatenate([k1] * 4), np.concatenate([v1] * 4)
+    c = oracle.OracleCache(4, H, 128, 128, cap=1)
+    # ok (no group) / needs 2 groups with cap 1 / longer than T / negative
+    c.prefill(K, V, [200, 400, 401, -1])
+    assert c.counters(0) == dict(n_groups=0, fill=200, pending=0, half_base=0, err=0)
+    assert c.state[1, oracle.ERR] == oracle.DEV_CAPACITY
+    assert c.state[2, oracle.ERR] == oracle.DEV_PREFILL and c.state[3, oracle.ERR] == oracle.DEV_PREFILL
+    assert not c.state[1:, :oracle.ERR].any() and not c.bk[1:].any() and not c.kq.any()
+    # a second prefill of a non-empty cache changes nothing
+    snap = (c.state.copy(), c.bk.copy(), c.bv.copy())
+    c.prefill(K, V, [300, 0, 0, 0])
+    assert c.state[0, oracle.ERR] == oracle.DEV_PREFILL
+    assert np.array_equal(c.state[0, :oracle.ERR], snap[0][0, :oracle.ERR])
+    assert np.array_equal(c.bk, snap[1]) and np.array_equal(c.bv, snap[2])
+    # cap 1 fits exactly one group: 257..384 tokens
+    c2 = oracle.OracleCache(1, H, 128, 128, cap=1)
+    c2.prefill(k1, v1, [384])
+    assert c2.counters(0)["n_groups"] == 1 and c2.counters(0)["fill"] == 256
