@@ -542,6 +542,12 @@ def profile(args):
     r = Round(torch, w, seed=0)
     for i in range(args.warmup if args.profile == "step" else 0):
         r.step(i)
+    if args.profile == "prefill":
+        T = w.context[0]
+        kp, vp = synthetic.kv_tokens(w, 0, 0, T)
+        kp, vp = torch.from_numpy(kp[None]).cuda(), torch.from_numpy(vp[None]).cuda()
+        lens = torch.tensor([T], dtype=torch.int32, device="cuda")
+        pc = qs.Cache(1, w.H, r.cache.cap)
     for i in range(args.profile_calls):
         if args.profile == "draft":
             r.set_state(r.ng1, r.f1 + 1)
@@ -552,6 +558,9 @@ def profile(args):
         elif args.profile == "flush":
             r.cache.state.copy_(r.state0)
             qs.qs_quantize_flush(r.cache, None)
+        elif args.profile == "prefill":
+            qs.qs_state_reset(pc)
+            qs.qs_prefill(pc, kp, vp, lens)
         else:
             r.step(i)
     torch.cuda.synchronize()
@@ -569,7 +578,7 @@ def main():
     ap.add_argument("--call-iters", type=int, default=30)
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile", choices=["draft", "verify", "flush", "step"])
+    ap.add_argument("--profile", choices=["draft", "verify", "flush", "prefill", "step"])
     ap.add_argument("--profile-calls", type=int, default=3)
     args = ap.parse_args()
     if args.profile:

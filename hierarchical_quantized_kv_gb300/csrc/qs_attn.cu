@@ -11,19 +11,19 @@
 // works with Flash Decoding: split-KV partial softmax, then an LSE combine).
 //
 // Design (GB300):
-//  * One persistent CTA per resident slot (SMs x occupancy).  All (sequence,
-//    head) segments are laid end to end as units (a quantized group of 128
-//    tokens, or a chunk of fp16 buffer tokens) and every CTA takes an equal
+//  * One persistent CTA of twelve warps per SM.  All (sequence, head)
+//    segments are laid end to end as units (a quantized group of 128 tokens,
+//    or a chunk of fp16 buffer tokens) and every CTA takes an equal
 //    contiguous range, so ragged batches balance without a host round trip.
 //  * Each unit's contiguous plane blocks arrive by bulk async copies
 //    (cp.async.bulk, TMA engine) in a ring of shared-memory stages guarded by
 //    mbarriers; draft units copy only the C_U planes (8 KB keys + 8 KB values
 //    + 1 KB scales/zeros).  There is no producer warp: the last warp to finish
 //    with a stage (a shared-memory arrival counter) issues its refill, so all
-//    four warps compute and three CTAs fit on an SM.
-//  * Units alternate between the CTA's two warp pairs; within a pair each
-//    warp takes 64 tokens of the group (so per-unit fixed costs amortize over
-//    64 tokens).  Nibbles become
+//    twelve warps compute.
+//  * Warps claim half-units (64 tokens of a group) from a shared counter, so
+//    the SM's warps finish together; per-unit fixed costs amortize over 64
+//    tokens.  Nibbles become
 //    exact fp16 integers in registers (bit tricks, no conversion
 //    instructions), and the dense contractions q.K^T and P.V run on
 //    m16n8k16 tensor-core MMAs with fp32 accumulation.  Scales are folded:
@@ -31,7 +31,7 @@
 //    per-query biases, so the inner loops touch codes only.
 //  * Each warp keeps its own online softmax and writes one partial per piece
 //    of a segment it touches.  At the end of its range the CTA merges its
-//    four warps' partials (log-sum-exp); a segment split across CTAs is
+//    warps' partials (log-sum-exp); a segment split across CTAs is
 //    finished by whichever of them arrives last on the segment's counter,
 //    so the whole call is one kernel launch.
 #include <math.h>
@@ -41,7 +41,7 @@
 namespace qs {
 namespace {
 
-constexpr int kPairs = 6;               // warp pairs per CTA; a pair computes one unit
+constexpr int kPairs = 6;               // units in compute at once (two half-units each)
 constexpr int kWarps = 2 * kPairs;
 constexpr int kThreads = kWarps * 32;  // one CTA per SM
 constexpr int kTailRow = 272;  // padded fp16 row stride (bytes) of buffer tiles
@@ -53,7 +53,7 @@ template <>
 struct Cfg<QS_DRAFT_UPPER4> {
   static constexpr int kGroupBytes = 8192 + 8192 + 1024;
   static constexpr int kTailTok = 32;
-  static constexpr int kStages = 2 * kPairs;  // a unit in compute and one in flight per pair
+  static constexpr int kStages = 2 * kPairs;  // about one unit in flight per unit in compute
 };
 template <>
 struct Cfg<QS_VERIFY_INT8> {
@@ -72,8 +72,7 @@ struct Layout {
   static constexpr int kBarOff = Cfg<MODE>::kStages * kStageBytes;               // full barriers
   static constexpr int kCntOff = align16(kBarOff + 8 * Cfg<MODE>::kStages);      // release counters
   static constexpr int kIssOff = align16(kCntOff + 4 * Cfg<MODE>::kStages);      // unit per stage
-  static constexpr int kClaimOff = align16(kIssOff + 4 * Cfg<MODE>::kStages);    // claimed units
-  static constexpr int kZeroOff = align16(kClaimOff + 4 * 2 * kPairs);          // zero row (ldmatrix)
+  static constexpr int kZeroOff = align16(kIssOff + 4 * Cfg<MODE>::kStages);     // zero row (ldmatrix)
   static constexpr int kTabOff = kZeroOff + 32;
   // per-sequence tables: n_groups, fill, half_base, segment length, base
   // unit, first segment ordinal
@@ -354,21 +353,16 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 }
 
 // ------------------------------------------------------- log-sum-exp merge
-// CTA-wide (128 threads) merge of ns partials of one (sequence, head).
-// Partial k starts at src + k * kstride floats and holds, for each query
-// j < n_q, the unnormalized O_j[d] at j * 128 + d, then m_j (log2 domain) at
-// n_q * 128 + j and l_j at n_q * 128 + 8 + j:
+// Merge of ns partials of one (sequence, head): partial k < nA starts at
+// srcA + k * kstrideA floats, partial k >= nA at srcB + (k - nA) * kstrideB.
+// Each holds, for each query j < n_q, the unnormalized O_j[d] at j * 128 + d,
+// then m_j (log2 domain) at n_q * 128 + j and l_j at n_q * 128 + 8 + j:
 //   M_j = max_k m_kj,  L_j = sum_k 2^(m_kj - M_j) l_kj,
 //   O_j = sum_k 2^(m_kj - M_j) O_kj.
 // final: out_j = O_j / L_j (fp16) and lse_j = (M_j + log2 L_j) ln 2; else the
-// merged partial is written to dst (same layout; dst may be partial 0).
-// Lanes hold four channels each.  The twelve warps take jpr queries at once
-// (the smallest divisor of twelve >= n_q) and split the partials into
-// 12 / jpr phases, merged at the end through `red` (384 x 6 floats of shared
-// memory).  Each thread loads its partials eight at a time, all eight in
-// flight before the first is used.  A partial with m = -inf is empty (its l
-// and O are not read into the sums; they may be stale).  src is a generic
-// address: shared memory, or global memory written by other CTAs.
+// merged partial is written to dst (same layout; dst may be partial 0 of the
+// sources).  A partial with m = -inf is empty (its l and O are not read into
+// the sums; they may be stale).
 struct MergeOut {
   bool final;
   uint16_t *out;  // final: fp16 [n_q][128] of this (sequence, head)
@@ -391,101 +385,108 @@ __device__ __forceinline__ float4 ld_part4(const float *p) {
   return v;
 }
 
-// Not inlined: it runs once per piece at the end of the kernel, when its
-// instructions are not in the instruction cache, so one small copy matters
-// more than call overhead.
-__device__ __noinline__ void merge_partials(const float *src, int kstride, int ns, int n_q,
+// CTA-wide: lanes hold four channels each; the twelve warps take jpr
+// queries at once (the smallest divisor of twelve >= n_q) and split the
+// partials into 12 / jpr phases.  Each thread loads its partials four at a
+// time, all four in flight before the first is used; the phases then meet
+// in `red` (384 x 6 floats of shared memory): the largest m first, then one
+// independent rescale per phase.  Not inlined: it runs at the end of the
+// kernel from a cold instruction cache, where one small copy matters more
+// than the call.
+__device__ __noinline__ void merge_partials(const float *srcA, int kstrideA, int nA,
+                                            const float *srcB, int kstrideB, int ns, int n_q,
                                             const MergeOut &mo, float *red) {
-  constexpr int kBatch = 4;  // partials whose loads are all in flight together
+  constexpr int kBatch = 4;
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int jpr = n_q <= 4 ? n_q : (n_q <= 6 ? 6 : 12);  // queries at once
-  const int ph = kWarps / jpr, phase = w / jpr;
+  const int ph = kWarps / jpr, phase = w / jpr, j = w % jpr;
   const int mo_off = n_q * kD;
-  const int j = w % jpr;
   float M = -INFINITY, L = 0.f;
   float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
-  {
-    if (j < n_q) {
+  if (j < n_q) {
 #pragma unroll 1
-      for (int kb = phase; kb < ns; kb += kBatch * ph) {
-        float ms[kBatch], ls[kBatch];
-        float4 os[kBatch];
+    for (int kb = phase; kb < ns; kb += kBatch * ph) {
+      float ms[kBatch], ls[kBatch];
+      float4 os[kBatch];
 #pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-          const int k = kb + u * ph;
+      for (int u = 0; u < kBatch; ++u) {
+        const int k = kb + u * ph;
+        ms[u] = -INFINITY;
+        ls[u] = 0.f;
+        os[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (k < ns) {
+          const float *sk = k < nA ? srcA + k * kstrideA : srcB + (k - nA) * kstrideB;
+          ms[u] = ld_part(sk + mo_off + j);
+          ls[u] = ld_part(sk + mo_off + 8 + j);
+          os[u] = ld_part4(sk + j * kD + 4 * lane);
+        }
+      }
+      float mn = M;
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        if (!(ms[u] > -INFINITY)) {  // empty partial: stale l and O stay out
           ms[u] = -INFINITY;
           ls[u] = 0.f;
           os[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (k < ns) {
-            const float *sk = src + k * kstride;
-            ms[u] = ld_part(sk + mo_off + j);
-            ls[u] = ld_part(sk + mo_off + 8 + j);
-            os[u] = ld_part4(sk + j * kD + 4 * lane);
-          }
         }
-        float mn = M;
-#pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-          if (!(ms[u] > -INFINITY)) {  // empty partial: stale l and O stay out
-            ms[u] = -INFINITY;
-            ls[u] = 0.f;
-            os[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-          }
-          mn = fmaxf(mn, ms[u]);
-        }
-        if (mn == -INFINITY) continue;  // nothing visible so far
-        const float a = (M == -INFINITY) ? 0.f : fast_exp2(M - mn);
-        L *= a;
-        A.x *= a; A.y *= a; A.z *= a; A.w *= a;
-#pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-          const float f = (ms[u] == -INFINITY) ? 0.f : fast_exp2(ms[u] - mn);
-          L = fmaf(f, ls[u], L);
-          A.x = fmaf(f, os[u].x, A.x);
-          A.y = fmaf(f, os[u].y, A.y);
-          A.z = fmaf(f, os[u].z, A.z);
-          A.w = fmaf(f, os[u].w, A.w);
-        }
-        M = mn;
+        mn = fmaxf(mn, ms[u]);
       }
+      if (mn == -INFINITY) continue;  // nothing visible so far
+      const float a = (M == -INFINITY) ? 0.f : fast_exp2(M - mn);
+      L *= a;
+      A.x *= a; A.y *= a; A.z *= a; A.w *= a;
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const float f = (ms[u] == -INFINITY) ? 0.f : fast_exp2(ms[u] - mn);
+        L = fmaf(f, ls[u], L);
+        A.x = fmaf(f, os[u].x, A.x);
+        A.y = fmaf(f, os[u].y, A.y);
+        A.z = fmaf(f, os[u].z, A.z);
+        A.w = fmaf(f, os[u].w, A.w);
+      }
+      M = mn;
     }
-    if (ph > 1) {  // merge the phases (warps jpr apart) through shared memory
-      float *mine = red + 6 * threadIdx.x;
-      mine[0] = M; mine[1] = L; mine[2] = A.x; mine[3] = A.y; mine[4] = A.z; mine[5] = A.w;
-      __syncthreads();
-      if (phase == 0) {
+  }
+  if (ph > 1) {  // the phases (warps jpr apart) meet in shared memory
+    float *mine = red + 6 * threadIdx.x;
+    mine[0] = M; mine[1] = L; mine[2] = A.x; mine[3] = A.y; mine[4] = A.z; mine[5] = A.w;
+    __syncthreads();
+    if (phase == 0 && j < n_q) {
+      float mx = M;
+      for (int q = 1; q < ph; ++q) mx = fmaxf(mx, red[6 * (threadIdx.x + 32 * jpr * q)]);
+      if (mx != -INFINITY) {
+        const float f0 = (M == -INFINITY) ? 0.f : fast_exp2(M - mx);
+        L *= f0;
+        A.x *= f0; A.y *= f0; A.z *= f0; A.w *= f0;
         for (int q = 1; q < ph; ++q) {
           const float *o = red + 6 * (threadIdx.x + 32 * jpr * q);
-          const float ms = o[0];
-          const float mn = fmaxf(M, ms);
-          const float a = (M == -INFINITY) ? 0.f : fast_exp2(M - mn);
-          const float f = (ms == -INFINITY) ? 0.f : fast_exp2(ms - mn);
-          L = fmaf(L, a, f * o[1]);
-          A.x = fmaf(A.x, a, f * o[2]);
-          A.y = fmaf(A.y, a, f * o[3]);
-          A.z = fmaf(A.z, a, f * o[4]);
-          A.w = fmaf(A.w, a, f * o[5]);
-          M = mn;
+          const float f = (o[0] == -INFINITY) ? 0.f : fast_exp2(o[0] - mx);
+          L = fmaf(f, o[1], L);
+          A.x = fmaf(f, o[2], A.x);
+          A.y = fmaf(f, o[3], A.y);
+          A.z = fmaf(f, o[4], A.z);
+          A.w = fmaf(f, o[5], A.w);
         }
+        M = mx;
       }
-      __syncthreads();  // red is free again; every read of src is done
-    } else {
-      __syncwarp();  // the warp's reads of query j are done before dst is written
     }
-    if (phase == 0 && j < n_q) {
-      if (mo.final) {
-        const float Ld = L > 0.f ? L : 1.f;  // L > 0 whenever a token is visible
-        uint2 h;
-        h.x = pack_half2(A.x / Ld, A.y / Ld);
-        h.y = pack_half2(A.z / Ld, A.w / Ld);
-        *reinterpret_cast<uint2 *>(mo.out + j * kD + 4 * lane) = h;
-        if (mo.lse && lane == 0) mo.lse[j] = (M + log2f(L)) * 0.69314718055994531f;
-      } else {
-        __stcg(reinterpret_cast<float4 *>(mo.dst + j * kD) + lane, A);
-        if (lane == 0) {
-          __stcg(mo.dst + mo_off + j, M);
-          __stcg(mo.dst + mo_off + 8 + j, L);
-        }
+    __syncthreads();  // red is free again; every read of the sources is done
+  } else {
+    __syncwarp();  // the warp's reads of query j are done before dst is written
+  }
+  if (phase == 0 && j < n_q) {
+    if (mo.final) {
+      const float Ld = L > 0.f ? L : 1.f;  // L > 0 whenever a token is visible
+      uint2 h;
+      h.x = pack_half2(A.x / Ld, A.y / Ld);
+      h.y = pack_half2(A.z / Ld, A.w / Ld);
+      *reinterpret_cast<uint2 *>(mo.out + j * kD + 4 * lane) = h;
+      if (mo.lse && lane == 0) mo.lse[j] = (M + log2f(L)) * 0.69314718055994531f;
+    } else {
+      __stcg(reinterpret_cast<float4 *>(mo.dst + j * kD) + lane, A);
+      if (lane == 0) {
+        __stcg(mo.dst + mo_off + j, M);
+        __stcg(mo.dst + mo_off + 8 + j, L);
       }
     }
   }
@@ -524,11 +525,6 @@ __device__ __forceinline__ void write_empty(float *dst, int n_q, int lane) {
   }
 }
 
-// Barrier of the two warps of pair `id - 1` (named barrier `id`, 64 threads).
-__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
-
 // Wait (bounded) until a stage's copy of unit i has been issued.
 __device__ __forceinline__ bool wait_issued(volatile int *issued, int i) {
   if (*issued == i) return true;
@@ -551,16 +547,15 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const Params prm) {
   extern __shared__ __align__(128) uint8_t smem[];
   const qs_cache &c = prm.c;
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int pr = w >> 1, hw = w & 1;  // warp pair, half of a unit
+
   const int r = lane >> 2, cq = lane & 3;
   const uint32_t sbase = smem_addr(smem);
   const uint32_t full0 = sbase + L::kBarOff, zero_row = sbase + L::kZeroOff;
   int *cnt = reinterpret_cast<int *>(smem + L::kCntOff);            // releases per stage
   volatile int *issued = reinterpret_cast<int *>(smem + L::kIssOff);  // unit copied into a stage
-  volatile int *claim = reinterpret_cast<int *>(smem + L::kClaimOff); // [pair][2] claimed unit
   Tables T = tables_at(smem, L::kTabOff);
   __shared__ long long s_total;
-  __shared__ int s_abort, s_next, s_seg[2], s_ord[2], s_need[2], s_last[2];
+  __shared__ int s_abort, s_next, s_left_first, s_first_fin, s_seg[2], s_ord[2], s_need[2], s_last[2];
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -571,6 +566,8 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const Params prm) {
     fence_mbar_init();
     s_next = 0;
     s_abort = 0;
+    s_left_first = 0;
+    s_first_fin = 0;
   }
   if (threadIdx.x < 8) reinterpret_cast<uint32_t *>(smem + L::kZeroOff)[threadIdx.x] = 0;
   pdl_trigger();
@@ -604,6 +601,31 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const Params prm) {
   const int ord_first = first.ord, ord_last = lastseg.ord;
   // partial slot of warp ww for the piece of segment ordinal o
   auto slot = [&](int o, int ww) { return prm.ws + ((size_t)(o + p) * kWarps + ww) * stride; };
+  // A segment split across CTAs p_lo..p_hi is finished by whichever CTA
+  // arrives last on its counter.  CTAs p_lo..p_hi-1 hold it as their last
+  // piece and arrive with one merged CTA partial at the end.  CTA p_hi holds
+  // it as its first piece; when its range goes on past the segment it does
+  // not merge it at all: the warp that leaves the piece last arrives for the
+  // CTA (the twelve warp partials are all written and fenced by then), and
+  // the finishing CTA reads those twelve partials directly.
+  const bool shared_first = ord_first != ord_last && first.s0 < x0;
+  auto leave = [&](int o) {
+    if (!shared_first || o != ord_first) return;
+    __syncwarp();
+    __threadfence();  // this warp's partial is visible before it counts
+    int last = 0;
+    if (lane == 0) last = atomicAdd(&s_left_first, 1) == kWarps - 1;
+    if (!__shfl_sync(0xffffffffu, last, 0)) return;
+    __threadfence();
+    const long long seg = (long long)first.b * c.H + first.h;
+    const int plo = cta_of(first.s0, U, prm.P);  // the segment ends in this range: p_hi = p
+    if (lane == 0 && atomicAdd(&c.arrive[seg], 1) == p - plo) {
+      // rare: the CTAs before have all arrived; this CTA finishes the segment
+      // at its end
+      atomicExch(&c.arrive[seg], 0);  // every other arrival is in
+      s_first_fin = 1;
+    }
+  };
 
   // units i and i + S share stage i % S; warp 0 issues the first S
   if (w == 0) {
@@ -621,23 +643,36 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const Params prm) {
   int fill = 0, ng = 0;
   int cur_ord = -1;  // segment ordinal of this warp's softmax state (-1: none yet)
   Seg cur, ahead;
-  for (int k = 0;; ++k) {
-    // the pair's leader claims the next unit; both warps take it after the
-    // pair barrier (claims alternate between two slots)
-    if (hw == 0 && lane == 0) {
-      int i = *reinterpret_cast<volatile int *>(&s_abort) ? n : atomicAdd(&s_next, 1);
-      claim[2 * pr + (k & 1)] = i < n ? i : n;
-    }
-    named_bar_sync(1 + pr, 64);
-    const int i = claim[2 * pr + (k & 1)];
-    if (i >= n) break;
+  // Work is claimed in half-units (claim h: unit h / 2, tokens of half h % 2)
+  // from one shared counter.  Both halves of a unit go to whichever warps
+  // claim them; the stage's release counter joins them again.  Draft claims
+  // one ahead, so the atomic's latency hides behind a unit's compute; verify,
+  // whose ring holds only as many units as are in compute, claims when free
+  // (a claim made ahead would wait on a copy that cannot start yet).
+  constexpr bool kAhead = MODE == QS_DRAFT_UPPER4;
+  auto claim = [&]() {
+    int h = 0;
+    if (lane == 0) h = *reinterpret_cast<volatile int *>(&s_abort) ? 2 * n : atomicAdd(&s_next, 1);
+    return __shfl_sync(0xffffffffu, h, 0);
+  };
+  int h_next = kAhead ? claim() : 0;
+  for (;;) {
+    const int hcl = kAhead ? h_next : claim();
+    if (hcl >= 2 * n) break;
+    if (kAhead) h_next = claim();
+    const int i = hcl >> 1, hw = hcl & 1;
     cur.seek(x0 + i, T, c.B);
     if (cur.ord != cur_ord) {
       // a new piece: the finished one's partial (empty ones for pieces this
       // warp skipped), then fresh state and this head's queries
-      if (cur_ord >= 0) write_partial(sm, slot(cur_ord, w), prm.n_q, lane);
-      for (int o = cur_ord >= 0 ? cur_ord + 1 : ord_first; o < cur.ord; ++o)
+      if (cur_ord >= 0) {
+        write_partial(sm, slot(cur_ord, w), prm.n_q, lane);
+        leave(cur_ord);
+      }
+      for (int o = cur_ord >= 0 ? cur_ord + 1 : ord_first; o < cur.ord; ++o) {
         write_empty(slot(o, w), prm.n_q, lane);
+        leave(o);
+      }
       cur_ord = cur.ord;
       const size_t bh = (size_t)cur.b * c.H + cur.h;
       const int qi = PK ? (r >> 1) : r;  // the query in B column r
@@ -880,7 +915,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const Params prm) {
 
     }
 
-    // release the stage; the later warp of the pair issues the refill
+    // release the stage; the later of the unit's two halves issues the refill
     // (unit i + S) unless its own wait failed
     __syncwarp();
     int last = 0;
@@ -899,14 +934,19 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const Params prm) {
   }
   // this warp's partials for the pieces after its last unit's piece are empty
   // (all but the range's last piece go to the workspace)
-  if (cur_ord >= 0 && cur_ord < ord_last) write_partial(sm, slot(cur_ord, w), prm.n_q, lane);
-  for (int o = cur_ord >= 0 ? cur_ord + 1 : ord_first; o < ord_last; ++o)
+  if (cur_ord >= 0 && cur_ord < ord_last) {
+    write_partial(sm, slot(cur_ord, w), prm.n_q, lane);
+    leave(cur_ord);
+  }
+  for (int o = cur_ord >= 0 ? cur_ord + 1 : ord_first; o < ord_last; ++o) {
     write_empty(slot(o, w), prm.n_q, lane);
+    leave(o);
+  }
 
   __syncthreads();
   // no copy may still be landing in the stage memory reused below: after a
   // timeout, wait for each stage's last copy (otherwise every issued copy
-  // has been waited for by the pair that claimed its unit)
+  // has been waited for by the warps that claimed its halves)
   if (w == 0 && s_abort) {
     const unsigned long long deadline = globaltimer_ns() + kWaitLimitNs;
     for (int s = lane; s < S; s += 32) {
@@ -918,23 +958,33 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const Params prm) {
   }
   __syncthreads();
 
-  // ---- log-sum-exp merge.  Per piece of this CTA's range: merge the twelve
-  // warp partials (the last piece's straight from registers through shared
-  // memory); a segment that lies wholly in the range is final here.  A
-  // segment shared with other CTAs gets one CTA partial (in warp slot 0) and
-  // an arrival on its counter; the CTA that arrives last merges the CTA
-  // partials of the whole segment and resets the counter.  Only the first
-  // and the last piece of a range can be shared.
+  // ---- log-sum-exp merge.  Per piece of this CTA's range (but a shared
+  // first piece, see above): merge the twelve warp partials (the last piece's
+  // straight from registers through shared memory); a segment that lies
+  // wholly in the range is final here.  A segment shared with other CTAs gets
+  // one CTA partial (in warp slot 0) and an arrival on its counter; the CTA
+  // that arrives last merges the CTA partials of the whole segment and
+  // resets the counter.  Only the first and the last piece of a range can be
+  // shared.
   const bool aborted = s_abort != 0;
   float *red = reinterpret_cast<float *>(smem);                 // stage memory, free now
   float *last_part = reinterpret_cast<float *>(smem + 16384);  // kWarps partials
   if (cur_ord == ord_last) write_partial(sm, last_part + w * stride, prm.n_q, lane);
   else write_empty(last_part + w * stride, prm.n_q, lane);
   __syncthreads();
+  if (s_first_fin && !aborted) {
+    __threadfence();  // the other CTAs' partials are visible from here on
+    const long long seg = (long long)first.b * c.H + first.h;
+    const int plo = cta_of(first.s0, U, prm.P);
+    const MergeOut fo{true, prm.out + (size_t)seg * prm.n_q * kD,
+                      prm.lse ? prm.lse + (size_t)seg * prm.n_q : nullptr, nullptr};
+    merge_partials(prm.ws + (size_t)(ord_first + plo) * kWarps * stride, kWarps * stride, p - plo,
+                   slot(ord_first, 0), stride, p - plo + kWarps, prm.n_q, fo, red);
+  }
   int n_arr = 0;
   {
     Seg pc;
-    int x = x0;
+    int x = shared_first ? first.s0 + first.len : x0;  // the first piece is done already
     while (x < x1) {
       pc.seek(x, T, c.B);
       const long long seg = (long long)pc.b * c.H + pc.h;
@@ -942,10 +992,9 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const Params prm) {
       const int plo = cta_of(S0, U, prm.P), phi = cta_of(E0 - 1, U, prm.P);
       const MergeOut mo{plo == phi, prm.out + (size_t)seg * prm.n_q * kD,
                         prm.lse ? prm.lse + (size_t)seg * prm.n_q : nullptr, slot(pc.ord, 0)};
-      if (!aborted) {
-        merge_partials(pc.ord == ord_last ? last_part : slot(pc.ord, 0), stride, kWarps, prm.n_q, mo,
-                       red);
-      }
+      if (!aborted)
+        merge_partials(pc.ord == ord_last ? last_part : slot(pc.ord, 0), stride, kWarps, nullptr, 0,
+                       kWarps, prm.n_q, mo, red);
       if (plo != phi) {
         if (threadIdx.x == 0) {
           s_seg[n_arr] = (int)seg;
@@ -978,9 +1027,15 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const Params prm) {
     const int plo = cta_of(S0, U, prm.P), phi = cta_of(E0 - 1, U, prm.P);
     const MergeOut mo{true, prm.out + (size_t)seg * prm.n_q * kD,
                       prm.lse ? prm.lse + (size_t)seg * prm.n_q : nullptr, nullptr};
-    // CTA pp's partial of this segment is in its warp slot 0
-    merge_partials(prm.ws + ((size_t)(s_ord[a] + plo) * kWarps) * stride, kWarps * stride,
-                   phi - plo + 1, prm.n_q, mo, red);
+    // CTA pp's partial of this segment is in its warp slot 0, except that
+    // CTA p_hi left its twelve warp partials when the segment was only the
+    // first piece of its range
+    const bool raw = S0 < range_lo(phi, U, prm.P) && E0 < range_lo(phi + 1, U, prm.P);
+    const float *cta0 = prm.ws + ((size_t)(s_ord[a] + plo) * kWarps) * stride;
+    const float *raw0 = prm.ws + ((size_t)(s_ord[a] + phi) * kWarps) * stride;
+    const int nA = raw ? phi - plo : phi - plo + 1;
+    merge_partials(cta0, kWarps * stride, nA, raw0, stride, nA + (raw ? kWarps : 0), prm.n_q, mo,
+                   red);
   }
 }
 
