@@ -66,6 +66,7 @@ def lib():
         for name, args in (("qso_append", [P, P, P, I]), ("qso_rollback", [P, P]),
                            ("qso_need_flush", [P, I, P]), ("qso_flush", [P, P]),
                            ("qso_prefill", [P, P, P, I, P]),
+                           ("qso_spec_accept", [P, P, P, P, P, I, I, I, P, P, P]),
                            ("qso_attn", [P, I, P, I, D_, P, P])):
             f = getattr(L, name)
             f.restype = None
@@ -123,6 +124,21 @@ def split_code(q):
 
 def dequant(q, scale_bits, zero_bits, upper_only):
     return lib().qso_dequant(int(q), int(scale_bits), int(zero_bits), int(bool(upper_only)))
+
+
+def spec_accept(p, q, draft, u, e):
+    """Speculative-sampling verification (see qso_spec_accept): p [B, g+1, V],
+    q [B, g, V], u [B, g] float32; draft [B, g] int32; e [B, V] float32 Exp(1)
+    variates.  Returns (n_accept, token, n_drop), int32 [B] each."""
+    p, q, u, e = (np.ascontiguousarray(x, np.float32) for x in (p, q, u, e))
+    draft = np.ascontiguousarray(draft, np.int32)
+    B, g1, V = p.shape
+    g = g1 - 1
+    assert q.shape == (B, g, V) and draft.shape == (B, g) and u.shape == (B, g) and e.shape == (B, V)
+    na, tok, nd = (np.zeros(B, np.int32) for _ in range(3))
+    lib().qso_spec_accept(_ptr(p), _ptr(q), _ptr(draft), _ptr(u), _ptr(e), B, g, V,
+                          _ptr(na), _ptr(tok), _ptr(nd))
+    return na, tok, nd
 
 
 def num_threads():

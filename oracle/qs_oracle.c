@@ -349,6 +349,79 @@ void qso_prefill(qso_cache *c, const uint16_t *k, const uint16_t *v, int T,
   }
 }
 
+/* ------------------------------------------------ speculative acceptance */
+
+/* Draw from the distribution proportional to w[0..V-1] (non-negative) by an
+ * exponential race: with e_x independent Exp(1) variates, the index of the
+ * smallest e_x / w_x over w_x > 0 is distributed as w / sum(w).  Ties go to
+ * the smaller index; -1 if every weight is 0.  Each quotient is one IEEE fp32
+ * division. */
+static int race(const float *w, const float *e, int V) {
+  int best = -1;
+  float key = 0.0f;
+  for (int x = 0; x < V; ++x) {
+    if (!(w[x] > 0.0f)) continue;
+    float k = e[x] / w[x];
+    if (best < 0 || k < key) {
+      best = x;
+      key = k;
+    }
+  }
+  return best;
+}
+
+/* Speculative-sampling verification for B sequences, gamma draft tokens each.
+ *   p     [B][gamma+1][V]  target probabilities at the gamma+1 positions
+ *   q     [B][gamma][V]    draft probabilities the draft tokens came from
+ *   draft [B][gamma]       draft tokens
+ *   u     [B][gamma]       uniforms in [0, 1), one per draft token
+ *   e     [B][V]           Exp(1) variates for the one draw per sequence
+ * Draft token i is accepted when u_i * q_i(x_i) < p_i(x_i) (probability
+ * min(1, p_i(x_i) / q_i(x_i))); the first rejection at position a stops the
+ * round and the emitted token is drawn from the residual
+ * max(0, p_a - q_a) (from p_a if that residual is all zero); with every draft
+ * token accepted it is drawn from p_gamma.  A draft token outside [0, V) is
+ * rejected.  Outputs: n_accept[b] = a, token[b] (or -1 if the weights are all
+ * zero) and n_drop[b] = gamma - a (the rollback count of the synthetic round).
+ * Pith review page, referee report on Algorithm 1 (VERIFY / CORRECT as
+ * rejection sampling with acceptance min(1, p/q) and residual (p - q)_+);
+ * [P1] "The Self-Speculative Verification Loop" (acceptance test, stop at
+ * the first rejection). */
+void qso_spec_accept(const float *p, const float *q, const int32_t *draft,
+                     const float *u, const float *e, int B, int gamma, int V,
+                     int32_t *n_accept, int32_t *token, int32_t *n_drop) {
+  float *w = malloc(sizeof(float) * (size_t)V);
+  for (int b = 0; b < B; ++b) {
+    const float *pb = p + (size_t)b * (gamma + 1) * V;
+    const float *qb = q + (size_t)b * gamma * V;
+    int a = 0;
+    while (a < gamma) {
+      int x = draft[(size_t)b * gamma + a];
+      float pa = (x >= 0 && x < V) ? pb[(size_t)a * V + x] : 0.0f;
+      float qa = (x >= 0 && x < V) ? qb[(size_t)a * V + x] : 0.0f;
+      if (x < 0 || x >= V || !(u[(size_t)b * gamma + a] * qa < pa)) break;
+      ++a;
+    }
+    const float *eb = e + (size_t)b * V;
+    int t;
+    if (a < gamma) {
+      const float *pr = pb + (size_t)a * V, *qr = qb + (size_t)a * V;
+      for (int x = 0; x < V; ++x) {
+        float d = pr[x] - qr[x];
+        w[x] = d > 0.0f ? d : 0.0f;
+      }
+      t = race(w, eb, V);
+      if (t < 0) t = race(pr, eb, V);
+    } else {
+      t = race(pb + (size_t)gamma * V, eb, V);
+    }
+    n_accept[b] = a;
+    token[b] = t;
+    n_drop[b] = gamma - a;
+  }
+  free(w);
+}
+
 /* -------------------------------------------------------------- attention */
 
 /* Decode attention in fp64 for every (b, h) and each of n_q queries

@@ -499,3 +499,89 @@ def test_prefill_error_paths_are_flagged_and_no_ops():
     c2 = oracle.OracleCache(1, H, 128, 128, cap=1)
     c2.prefill(k1, v1, [384])
     assert c2.counters(0)["n_groups"] == 1 and c2.counters(0)["fill"] == 256
+
+
+# ------------------------------------------------ speculative acceptance
+
+def _spec_inputs(rng, p, q, N):
+    """N independent rounds with the same p, q rows: draft tokens drawn from q
+    (inverse CDF), acceptance uniforms and Exp(1) variates."""
+    g = q.shape[0]
+    V = p.shape[1]
+    draft = np.empty((N, g), np.int32)
+    for i in range(g):
+        cdf = np.cumsum(q[i].astype(np.float64))
+        draft[:, i] = np.minimum(np.searchsorted(cdf, rng.random(N) * cdf[-1], side="right"), V - 1)
+    u = rng.random((N, g)).astype(np.float32)
+    e = rng.exponential(size=(N, V)).astype(np.float32)
+    P = np.ascontiguousarray(np.broadcast_to(p, (N,) + p.shape))
+    Q = np.ascontiguousarray(np.broadcast_to(q, (N,) + q.shape))
+    return P, Q, draft, u, e
+
+
+def _z(count, n, prob):
+    return abs(count - n * prob) / np.sqrt(max(n * prob * (1 - prob), 1e-12))
+
+
+def test_spec_accept_preserves_the_target_distribution():
+    """Speculative sampling's defining property, checked by simulation (fixed
+    seed, 5-sigma bounds): the first emitted token is distributed as p_0 (the
+    draft token when accepted, else the residual draw), the first token is
+    accepted with probability sum_x min(p_0, q_0), the token after an accepted
+    one is distributed as p_1, and the bonus token after gamma acceptances as
+    p_gamma.  A wrong acceptance ratio, a draw from p instead of (p - q)_+, or
+    a shifted position all fail it."""
+    rng = np.random.default_rng(2024)
+    V, g, N = 5, 3, 200000
+    p = np.array([[0.40, 0.10, 0.20, 0.05, 0.25],
+                  [0.05, 0.50, 0.15, 0.20, 0.10],
+                  [0.30, 0.30, 0.10, 0.10, 0.20],
+                  [0.10, 0.10, 0.10, 0.60, 0.10]], np.float32)
+    q = np.array([[0.10, 0.40, 0.20, 0.25, 0.05],
+                  [0.30, 0.20, 0.20, 0.10, 0.20],
+                  [0.20, 0.20, 0.20, 0.20, 0.20]], np.float32)
+    P, Q, draft, u, e = _spec_inputs(rng, p, q, N)
+    na, tok, nd = oracle.spec_accept(P, Q, draft, u, e)
+    assert np.array_equal(nd, g - na) and na.min() >= 0 and na.max() <= g
+    y0 = np.where(na >= 1, draft[:, 0], tok)
+    for x in range(V):
+        assert _z((y0 == x).sum(), N, p[0, x]) < 5, ("y0", x)
+    acc = float(np.minimum(p[0], q[0]).sum())
+    assert _z((na >= 1).sum(), N, acc) < 5
+    sel = na >= 1
+    y1 = np.where(na[sel] >= 2, draft[sel, 1], tok[sel])
+    for x in range(V):
+        assert _z((y1 == x).sum(), sel.sum(), p[1, x]) < 5, ("y1", x)
+    allacc = na == g
+    assert allacc.sum() > 1000
+    for x in range(V):
+        assert _z((tok[allacc] == x).sum(), allacc.sum(), p[g, x]) < 5, ("bonus", x)
+
+
+def test_spec_accept_special_cases():
+    V, g = 6, 4
+    rng = np.random.default_rng(3)
+    p = rng.dirichlet(np.ones(V), g + 1).astype(np.float32)
+    q = p[:g].copy()
+    draft = np.array([[1, 2, 3, 4]], np.int32)
+    u = np.full((1, g), 0.999, np.float32)
+    e = np.array([[3.0, 0.5, 2.0, 1.0, 0.25, 4.0]], np.float32)
+    # q == p: every draft token is accepted; the bonus comes from p_gamma
+    na, tok, nd = oracle.spec_accept(p[None], q[None], draft, u, e)
+    assert na[0] == g and nd[0] == 0
+    assert tok[0] == int(np.argmin(e[0] / p[g]))
+    # a draft token the target gives probability 0 is rejected there, and the
+    # draw excludes every token where p <= q
+    p2 = p.copy()
+    p2[2, 0] += p2[2, 3]  # the mass of token 3 moves to token 0
+    p2[2, 3] = 0.0
+    na, tok, nd = oracle.spec_accept(p2[None], q[None], draft, u, e)
+    assert na[0] == 2 and nd[0] == 2
+    assert tok[0] == 0  # the only token with p > q at position 2
+    # a draft token outside [0, V) is rejected
+    na, _, _ = oracle.spec_accept(p[None], q[None], np.array([[1, 2, V, 4]], np.int32), u, e)
+    assert na[0] == 2
+    # all-zero weights: token -1
+    z = np.zeros((1, g + 1, V), np.float32)
+    na, tok, nd = oracle.spec_accept(z, np.zeros((1, g, V), np.float32), draft, u, e)
+    assert na[0] == 0 and tok[0] == -1 and nd[0] == g
