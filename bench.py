@@ -364,6 +364,18 @@ def native(args):
         assert torch.equal(pc.state[0, :4].cpu(), r.state0[0, :4].cpu())
         prefill_gbs = prefill_bytes(T, w.H) / prefill_us / 1e3
         del kp, vp, pc
+    # speculative acceptance for the round (synthetic probabilities over a
+    # 32,000-token vocabulary): accept/reject, the emitted token, n_drop
+    V = 32000
+    g_ = torch.Generator(device="cuda").manual_seed(0)
+    pp = torch.softmax(torch.randn((w.B, GAMMA + 1, V), device="cuda", generator=g_), dim=-1)
+    qq = torch.softmax(torch.randn((w.B, GAMMA, V), device="cuda", generator=g_), dim=-1)
+    dr = torch.randint(0, V, (w.B, GAMMA), device="cuda", dtype=torch.int32, generator=g_)
+    uu = torch.rand((w.B, GAMMA), device="cuda", generator=g_)
+    ee = torch.empty((w.B, V), device="cuda").exponential_(generator=g_)
+    sa = [torch.empty(w.B, dtype=torch.int32, device="cuda") for _ in range(3)]
+    spec_us = time_calls(torch, lambda: qs.qs_spec_accept(pp, qq, dr, uu, ee, *sa), lambda: None, it,
+                         l2)
     draft_b, verify_b = r.bytes["draft"][0], r.bytes["verify"]
     draft_gbs, verify_gbs = draft_b / draft_us / 1e3, verify_b / verify_us / 1e3
     # dominant kernel by device time within a step
@@ -415,6 +427,7 @@ def native(args):
         "flush_us": round(flush_us, 2),
         "prefill_us": None if prefill_us is None else round(prefill_us, 2),
         "prefill_gbs": None if prefill_gbs is None else round(prefill_gbs, 1),
+        "spec_accept_us": round(spec_us, 2),
         "roofline": {"bound": "hbm", "kernel": "qs_attn_decode %s (split_kernel: split-KV attention + LSE merge, one launch)" % dominant[0],
                      "achieved": round(dominant[1], 1), "peak": peak,
                      "peak_kind": "%s hbm_gbs (copy, burst)" % peak_kind, "unit": "GB/s",

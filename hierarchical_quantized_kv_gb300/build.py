@@ -12,7 +12,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libqs.so")
-SOURCES = ["qs_buffer.cu", "qs_quantize.cu", "qs_attn.cu", "qs_attn_static.cu"]
+SOURCES = ["qs_buffer.cu", "qs_quantize.cu", "qs_attn.cu", "qs_attn_static.cu", "qs_spec.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC = os.environ.get("NVCC", "nvcc")
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",

@@ -187,23 +187,13 @@ struct Seg {
   }
 };
 
-// ---- nibble / byte planes -> exact centred fp16 integers (half2 per pair) -
-// Pair p of a 32-bit word holds elements (p, p + 4) of its 8 nibbles.  Draft
-// returns 16 C_U - 128, verify the 8-bit code minus 128, C_INT8 - 128 =
-// 16 C_U + C_L - 128.  Centring keeps s * code close to k - (z + 128 s), the
-// middle of the group's range, so the fp16 rounding of q * s and p * s_V acts
-// on values of the size of the data instead of their distance to the group
-// minimum; the 128 s (draft: 136 s, the midpoint 8 included) goes into the
-// zero-point bias, computed in fp32.  Every subtraction below is exact.
-__device__ __forceinline__ void pairs_upper(uint32_t w, uint32_t (&e)[4]) {
-  const uint32_t w8 = w >> 8;
-  // bits 0-3 under exponent 2^14: 16384 + 16 n; bits 4-7 under 2^10: 1024 + 16 n
-  e[0] = hsub2_u32(and_or(w, 0x000F000Fu, 0x74007400u), 0x74087408u);   // - 16512
-  e[1] = hsub2_u32(and_or(w, 0x00F000F0u, 0x64006400u), 0x64806480u);   // - 1152
-  e[2] = hsub2_u32(and_or(w8, 0x000F000Fu, 0x74007400u), 0x74087408u);
-  e[3] = hsub2_u32(and_or(w8, 0x00F000F0u, 0x64006400u), 0x64806480u);
-}
-
+// ---- nibble / byte planes -> exact fp16 integers (half2 per pair) --------
+// Pair p of a 32-bit word holds elements (p, p + 4) of its 8 nibbles.
+// Verify returns the 8-bit code minus 128, C_INT8 - 128 = 16 C_U + C_L - 128
+// (centred).  Centring keeps s * code close to k - (z + 128 s), the middle of
+// the group's range, so the fp16 rounding of p * s_V acts on values of the
+// size of the data instead of their distance to the group minimum; the 128 s
+// goes into the zero-point bias, computed in fp32.  Every subtraction is exact.
 __device__ __forceinline__ void pairs_int8(uint32_t wu, uint32_t wl, uint32_t (&e)[4]) {
   const uint32_t ev = bitsel(wl, wu << 4, 0x0F0F0F0Fu);   // codes 0,2,4,6
   const uint32_t od = bitsel(wl >> 4, wu, 0x0F0F0F0Fu);   // codes 1,3,5,7
@@ -214,15 +204,33 @@ __device__ __forceinline__ void pairs_int8(uint32_t wu, uint32_t wl, uint32_t (&
   e[3] = hsub2_u32(prmt(od, 0x64646464u, 0x4341), 0x64806480u);
 }
 
-// Offset, in units of the scale, that centring moves into the zero-point term.
+// Draft returns each C_U as 1024 + 16 C_U (the nibble under mantissa bits
+// 4-7 of 2^10): three shifts and four LOP3 per word, no subtraction.  The
+// constant 1152 above the centred value 16 C_U - 128 is taken out exactly:
+// for keys through the zero-point bias (B = q * s is carried to ~2^-22, and
+// the ratio 1152 / 16 of offset to code step keeps the fp32 accumulation
+// error negligible), for values by an MMA of ones against the same fp16 P'
+// the codes are multiplied with, so the result equals the centred product.
+__device__ __forceinline__ void pairs_upper_raw(uint32_t w, uint32_t (&e)[4]) {
+  e[0] = and_or(w << 4, 0x00F000F0u, 0x64006400u);
+  e[1] = and_or(w, 0x00F000F0u, 0x64006400u);
+  e[2] = and_or(w >> 4, 0x00F000F0u, 0x64006400u);
+  e[3] = and_or(w >> 8, 0x00F000F0u, 0x64006400u);
+}
+constexpr float kRawOff = 1152.f;  // pairs_upper_raw value minus the centred value
+
+// Offset, in units of the scale, that the zero-point terms carry: the
+// centring (verify 128; draft 136, the midpoint 8 included) and, for draft
+// keys read raw, minus 1152.
 template <int MODE>
 struct Centre {
   static constexpr float kOff = (MODE == QS_DRAFT_UPPER4) ? 136.f : 128.f;
+  static constexpr float kOffK = (MODE == QS_DRAFT_UPPER4) ? 136.f - kRawOff : 128.f;
 };
 
 template <int MODE>
 __device__ __forceinline__ void pairs(uint32_t wu, uint32_t wl, uint32_t (&e)[4]) {
-  if (MODE == QS_DRAFT_UPPER4) pairs_upper(wu, e);
+  if (MODE == QS_DRAFT_UPPER4) pairs_upper_raw(wu, e);
   else pairs_int8(wu, wl, e);
 }
 
@@ -725,11 +733,12 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const Params prm) {
           mma16816(bacc, zw.x, sw.x, zw.y, sw.y, qp0[k0], qp1[k0]);
           mma16816(bacc2, zw.z, sw.z, zw.w, sw.w, qp0[k1], qp1[k1]);
         }
-        // key dequant s (code - 128) + (z + kOff s): bias = sum q z + kOff sum q s
+        // key dequant s (code - 128) + (z + kOff s) with the code as read
+        // (draft: raw, code - 128 + 1152): bias = sum q z + kOffK sum q s
         const float bk0 =
-            fmaf(Centre<MODE>::kOff, bacc[2] + bacc2[2], bacc[0] + bacc2[0]) * prm.sl2;
+            fmaf(Centre<MODE>::kOffK, bacc[2] + bacc2[2], bacc[0] + bacc2[0]) * prm.sl2;
         const float bk1 =
-            fmaf(Centre<MODE>::kOff, bacc[3] + bacc2[3], bacc[1] + bacc2[1]) * prm.sl2;
+            fmaf(Centre<MODE>::kOffK, bacc[3] + bacc2[3], bacc[1] + bacc2[1]) * prm.sl2;
 
         // raw scores (q.k before scale and bias): four m-tiles of 16 tokens
         float s[4][4];
@@ -814,6 +823,22 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const Params prm) {
             }
             bp0[mt] = movmatrix_trans(pack_half2(pv[0], pv[1]));
             bp1[mt] = movmatrix_trans(pack_half2(pv[2], pv[3]));
+          }
+        }
+        if (MODE == QS_DRAFT_UPPER4) {
+          // value codes are read raw (1152 above their centred value): take
+          // 1152 * sum_t P'_t out of the value bias, the sum formed by the
+          // tensor core from the same fp16 P' it multiplies the codes with
+          constexpr uint32_t kOnes = 0x3C003C00u;  // fp16 (1, 1)
+          float sp[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int mt = 0; mt < 4; ++mt) mma16816(sp, kOnes, kOnes, kOnes, kOnes, bp0[mt], bp1[mt]);
+          // every row of the product holds the column sum, while the value
+          // bias is a per-lane partial summed over the eight row lanes later:
+          // one lane per column takes it
+          if (r == 0) {
+            sm.bv[0] = fmaf(-kRawOff, sp[0], sm.bv[0]);
+            sm.bv[1] = fmaf(-kRawOff, sp[1], sm.bv[1]);
           }
         }
         // O^T = a O^T + V^T P'  (values: quarters 2hw and 2hw+1, channel-major)

@@ -61,6 +61,7 @@ _SIGS = {
                        _P, _P, ctypes.c_size_t, _P],
     "qs_get_errors": [ctypes.POINTER(QsCacheStruct), _P, _P],
     "qs_prefill": [ctypes.POINTER(QsCacheStruct), _P, _P, _I32, _P, _P],
+    "qs_spec_accept": [_P, _P, _P, _P, _P, _I32, _I32, _I32, _P, _P, _P, _P],
 }
 
 
@@ -178,6 +179,17 @@ def qs_prefill(cache, k, v, lens, stream=None):
     assert k.is_contiguous() and v.is_contiguous() and k.shape == v.shape
     _check("qs_prefill", lib().qs_prefill(cache._ref, _ptr(k), _ptr(v), int(k.shape[2]), _ptr(lens),
                                           _stream(stream)))
+
+
+def qs_spec_accept(p, q, draft, u, e, n_accept, token, n_drop, stream=None):
+    """p [B, g+1, V], q [B, g, V], u [B, g], e [B, V]: float32 device tensors;
+    draft [B, g] int32; outputs n_accept, token, n_drop: int32 [B] tensors."""
+    B, g1, V = p.shape
+    for t in (p, q, draft, u, e):
+        assert t.is_contiguous()
+    _check("qs_spec_accept", lib().qs_spec_accept(_ptr(p), _ptr(q), _ptr(draft), _ptr(u), _ptr(e), B,
+                                                  g1 - 1, V, _ptr(n_accept), _ptr(token),
+                                                  _ptr(n_drop), _stream(stream)))
 
 
 def qs_attn_workspace_size(cache, n_q):

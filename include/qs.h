@@ -207,6 +207,37 @@ qs_status qs_quantize_flush(const qs_cache *c, const uint8_t *d_mask, qs_stream_
 qs_status qs_prefill(const qs_cache *c, const uint16_t *k, const uint16_t *v, int32_t T,
                      const int32_t *d_len, qs_stream_t stream);
 
+/* Speculative-sampling acceptance for B sequences with gamma draft tokens
+ * each (1 <= gamma <= 64), vocabulary V; all arrays are device arrays, read
+ * or written only by this call, 4-byte aligned:
+ *   p        float [B][gamma+1][V]  target probabilities at the gamma + 1
+ *                                   positions (the last one for the bonus)
+ *   q        float [B][gamma][V]    draft probabilities the draft tokens were
+ *                                   sampled from
+ *   draft    int32 [B][gamma]       the draft tokens
+ *   u        float [B][gamma]       uniforms in [0, 1), one per draft token
+ *   e        float [B][V]           Exp(1) variates for the one draw per
+ *                                   sequence (positive)
+ *   n_accept int32 [B] (out)        accepted draft tokens a
+ *   token    int32 [B] (out)        the token emitted after them, or -1 if its
+ *                                   weights are all zero
+ *   n_drop   int32 [B] (out)        gamma - a: pass it to qs_buffer_rollback
+ * Draft token i is accepted when u_i * q_i(x_i) < p_i(x_i) in fp32, i.e. with
+ * probability min(1, p_i(x_i) / q_i(x_i)); the first rejection at position a
+ * ends the round and the token is drawn from max(0, p_a - q_a) (from p_a if
+ * that is zero everywhere); after gamma acceptances it is drawn from p_gamma.
+ * A draft token outside [0, V) is rejected.  Draws: the index of the smallest
+ * e_x / w_x over w_x > 0 (ties to the smaller index), which is distributed as
+ * w / sum(w).  One cluster of 8 CTAs per sequence splits the vocabulary.
+ * Errors: QS_ERR_ARG (null pointer, B outside 1..65535, gamma outside 1..64,
+ * V < 1), QS_ERR_ALIGN.  Source: Pith review page, referee report on
+ * Algorithm 1 (VERIFY / CORRECT as rejection sampling with acceptance
+ * min(1, p/q) and residual (p - q)_+); "QuantSpec Guide", "The
+ * Self-Speculative Verification Loop". */
+qs_status qs_spec_accept(const float *p, const float *q, const int32_t *draft, const float *u,
+                         const float *e, int32_t B, int32_t gamma, int32_t V, int32_t *n_accept,
+                         int32_t *token, int32_t *n_drop, qs_stream_t stream);
+
 /* Bytes of device workspace qs_attn_decode needs for n_q queries (1..8) on
  * the current device.  Pure host function (reads device attributes). */
 qs_status qs_attn_workspace_size(const qs_cache *c, int32_t n_q, size_t *bytes);

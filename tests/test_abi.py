@@ -101,3 +101,20 @@ def test_pack_unpack_roundtrip():
         byte = vu[a, b2, uu, d, p // 2]
         nib = (byte >> (4 * (p % 2))) & 15
         assert nib == kq[a, b2, 32 * uu + layout.vperm(p), d] >> 4
+
+
+def test_prefill_and_spec_accept_host_validation(L):
+    c = _fake_cache()
+    p = ctypes.c_void_p(0x20000)
+    assert L.qs_prefill(ctypes.byref(c), None, p, 10, p, None) == qs.QS_ERR_ARG
+    assert L.qs_prefill(ctypes.byref(c), p, p, -1, p, None) == qs.QS_ERR_ARG
+    assert L.qs_prefill(ctypes.byref(c), ctypes.c_void_p(0x20008), p, 10, p, None) == qs.QS_ERR_ALIGN
+    f = L.qs_spec_accept
+    args = [p] * 5 + [4, 4, 100] + [p] * 3 + [None]  # valid shape: not launched here
+    for i, bad in ((0, None), (5, 0), (6, 0), (6, 65), (7, 0), (9, None)):
+        a = list(args)
+        a[i] = bad
+        assert f(*a) == qs.QS_ERR_ARG, (i, bad)
+    a = list(args)
+    a[3] = ctypes.c_void_p(0x20002)
+    assert f(*a) == qs.QS_ERR_ALIGN
