@@ -67,7 +67,7 @@ def lib():
                            ("qso_need_flush", [P, I, P]), ("qso_flush", [P, P]),
                            ("qso_prefill", [P, P, P, I, P]),
                            ("qso_spec_accept", [P, P, P, P, P, I, I, I, P, P, P]),
-                           ("qso_attn", [P, I, P, I, D_, P, P])):
+                           ("qso_attn", [P, I, P, I, I, D_, P, P])):
             f = getattr(L, name)
             f.restype = None
             f.argtypes = args
@@ -206,18 +206,20 @@ class OracleCache:
         c = self._c()
         lib().qso_prefill(ctypes.byref(c), _ptr(kb), _ptr(vb), kb.shape[2], _ptr(n))
 
-    def attn(self, q, upper_only, scale=None):
-        """Decode attention in fp64: q [B, H, n_q, D] fp16 ->
-        (out [B, H, n_q, D] float64, lse [B, H, n_q] float64)."""
+    def attn(self, q, upper_only, scale=None, group=1):
+        """Decode attention in fp64: q [B, H*group, n_q, D] fp16 ->
+        (out [B, H*group, n_q, D] float64, lse [B, H*group, n_q] float64);
+        query head h*group + i reads KV head h."""
         qb = _as_half_bits(q)
+        assert qb.shape[1] == self.H * group
         n_q = qb.shape[2]
         if scale is None:
             scale = 1.0 / np.sqrt(self.D)
         scale = float(np.float32(scale))
-        out = np.zeros((self.B, self.H, n_q, self.D), np.float64)
-        lse = np.zeros((self.B, self.H, n_q), np.float64)
+        out = np.zeros((self.B, self.H * group, n_q, self.D), np.float64)
+        lse = np.zeros((self.B, self.H * group, n_q), np.float64)
         c = self._c()
-        lib().qso_attn(ctypes.byref(c), int(bool(upper_only)), _ptr(qb), n_q, scale,
+        lib().qso_attn(ctypes.byref(c), int(bool(upper_only)), _ptr(qb), n_q, int(group), scale,
                        _ptr(out), _ptr(lse))
         return out, lse
 

@@ -424,17 +424,19 @@ void qso_spec_accept(const float *p, const float *q, const int32_t *draft,
 
 /* -------------------------------------------------------------- attention */
 
-/* Decode attention in fp64 for every (b, h) and each of n_q queries
- * (q: [B][H][n_q][D] fp16).  Keys/values are the dequantized groups
+/* Decode attention in fp64 for every (b, h) and each of n_q queries of each
+ * of the `group` query heads that share KV head h (grouped-query attention;
+ * group = 1 is multi-head): q is [B][H*group][n_q][D] fp16, query head
+ * h*group + i reads KV head h.  Keys/values are the dequantized groups
  * (upper_only = 1: draft, 16*C_U + 8; 0: verify, INT8) followed by the fp16
  * buffer tokens.  Query j sits at the position of buffer token
  * fill - n_q + j and sees every token at or before it.  Writes
- * out [B][H][n_q][D] and lse [B][H][n_q] (natural log of the softmax
- * denominator of the scaled scores).  A sequence with n_q > fill gets
+ * out [B][H*group][n_q][D] and lse [B][H*group][n_q] (natural log of the
+ * softmax denominator of the scaled scores).  A sequence with n_q > fill gets
  * QSO_DEV_NQ_GT_FILL, zero output and lse = -inf.
  * [P1] "Hierarchical Two-Level Quantization" (draft loads upper 4 bits,
  * target reconstructs INT8); [P3] "What carries the argument". */
-void qso_attn(qso_cache *c, int upper_only, const uint16_t *q, int n_q,
+void qso_attn(qso_cache *c, int upper_only, const uint16_t *q, int n_q, int group,
               double scale, double *out, double *lse) {
   int G = c->G, D = c->D;
   for (int b = 0; b < c->B; ++b)
@@ -445,9 +447,9 @@ void qso_attn(qso_cache *c, int upper_only, const uint16_t *q, int n_q,
       const int32_t *s = st(c, b);
       int ng = s[QSO_N_GROUPS], fill = s[QSO_FILL];
       long Tq = (long)ng * G, T = Tq + fill;
-      long o = bh(c, b, h) * n_q;
+      long o = bh(c, b, h) * group * n_q; /* rows of query heads h*group.. */
       if (n_q > fill) {
-        for (int j = 0; j < n_q; ++j) {
+        for (int j = 0; j < group * n_q; ++j) {
           for (int d = 0; d < D; ++d) out[(o + j) * D + d] = 0.0;
           lse[o + j] = -INFINITY;
         }
@@ -475,8 +477,9 @@ void qso_attn(qso_cache *c, int upper_only, const uint16_t *q, int n_q,
         }
       }
       double *S = malloc(sizeof(double) * T);
-      for (int j = 0; j < n_q; ++j) {
-        const uint16_t *qj = q + (o + j) * D;
+      for (int gj = 0; gj < group * n_q; ++gj) {
+        int j = gj % n_q; /* query head h*group + gj / n_q, position j */
+        const uint16_t *qj = q + (o + gj) * D;
         long last = Tq + fill - n_q + j; /* causal limit */
         double m = -INFINITY;
         for (long t = 0; t <= last; ++t) {
@@ -492,12 +495,12 @@ void qso_attn(qso_cache *c, int upper_only, const uint16_t *q, int n_q,
           S[t] = exp(S[t] - m);
           l += S[t];
         }
-        double *oj = out + (o + j) * D;
+        double *oj = out + (o + gj) * D;
         for (int d = 0; d < D; ++d) oj[d] = 0.0;
         for (long t = 0; t <= last; ++t)
           for (int d = 0; d < D; ++d) oj[d] += S[t] * V[t * D + d];
         for (int d = 0; d < D; ++d) oj[d] /= l;
-        lse[o + j] = m + log(l);
+        lse[o + gj] = m + log(l);
       }
       free(S);
       free(K);

@@ -585,3 +585,29 @@ def test_spec_accept_special_cases():
     z = np.zeros((1, g + 1, V), np.float32)
     na, tok, nd = oracle.spec_accept(z, np.zeros((1, g, V), np.float32), draft, u, e)
     assert na[0] == 0 and tok[0] == -1 and nd[0] == g
+
+
+# ------------------------------------------------ grouped-query attention
+
+@pytest.mark.parametrize("group,n_q", [(1, 5), (4, 1), (4, 5), (3, 8)])
+def test_grouped_query_attention_equals_replicated_heads(group, n_q):
+    """Query head h*g + i of grouped-query attention attends KV head h: the
+    result equals multi-head attention on a cache whose KV heads are each
+    repeated g times (same fp64 arithmetic, so bit for bit), in both modes."""
+    rng = np.random.default_rng(40 + group * 10 + n_q)
+    B, H, T = 2, 2, 700
+    k = h(rng.standard_normal((B, H, T, 128)) * 2)
+    v = h(rng.standard_normal((B, H, T, 128)))
+    oc = oracle.OracleCache(B, H, 128, 128, cap=4)
+    oc.prefill(k, v, [T, 300])
+    rep = oracle.OracleCache(B, H * group, 128, 128, cap=4)
+    for name in ("kq", "vq", "ks", "kz", "vs", "vz", "bk", "bv"):
+        setattr(rep, name, np.ascontiguousarray(np.repeat(getattr(oc, name), group, axis=1)))
+    rep.state = oc.state.copy()
+    q = h(rng.standard_normal((B, H * group, n_q, 128)))
+    for upper in (True, False):
+        o1, l1 = oc.attn(q, upper, group=group)
+        o2, l2 = rep.attn(q, upper)
+        assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+    # and the rows differ across the query heads of one KV head
+    assert not np.array_equal(o1[:, 0], o1[:, group - 1]) or group == 1
