@@ -76,13 +76,14 @@ def load_peaks():
 
 # ---------------------------------------------------------------- bytes
 
-def attn_bytes(ng, fill, n_q, mode_draft, BH):
+def attn_bytes(ng, fill, n_q, mode_draft, BH, group=1):
     """Algorithmic bytes of one decode-attention call per the method: the
     quantized planes it must read (draft: C_U + scales/zeros = 136 B per
     token-head; verify: C_U + C_L + scales/zeros = 264 B), the fp16 buffer
-    tokens (512 B each), the queries and the outputs."""
+    tokens (512 B each), the queries and the outputs (group query heads per
+    KV head)."""
     grp = (8 * KB + 8 * KB + KB) if mode_draft else (4 * 8 * KB + KB)
-    return BH * (ng * grp + fill * 512 + n_q * 256 * 2)
+    return BH * (ng * grp + fill * 512 + group * n_q * 256 * 2)
 
 
 FLUSH_BYTES_PER_HEAD = 2 * 128 * 256 + 4 * 8 * KB + KB   # read both halves' rows, write planes + meta
@@ -283,6 +284,34 @@ def time_calls(torch, fn, setup, iters, l2_scratch):
     return statistics.mean(ts[1:]) if len(ts) > 1 else ts[0]
 
 
+def gqa_calls(torch, qs, synthetic, l2, it):
+    """Grouped-query decode attention on the Llama-3.1-8B shape (8 KV heads,
+    32 query heads, 32k context): per-call draft (4 rows per KV head) and
+    5-query verify (20 rows) times and GB/s, L2 evicted before each call."""
+    w = synthetic.llama31_8b_32k()
+    T = w.context[0]
+    k, v = synthetic.kv_tokens(w, 0, 0, T)
+    cache = qs.Cache(1, w.H, w.n_groups[0] + 1)
+    qs.qs_prefill(cache, torch.from_numpy(k[None]).cuda(), torch.from_numpy(v[None]).cuda(),
+                  torch.tensor([T], dtype=torch.int32, device="cuda"))
+    res = {"workload": w.name}
+    for call, (name, mode, n_q) in enumerate((("draft", qs.QS_DRAFT_UPPER4, 1),
+                                              ("verify", qs.QS_VERIFY_INT8, GAMMA + 1))):
+        q = torch.from_numpy(synthetic.queries(w, call, n_q)).cuda()
+        out = torch.empty_like(q)
+        lse = torch.empty(q.shape[:3], dtype=torch.float32, device="cuda")
+        ws = torch.empty(qs.qs_attn_workspace_size_gqa(cache, n_q, w.group), dtype=torch.uint8,
+                         device="cuda")
+        us = time_calls(torch, lambda: qs.qs_attn_decode_gqa(cache, mode, q, w.group, 1 / np.sqrt(w.D),
+                                                              out, lse, ws), lambda: None, it, l2)
+        nb = attn_bytes(w.n_groups[0], w.fill[0], n_q, mode == qs.QS_DRAFT_UPPER4, w.H, w.group)
+        res[name + "_us"] = round(us, 2)
+        res[name + "_gbs"] = round(nb / us / 1e3, 1)
+    assert np.all(qs.qs_get_errors(cache) == 0)
+    del cache
+    return res
+
+
 def native(args):
     import torch
     import torch.distributed as dist
@@ -364,6 +393,7 @@ def native(args):
         assert torch.equal(pc.state[0, :4].cpu(), r.state0[0, :4].cpu())
         prefill_gbs = prefill_bytes(T, w.H) / prefill_us / 1e3
         del kp, vp, pc
+    gqa = gqa_calls(torch, qs, synthetic, l2, it) if w.name == synthetic.llama_32k().name else None
     # speculative acceptance for the round (synthetic probabilities over a
     # 32,000-token vocabulary): accept/reject, the emitted token, n_drop
     V = 32000
@@ -428,6 +458,7 @@ def native(args):
         "prefill_us": None if prefill_us is None else round(prefill_us, 2),
         "prefill_gbs": None if prefill_gbs is None else round(prefill_gbs, 1),
         "spec_accept_us": round(spec_us, 2),
+        "gqa": gqa,
         "roofline": {"bound": "hbm", "kernel": "qs_attn_decode %s (split_kernel: split-KV attention + LSE merge, one launch)" % dominant[0],
                      "achieved": round(dominant[1], 1), "peak": peak,
                      "peak_kind": "%s hbm_gbs (copy, burst)" % peak_kind, "unit": "GB/s",

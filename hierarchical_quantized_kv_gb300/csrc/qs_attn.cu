@@ -42,6 +42,7 @@ namespace qs {
 namespace {
 
 constexpr int kPairs = 6;               // units in compute at once (two half-units each)
+constexpr int kMaxR = 24;              // query rows per KV head (three column groups of 8)
 constexpr int kWarps = 2 * kPairs;
 constexpr int kThreads = kWarps * 32;  // one CTA per SM
 constexpr int kTailRow = 272;  // padded fp16 row stride (bytes) of buffer tiles
@@ -87,7 +88,10 @@ struct Params {
   uint16_t *out;
   float *lse;
   float *ws;
-  int n_q;
+  int n_q;    // query positions (causal, the last n_q buffer tokens)
+  int R;      // query rows per KV head: group * n_q (row r: query head r / n_q,
+              // position r % n_q)
+  int ncg;    // column groups of eight rows, ceil(R / 8): warp w serves group w % ncg
   int P;      // split-kernel grid size (number of contiguous unit ranges)
   float sl2;  // softmax_scale * log2(e)
 };
@@ -393,25 +397,30 @@ __device__ __forceinline__ float4 ld_part4(const float *p) {
   return v;
 }
 
-// CTA-wide: lanes hold four channels each; the twelve warps take jpr
-// queries at once (the smallest divisor of twelve >= n_q) and split the
-// partials into 12 / jpr phases.  Each thread loads its partials four at a
-// time, all four in flight before the first is used; the phases then meet
-// in `red` (384 x 6 floats of shared memory): the largest m first, then one
-// independent rescale per phase.  Not inlined: it runs at the end of the
-// kernel from a cold instruction cache, where one small copy matters more
+// CTA-wide: lanes hold four channels each; the twelve warps take jpr rows
+// at once (the smallest divisor of twelve >= R, or twelve in rounds) and
+// split the partials into 12 / jpr phases.  Each thread loads its partials
+// four at a time, all four in flight before the first is used; the phases
+// then meet in `red` (384 x 6 floats of shared memory): the largest m first,
+// then one independent rescale per phase.  Row j's partials start at
+// srcA + (j / 8) * cgA (and srcB + (j / 8) * cgB): warp partials hold only
+// the rows of their warp's column group.  Not inlined: it runs at the end of
+// the kernel from a cold instruction cache, where one small copy matters more
 // than the call.
-__device__ __noinline__ void merge_partials(const float *srcA, int kstrideA, int nA,
-                                            const float *srcB, int kstrideB, int ns, int n_q,
-                                            const MergeOut &mo, float *red) {
+__device__ __noinline__ void merge_partials(const float *srcA, int cgA, int kstrideA, int nA,
+                                            const float *srcB, int cgB, int kstrideB, int ns,
+                                            int R, const MergeOut &mo, float *red) {
   constexpr int kBatch = 4;
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int jpr = n_q <= 4 ? n_q : (n_q <= 6 ? 6 : 12);  // queries at once
-  const int ph = kWarps / jpr, phase = w / jpr, j = w % jpr;
-  const int mo_off = n_q * kD;
+  const int jpr = R <= 4 ? R : (R <= 6 ? 6 : 12);  // rows at once
+  const int ph = kWarps / jpr, phase = w / jpr;
+  const int mo_off = R * kD;
+#pragma unroll 1
+  for (int j = w % jpr; j - w % jpr < R; j += jpr) {  // rounds of jpr rows
+  const float *a0 = srcA + (j >> 3) * cgA, *b0 = srcB + (j >> 3) * cgB;
   float M = -INFINITY, L = 0.f;
   float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (j < n_q) {
+  if (j < R) {
 #pragma unroll 1
     for (int kb = phase; kb < ns; kb += kBatch * ph) {
       float ms[kBatch], ls[kBatch];
@@ -423,9 +432,9 @@ __device__ __noinline__ void merge_partials(const float *srcA, int kstrideA, int
         ls[u] = 0.f;
         os[u] = make_float4(0.f, 0.f, 0.f, 0.f);
         if (k < ns) {
-          const float *sk = k < nA ? srcA + k * kstrideA : srcB + (k - nA) * kstrideB;
+          const float *sk = k < nA ? a0 + k * kstrideA : b0 + (k - nA) * kstrideB;
           ms[u] = ld_part(sk + mo_off + j);
-          ls[u] = ld_part(sk + mo_off + 8 + j);
+          ls[u] = ld_part(sk + mo_off + kMaxR + j);
           os[u] = ld_part4(sk + j * kD + 4 * lane);
         }
       }
@@ -459,7 +468,7 @@ __device__ __noinline__ void merge_partials(const float *srcA, int kstrideA, int
     float *mine = red + 6 * threadIdx.x;
     mine[0] = M; mine[1] = L; mine[2] = A.x; mine[3] = A.y; mine[4] = A.z; mine[5] = A.w;
     __syncthreads();
-    if (phase == 0 && j < n_q) {
+    if (phase == 0 && j < R) {
       float mx = M;
       for (int q = 1; q < ph; ++q) mx = fmaxf(mx, red[6 * (threadIdx.x + 32 * jpr * q)]);
       if (mx != -INFINITY) {
@@ -482,7 +491,7 @@ __device__ __noinline__ void merge_partials(const float *srcA, int kstrideA, int
   } else {
     __syncwarp();  // the warp's reads of query j are done before dst is written
   }
-  if (phase == 0 && j < n_q) {
+  if (phase == 0 && j < R) {
     if (mo.final) {
       const float Ld = L > 0.f ? L : 1.f;  // L > 0 whenever a token is visible
       uint2 h;
@@ -494,42 +503,47 @@ __device__ __noinline__ void merge_partials(const float *srcA, int kstrideA, int
       __stcg(reinterpret_cast<float4 *>(mo.dst + j * kD) + lane, A);
       if (lane == 0) {
         __stcg(mo.dst + mo_off + j, M);
-        __stcg(mo.dst + mo_off + 8 + j, L);
+        __stcg(mo.dst + mo_off + kMaxR + j, L);
       }
     }
   }
+  }  // rounds
 }
 
 // One warp's partial of a piece (unnormalized, log2 domain; m = -inf if the
-// warp saw no visible token) in the layout merge_partials reads; dst is in
-// global or shared memory.
-__device__ __forceinline__ void write_partial(const Softmax &sm, float *dst, int n_q, int lane) {
+// warp saw no visible token) in the layout merge_partials reads: rows
+// [8 cg, 8 cg + 8) of R, O at row * 128 + d, m at R * 128 + row, l at
+// R * 128 + 24 + row; dst is in global or shared memory.
+__device__ __forceinline__ void write_partial(const Softmax &sm, float *dst, int R, int cg,
+                                              int lane) {
   const int r = lane >> 2, cq = lane & 3;
   const float l0 = warp_sum8(sm.l[0]), l1 = warp_sum8(sm.l[1]);
   const float v0 = warp_sum8(sm.bv[0]), v1 = warp_sum8(sm.bv[1]);
-  const int j0 = 2 * cq, j1 = 2 * cq + 1;
+  const int j0 = 8 * cg + 2 * cq, j1 = j0 + 1;
 #pragma unroll
   for (int md = 0; md < 8; ++md) {
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
       const int d = 16 * md + r + 8 * hh;
-      if (j0 < n_q) dst[j0 * kD + d] = sm.o[md][2 * hh] + v0;
-      if (j1 < n_q) dst[j1 * kD + d] = sm.o[md][2 * hh + 1] + v1;
+      if (j0 < R) dst[j0 * kD + d] = sm.o[md][2 * hh] + v0;
+      if (j1 < R) dst[j1 * kD + d] = sm.o[md][2 * hh + 1] + v1;
     }
   }
   if (r == 0) {
     const float m0 = sm.m[0] == -INFINITY ? -INFINITY : sm.m[0] - kExpShift;
     const float m1 = sm.m[1] == -INFINITY ? -INFINITY : sm.m[1] - kExpShift;
-    if (j0 < n_q) { dst[n_q * kD + j0] = m0; dst[n_q * kD + 8 + j0] = l0; }
-    if (j1 < n_q) { dst[n_q * kD + j1] = m1; dst[n_q * kD + 8 + j1] = l1; }
+    if (j0 < R) { dst[R * kD + j0] = m0; dst[R * kD + kMaxR + j0] = l0; }
+    if (j1 < R) { dst[R * kD + j1] = m1; dst[R * kD + kMaxR + j1] = l1; }
   }
 }
 
-// An empty partial (the warp saw none of the piece): m = -inf, l = 0.
-__device__ __forceinline__ void write_empty(float *dst, int n_q, int lane) {
-  if (lane < n_q) {
-    dst[n_q * kD + lane] = -INFINITY;
-    dst[n_q * kD + 8 + lane] = 0.f;
+// An empty partial of column group cg (the warp saw none of the piece):
+// m = -inf, l = 0 for its rows.
+__device__ __forceinline__ void write_empty(float *dst, int R, int cg, int lane) {
+  const int j = 8 * cg + lane;
+  if (lane < 8 && j < R) {
+    dst[R * kD + j] = -INFINITY;
+    dst[R * kD + kMaxR + j] = 0.f;
   }
 }
 
@@ -563,7 +577,8 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const Params prm) {
   volatile int *issued = reinterpret_cast<int *>(smem + L::kIssOff);  // unit copied into a stage
   Tables T = tables_at(smem, L::kTabOff);
   __shared__ long long s_total;
-  __shared__ int s_abort, s_next, s_left_first, s_first_fin, s_seg[2], s_ord[2], s_need[2], s_last[2];
+  __shared__ int s_abort, s_left_first, s_first_fin, s_seg[2], s_ord[2], s_need[2], s_last[2];
+  __shared__ int s_next[3];  // claim counter per column group
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -572,7 +587,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const Params prm) {
       issued[s] = -1;
     }
     fence_mbar_init();
-    s_next = 0;
+    s_next[0] = s_next[1] = s_next[2] = 0;
     s_abort = 0;
     s_left_first = 0;
     s_first_fin = 0;
@@ -587,12 +602,13 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const Params prm) {
   __syncthreads();
   const long long U = s_total;
   const int p = blockIdx.x;
-  const int stride = prm.n_q * kD + 16;  // floats per partial
+  const int R = prm.R, ncg = prm.ncg, cg = w % ncg;  // this warp's column group
+  const int stride = R * kD + 2 * kMaxR;             // floats per partial
 
   // sequences with n_q > fill see no token: zero outputs, lse = -inf, error
   for (int b = p; b < c.B; b += prm.P) {
     if (T.len[b] != 0) continue;
-    const size_t nh = (size_t)c.H * prm.n_q;
+    const size_t nh = (size_t)c.H * R;
     uint4 *o = reinterpret_cast<uint4 *>(prm.out + (size_t)b * nh * kD);
     for (size_t i = threadIdx.x; i < nh * (kD / 8); i += kThreads) o[i] = make_uint4(0, 0, 0, 0);
     if (prm.lse)
@@ -660,7 +676,8 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const Params prm) {
   constexpr bool kAhead = MODE == QS_DRAFT_UPPER4;
   auto claim = [&]() {
     int h = 0;
-    if (lane == 0) h = *reinterpret_cast<volatile int *>(&s_abort) ? 2 * n : atomicAdd(&s_next, 1);
+    if (lane == 0)
+      h = *reinterpret_cast<volatile int *>(&s_abort) ? 2 * n : atomicAdd(&s_next[cg], 1);
     return __shfl_sync(0xffffffffu, h, 0);
   };
   int h_next = kAhead ? claim() : 0;
@@ -674,17 +691,17 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const Params prm) {
       // a new piece: the finished one's partial (empty ones for pieces this
       // warp skipped), then fresh state and this head's queries
       if (cur_ord >= 0) {
-        write_partial(sm, slot(cur_ord, w), prm.n_q, lane);
+        write_partial(sm, slot(cur_ord, w), R, cg, lane);
         leave(cur_ord);
       }
       for (int o = cur_ord >= 0 ? cur_ord + 1 : ord_first; o < cur.ord; ++o) {
-        write_empty(slot(o, w), prm.n_q, lane);
+        write_empty(slot(o, w), R, cg, lane);
         leave(o);
       }
       cur_ord = cur.ord;
       const size_t bh = (size_t)cur.b * c.H + cur.h;
-      const int qi = PK ? (r >> 1) : r;  // the query in B column r
-      load_q_pairs(prm.q + (bh * prm.n_q + qi) * kD, qi < prm.n_q, cq, qp0, qp1);
+      const int qi = PK ? (r >> 1) : 8 * cg + r;  // the query row in B column r
+      load_q_pairs(prm.q + (bh * R + qi) * kD, qi < R, cq, qp0, qp1);
       sm.reset();
       fill = T.fill[cur.b];
       ng = T.ng[cur.b];
@@ -872,8 +889,11 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const Params prm) {
           // key fragments in the same permuted channel order as the quantized
           // path, built from shared memory (16-byte loads + byte permutes), so
           // the register-resident q pairs serve as B: no global loads here
-          // last visible buffer index of the thread's first query (2c; PK: c)
-          const int lim0 = fill - prm.n_q + (PK ? cq : 2 * cq);
+          // last visible buffer index of the thread's two columns: row
+          // (PK: c; else 8 cg + 2c and the next) sits at position row % n_q
+          const int row0 = PK ? cq : 8 * cg + 2 * cq;
+          const int lim0 = fill - prm.n_q + row0 % prm.n_q;
+          const int lim1 = fill - prm.n_q + (row0 + 1) % prm.n_q;
           float sv[kTailTiles][4];
           float g0 = -INFINITY, g1 = -INFINITY;
 #pragma unroll
@@ -899,7 +919,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const Params prm) {
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
               const int tok = mr + r + 8 * (k >> 1);
-              const bool vis = tok < rows && (i0 + tok) <= lim0 + (k & 1) && !(PK && (k & 1));
+              const bool vis = tok < rows && (i0 + tok) <= ((k & 1) ? lim1 : lim0) && !(PK && (k & 1));
               sv[tl][k] = vis ? acc[k] * prm.sl2 : -INFINITY;
             }
             g0 = fmaxf(g0, fmaxf(sv[tl][0], sv[tl][2]));
@@ -944,7 +964,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const Params prm) {
     // (unit i + S) unless its own wait failed
     __syncwarp();
     int last = 0;
-    if (lane == 0) last = (atomicAdd(&cnt[stage], 1) == 1);
+    if (lane == 0) last = (atomicAdd(&cnt[stage], 1) == 2 * ncg - 1);
     last = __shfl_sync(0xffffffffu, last, 0);
     if (last) {
       if (lane == 0) cnt[stage] = 0;
@@ -960,11 +980,11 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const Params prm) {
   // this warp's partials for the pieces after its last unit's piece are empty
   // (all but the range's last piece go to the workspace)
   if (cur_ord >= 0 && cur_ord < ord_last) {
-    write_partial(sm, slot(cur_ord, w), prm.n_q, lane);
+    write_partial(sm, slot(cur_ord, w), R, cg, lane);
     leave(cur_ord);
   }
   for (int o = cur_ord >= 0 ? cur_ord + 1 : ord_first; o < ord_last; ++o) {
-    write_empty(slot(o, w), prm.n_q, lane);
+    write_empty(slot(o, w), R, cg, lane);
     leave(o);
   }
 
@@ -994,17 +1014,17 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const Params prm) {
   const bool aborted = s_abort != 0;
   float *red = reinterpret_cast<float *>(smem);                 // stage memory, free now
   float *last_part = reinterpret_cast<float *>(smem + 16384);  // kWarps partials
-  if (cur_ord == ord_last) write_partial(sm, last_part + w * stride, prm.n_q, lane);
-  else write_empty(last_part + w * stride, prm.n_q, lane);
+  if (cur_ord == ord_last) write_partial(sm, last_part + w * stride, R, cg, lane);
+  else write_empty(last_part + w * stride, R, cg, lane);
   __syncthreads();
   if (s_first_fin && !aborted) {
     __threadfence();  // the other CTAs' partials are visible from here on
     const long long seg = (long long)first.b * c.H + first.h;
     const int plo = cta_of(first.s0, U, prm.P);
-    const MergeOut fo{true, prm.out + (size_t)seg * prm.n_q * kD,
-                      prm.lse ? prm.lse + (size_t)seg * prm.n_q : nullptr, nullptr};
-    merge_partials(prm.ws + (size_t)(ord_first + plo) * kWarps * stride, kWarps * stride, p - plo,
-                   slot(ord_first, 0), stride, p - plo + kWarps, prm.n_q, fo, red);
+    const MergeOut fo{true, prm.out + (size_t)seg * R * kD,
+                      prm.lse ? prm.lse + (size_t)seg * R : nullptr, nullptr};
+    merge_partials(prm.ws + (size_t)(ord_first + plo) * kWarps * stride, 0, kWarps * stride, p - plo,
+                   slot(ord_first, 0), stride, ncg * stride, p - plo + kWarps / ncg, R, fo, red);
   }
   int n_arr = 0;
   {
@@ -1015,11 +1035,11 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const Params prm) {
       const long long seg = (long long)pc.b * c.H + pc.h;
       const int S0 = pc.s0, E0 = pc.s0 + pc.len;
       const int plo = cta_of(S0, U, prm.P), phi = cta_of(E0 - 1, U, prm.P);
-      const MergeOut mo{plo == phi, prm.out + (size_t)seg * prm.n_q * kD,
-                        prm.lse ? prm.lse + (size_t)seg * prm.n_q : nullptr, slot(pc.ord, 0)};
+      const MergeOut mo{plo == phi, prm.out + (size_t)seg * R * kD,
+                        prm.lse ? prm.lse + (size_t)seg * R : nullptr, slot(pc.ord, 0)};
       if (!aborted)
-        merge_partials(pc.ord == ord_last ? last_part : slot(pc.ord, 0), stride, kWarps, nullptr, 0,
-                       kWarps, prm.n_q, mo, red);
+        merge_partials(pc.ord == ord_last ? last_part : slot(pc.ord, 0), stride, ncg * stride,
+                       kWarps / ncg, nullptr, 0, 0, kWarps / ncg, R, mo, red);
       if (plo != phi) {
         if (threadIdx.x == 0) {
           s_seg[n_arr] = (int)seg;
@@ -1050,8 +1070,8 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const Params prm) {
     const int b = (int)(seg / c.H), len = T.len[b];
     const int S0 = T.base[b] + (int)(seg % c.H) * len, E0 = S0 + len;
     const int plo = cta_of(S0, U, prm.P), phi = cta_of(E0 - 1, U, prm.P);
-    const MergeOut mo{true, prm.out + (size_t)seg * prm.n_q * kD,
-                      prm.lse ? prm.lse + (size_t)seg * prm.n_q : nullptr, nullptr};
+    const MergeOut mo{true, prm.out + (size_t)seg * R * kD,
+                      prm.lse ? prm.lse + (size_t)seg * R : nullptr, nullptr};
     // CTA pp's partial of this segment is in its warp slot 0, except that
     // CTA p_hi left its twelve warp partials when the segment was only the
     // first piece of its range
@@ -1059,8 +1079,8 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const Params prm) {
     const float *cta0 = prm.ws + ((size_t)(s_ord[a] + plo) * kWarps) * stride;
     const float *raw0 = prm.ws + ((size_t)(s_ord[a] + phi) * kWarps) * stride;
     const int nA = raw ? phi - plo : phi - plo + 1;
-    merge_partials(cta0, kWarps * stride, nA, raw0, stride, nA + (raw ? kWarps : 0), prm.n_q, mo,
-                   red);
+    merge_partials(cta0, 0, kWarps * stride, nA, raw0, stride, ncg * stride,
+                   nA + (raw ? kWarps / ncg : 0), R, mo, red);
   }
 }
 
@@ -1105,8 +1125,9 @@ qs_status grid_size(qs_mode mode, bool packed, int &P) {
   return grid_for_device<QS_VERIFY_INT8, false>(dev, P);
 }
 
-size_t ws_bytes(int P, int B, int H, int n_q) {
-  return (size_t)(P + (size_t)B * H) * kWarps * (size_t)(n_q * kD + 16) * sizeof(float);
+// Workspace: (P + B H) x 12 warp slots of R rows (R = group x n_q).
+size_t ws_bytes(int P, int B, int H, int R) {
+  return (size_t)(P + (size_t)B * H) * kWarps * (size_t)(R * kD + 2 * kMaxR) * sizeof(float);
 }
 
 template <int MODE, bool PK>
@@ -1122,25 +1143,30 @@ using namespace qs;
 
 extern "C" {
 
-qs_status qs_attn_workspace_size(const qs_cache *c, int32_t n_q, size_t *bytes) {
+qs_status qs_attn_workspace_size_gqa(const qs_cache *c, int32_t n_q, int32_t group,
+                                     size_t *bytes) {
   qs_status s = check_cache(c);
   if (s != QS_OK) return s;
-  if (!bytes || n_q < 1 || n_q > kMaxQ) return QS_ERR_ARG;
+  if (!bytes || n_q < 1 || n_q > kMaxQ || group < 1 || group * n_q > kMaxR) return QS_ERR_ARG;
   int P0 = 0, P1 = 0, P2 = 0;
   if ((s = grid_size(QS_DRAFT_UPPER4, false, P0)) != QS_OK) return s;
   if ((s = grid_size(QS_DRAFT_UPPER4, true, P1)) != QS_OK) return s;
   if ((s = grid_size(QS_VERIFY_INT8, false, P2)) != QS_OK) return s;
   const int P = P0 > P1 ? (P0 > P2 ? P0 : P2) : (P1 > P2 ? P1 : P2);
-  *bytes = ws_bytes(P, c->B, c->H, n_q);
+  *bytes = ws_bytes(P, c->B, c->H, group * n_q);
   return QS_OK;
 }
 
-qs_status qs_attn_decode(const qs_cache *c, qs_mode mode, const uint16_t *q, int32_t n_q,
-                         float softmax_scale, uint16_t *out, float *lse, void *workspace,
-                         size_t workspace_bytes, qs_stream_t stream) {
+qs_status qs_attn_workspace_size(const qs_cache *c, int32_t n_q, size_t *bytes) {
+  return qs_attn_workspace_size_gqa(c, n_q, 1, bytes);
+}
+
+qs_status qs_attn_decode_gqa(const qs_cache *c, qs_mode mode, const uint16_t *q, int32_t n_q,
+                             int32_t group, float softmax_scale, uint16_t *out, float *lse,
+                             void *workspace, size_t workspace_bytes, qs_stream_t stream) {
   qs_status s = check_cache(c);
   if (s != QS_OK) return s;
-  if (!q || !out || n_q < 1 || n_q > kMaxQ) return QS_ERR_ARG;
+  if (!q || !out || n_q < 1 || n_q > kMaxQ || group < 1 || group * n_q > kMaxR) return QS_ERR_ARG;
   if (mode != QS_DRAFT_UPPER4 && mode != QS_VERIFY_INT8) return QS_ERR_ARG;
   if (!(softmax_scale > 0.f) || !isfinite(softmax_scale)) return QS_ERR_ARG;
   if (!aligned16(q) || !aligned16(out) || (lse && !aligned16(lse))) return QS_ERR_ALIGN;
@@ -1150,16 +1176,25 @@ qs_status qs_attn_decode(const qs_cache *c, qs_mode mode, const uint16_t *q, int
   prm.out = out;
   prm.lse = lse;
   prm.n_q = n_q;
+  prm.R = group * n_q;
+  prm.ncg = (prm.R + 7) / 8;
   prm.sl2 = softmax_scale * 1.4426950408889634f;
-  const bool packed = (mode == QS_DRAFT_UPPER4 && n_q == 1);
+  const bool packed = (mode == QS_DRAFT_UPPER4 && prm.R == 1);
   if ((s = grid_size(mode, packed, prm.P)) != QS_OK) return s;
   if (!workspace || !aligned16(workspace) ||
-      workspace_bytes < ws_bytes(prm.P, c->B, c->H, n_q))
+      workspace_bytes < ws_bytes(prm.P, c->B, c->H, prm.R))
     return QS_ERR_WORKSPACE;
   prm.ws = static_cast<float *>(workspace);
   cudaStream_t st = (cudaStream_t)stream;
   if (mode == QS_VERIFY_INT8) return launch<QS_VERIFY_INT8, false>(prm, st);
   return packed ? launch<QS_DRAFT_UPPER4, true>(prm, st) : launch<QS_DRAFT_UPPER4, false>(prm, st);
+}
+
+qs_status qs_attn_decode(const qs_cache *c, qs_mode mode, const uint16_t *q, int32_t n_q,
+                         float softmax_scale, uint16_t *out, float *lse, void *workspace,
+                         size_t workspace_bytes, qs_stream_t stream) {
+  return qs_attn_decode_gqa(c, mode, q, n_q, 1, softmax_scale, out, lse, workspace,
+                            workspace_bytes, stream);
 }
 
 }  // extern "C"

@@ -60,6 +60,10 @@ _SIGS = {
     "qs_attn_decode": [ctypes.POINTER(QsCacheStruct), ctypes.c_int, _P, _I32, ctypes.c_float, _P,
                        _P, _P, ctypes.c_size_t, _P],
     "qs_get_errors": [ctypes.POINTER(QsCacheStruct), _P, _P],
+    "qs_attn_workspace_size_gqa": [ctypes.POINTER(QsCacheStruct), _I32, _I32,
+                                   ctypes.POINTER(ctypes.c_size_t)],
+    "qs_attn_decode_gqa": [ctypes.POINTER(QsCacheStruct), ctypes.c_int, _P, _I32, _I32, ctypes.c_float,
+                           _P, _P, _P, ctypes.c_size_t, _P],
     "qs_prefill": [ctypes.POINTER(QsCacheStruct), _P, _P, _I32, _P, _P],
     "qs_spec_accept": [_P, _P, _P, _P, _P, _I32, _I32, _I32, _P, _P, _P, _P],
 }
@@ -205,6 +209,23 @@ def qs_attn_decode(cache, mode, q, softmax_scale, out, lse=None, workspace=None,
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check("qs_attn_decode", lib().qs_attn_decode(
         cache._ref, int(mode), _ptr(q), n_q, float(softmax_scale), _ptr(out), _ptr(lse),
+        _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def qs_attn_workspace_size_gqa(cache, n_q, group):
+    n = ctypes.c_size_t()
+    _check("qs_attn_workspace_size_gqa", lib().qs_attn_workspace_size_gqa(
+        cache._ref, int(n_q), int(group), ctypes.byref(n)))
+    return n.value
+
+
+def qs_attn_decode_gqa(cache, mode, q, group, softmax_scale, out, lse=None, workspace=None,
+                       stream=None):
+    """q, out: fp16 [B, H*group, n_q, D]; lse: float32 [B, H*group, n_q] or None."""
+    n_q = q.shape[2]
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("qs_attn_decode_gqa", lib().qs_attn_decode_gqa(
+        cache._ref, int(mode), _ptr(q), n_q, int(group), float(softmax_scale), _ptr(out), _ptr(lse),
         _ptr(workspace), ws_bytes, _stream(stream)))
 
 

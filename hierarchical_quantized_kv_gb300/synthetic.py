@@ -41,6 +41,7 @@ class Workload:
     outlier_factor: float = 8.0
     gamma: int = 4
     seed: int = 0
+    group: int = 1               # query heads per KV head (H counts KV heads)
     extra: dict = field(default_factory=dict)
 
     @property
@@ -60,6 +61,12 @@ def tiny(seed=0):
 def llama_32k(seed=0):
     return Workload("llama2_7b_b1_h32_ctx32768", B=1, H=32, context=(32768,), fill=(256,),
                     seed=seed)
+
+
+def llama31_8b_32k(seed=0):
+    """Llama-3.1-8B attention shape: 32 query heads on 8 KV heads (group 4)."""
+    return Workload("llama31_8b_b1_kv8_q32_ctx32768", B=1, H=8, context=(32768,), fill=(256,),
+                    seed=seed, group=4)
 
 
 def ctx_128k(seed=0):
@@ -85,7 +92,7 @@ def ragged(seed=0, B=16, lo=4096, hi=65536):
 
 
 CONFIGS = {"tiny": tiny, "32k": llama_32k, "128k": ctx_128k,
-           "batched32k": batched_32k, "ragged": ragged}
+           "batched32k": batched_32k, "ragged": ragged, "gqa32k": llama31_8b_32k}
 
 
 def outlier_channels(w: Workload, b: int):
@@ -127,9 +134,9 @@ def kv_tokens(w: Workload, b: int, t0: int, n: int):
 
 
 def queries(w: Workload, call: int, n_q: int):
-    """Queries for decode call number ``call``: fp16 [B, H, n_q, D]."""
+    """Queries for decode call number ``call``: fp16 [B, H * group, n_q, D]."""
     r = _rng(w.seed, TAG_Q, call)
-    return r.standard_normal((w.B, w.H, n_q, w.D), dtype=np.float32).astype(np.float16)
+    return r.standard_normal((w.B, w.H * w.group, n_q, w.D), dtype=np.float32).astype(np.float16)
 
 
 def accepted_counts(w: Workload, step: int):

@@ -254,14 +254,31 @@ qs_status qs_attn_workspace_size(const qs_cache *c, int32_t n_q, size_t *bytes);
  *   workspace  device scratch of at least qs_attn_workspace_size bytes, 16-byte
  *          aligned; it holds split partials and is not read across calls.
  * Sequences with n_q > fill get QS_DEV_NQ_GT_FILL, zero output, lse = -inf.
- * Kernels: a persistent split kernel over a balanced partition of all
- * (sequence, head, group) units, then a log-sum-exp combine kernel.
- * Sources: "QuantSpec Guide", "Hierarchical Two-Level Quantization with
- * Bit-Sharing"; Pith review page, "What carries the argument" and Appendix E
- * (Flash Decoding). */
+ * One kernel launch: a persistent split-KV pass over a balanced partition of
+ * all (sequence, head, group) units, whose log-sum-exp merge of the splits
+ * runs in the same kernel.  Errors: QS_ERR_ARG (null q/out, n_q outside 1..8,
+ * bad mode, non-positive or non-finite scale), QS_ERR_ALIGN, QS_ERR_WORKSPACE,
+ * QS_ERR_CUDA.  Sources: "QuantSpec Guide", "Hierarchical Two-Level
+ * Quantization with Bit-Sharing"; Pith review page, "What carries the
+ * argument" and Appendix E (Flash Decoding). */
 qs_status qs_attn_decode(const qs_cache *c, qs_mode mode, const uint16_t *q, int32_t n_q,
                          float softmax_scale, uint16_t *out, float *lse, void *workspace,
                          size_t workspace_bytes, qs_stream_t stream);
+
+/* Grouped-query variant: `group` query heads share each KV head (query head
+ * h*group + i attends KV head h; group = 1 is qs_attn_decode).  q and out are
+ * fp16 [B][H*group][n_q][D], lse float [B][H*group][n_q]; group * n_q <= 24
+ * query rows per KV head.  Every KV byte is read once for all the rows of its
+ * group (the 5-query verify of a 4-way group is a 20-row tile).  Workspace:
+ * qs_attn_workspace_size_gqa.  Errors as qs_attn_decode, plus QS_ERR_ARG for
+ * group < 1 or group * n_q > 24.  Source: the pages name Llama-3.1-8B
+ * ("QuantSpec Guide", speedup table); its grouped-query head layout is taken
+ * from the model family (32 query heads on 8 KV heads), not from the pages. */
+qs_status qs_attn_workspace_size_gqa(const qs_cache *c, int32_t n_q, int32_t group,
+                                     size_t *bytes);
+qs_status qs_attn_decode_gqa(const qs_cache *c, qs_mode mode, const uint16_t *q, int32_t n_q,
+                             int32_t group, float softmax_scale, uint16_t *out, float *lse,
+                             void *workspace, size_t workspace_bytes, qs_stream_t stream);
 
 /* Size of the fixed scratch array behind qs_attn_decode_static_ws. */
 #define QS_STATIC_WS_BYTES (8u << 20)

@@ -103,6 +103,16 @@ def test_pack_unpack_roundtrip():
         assert nib == kq[a, b2, 32 * uu + layout.vperm(p), d] >> 4
 
 
+def test_gqa_host_validation(L):
+    c = _fake_cache()
+    p = ctypes.c_void_p(0x20000)
+    n = ctypes.c_size_t()
+    for n_q, g in ((1, 0), (5, 5), (8, 4), (0, 1), (9, 1)):
+        assert L.qs_attn_workspace_size_gqa(ctypes.byref(c), n_q, g, ctypes.byref(n)) == qs.QS_ERR_ARG
+        assert L.qs_attn_decode_gqa(ctypes.byref(c), 0, p, n_q, g, ctypes.c_float(0.1), p, None, p,
+                                    1 << 20, None) == qs.QS_ERR_ARG
+
+
 def test_prefill_and_spec_accept_host_validation(L):
     c = _fake_cache()
     p = ctypes.c_void_p(0x20000)

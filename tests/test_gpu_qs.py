@@ -469,3 +469,60 @@ def test_full_size_sampled(torch, cfg, bs, hs):
     both(1, VERIFY, 5)
     both(2, DRAFT, 1)
     assert np.all(qs.qs_get_errors(cache) == 0)
+
+
+# ------------------------------------------------- grouped-query attention
+
+def run_attn_gqa(torch, cache, mode, q, group):
+    B, HQ, n_q, D = q.shape
+    qd = to_dev(torch, q)
+    out = torch.full_like(qd, float("nan"))
+    lse = torch.full((B, HQ, n_q), float("nan"), dtype=torch.float32, device="cuda")
+    ws = torch.empty(qs.qs_attn_workspace_size_gqa(cache, n_q, group), dtype=torch.uint8,
+                     device="cuda")
+    qs.qs_attn_decode_gqa(cache, mode, qd, group, 1.0 / np.sqrt(D), out, lse, ws)
+    torch.cuda.synchronize()
+    return out.double().cpu().numpy(), lse.double().cpu().numpy()
+
+
+@pytest.mark.parametrize("group,n_q", [(4, 1), (8, 1), (4, 5), (2, 5), (3, 8), (1, 5), (5, 4),
+                                       (24, 1)])
+def test_gqa_attention(torch, group, n_q):
+    """Grouped-query attention (query head h*g + i on KV head h) against the
+    oracle for 1, 2 and 3 column groups of query rows (up to 24 rows per KV
+    head), ragged prompts, both modes."""
+    rng = np.random.default_rng(70 + 10 * group + n_q)
+    B, H, T, cap = 3, 2, 2200, 17
+    lens = np.array([1000, 333, 2200], np.int32)
+    k, v = h16(rng, (B, H, T, 128), 2.0), h16(rng, (B, H, T, 128))
+    cache = qs.Cache(B, H, cap)
+    qs.qs_prefill(cache, to_dev(torch, k), to_dev(torch, v), to_dev(torch, lens))
+    oc = oracle.OracleCache(B, H, 128, 128, cap)
+    oc.prefill(k, v, lens)
+    for mode in (DRAFT, VERIFY):
+        q = h16(rng, (B, H * group, n_q, 128))
+        got, gl = run_attn_gqa(torch, cache, mode, q, group)
+        ref, rl = oc.attn(q, upper_only=(mode == DRAFT), group=group)
+        assert_close(got, ref, gl, rl, "gqa g=%d n_q=%d mode %d" % (group, n_q, mode))
+    assert np.all(qs.qs_get_errors(cache) == 0)
+
+
+def test_gqa_full_size_llama31_8b(torch):
+    """Llama-3.1-8B attention shape at 32k (8 KV heads, 32 query heads): the
+    draft call (4 rows per KV head) and the 5-query verify call (20 rows, three
+    column groups), every head against the oracle."""
+    w = synthetic.llama31_8b_32k()
+    T = w.context[0]
+    k, v = synthetic.kv_tokens(w, 0, 0, T)
+    cap = w.n_groups[0] + 1
+    cache = qs.Cache(1, w.H, cap)
+    qs.qs_prefill(cache, to_dev(torch, k[None]), to_dev(torch, v[None]),
+                  to_dev(torch, np.array([T], np.int32)))
+    oc = oracle.OracleCache(1, w.H, w.D, w.G, cap)
+    oc.prefill(k[None], v[None], [T])
+    for call, (mode, n_q) in enumerate(((DRAFT, 1), (VERIFY, 5))):
+        q = synthetic.queries(w, call, n_q)
+        got, gl = run_attn_gqa(torch, cache, mode, q, w.group)
+        ref, rl = oc.attn(q, upper_only=(mode == DRAFT), group=w.group)
+        assert_close(got, ref, gl, rl, "llama31 8b mode %d" % mode)
+    assert np.all(qs.qs_get_errors(cache) == 0)
