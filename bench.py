@@ -582,6 +582,8 @@ def profile(args):
     import __graft_entry__
     __graft_entry__.build()
     from hierarchical_quantized_kv_gb300 import qs, synthetic
+    if args.profile.startswith("gqa_"):
+        return profile_gqa(args, torch, qs, synthetic)
     w = synthetic.CONFIGS[args.config]()
     r = Round(torch, w, seed=0)
     for i in range(args.warmup if args.profile == "step" else 0):
@@ -612,6 +614,29 @@ def profile(args):
     print("profile run ok: %d %s calls on %s" % (args.profile_calls, args.profile, w.name))
 
 
+def profile_gqa(args, torch, qs, synthetic):
+    """--profile gqa_draft | gqa_verify: the Llama-3.1-8B 32k shape (8 KV heads,
+    32 query heads), one prefill, then the calls."""
+    w = synthetic.llama31_8b_32k()
+    T = w.context[0]
+    k, v = synthetic.kv_tokens(w, 0, 0, T)
+    cache = qs.Cache(1, w.H, w.n_groups[0] + 1)
+    qs.qs_prefill(cache, torch.from_numpy(k[None]).cuda(), torch.from_numpy(v[None]).cuda(),
+                  torch.tensor([T], dtype=torch.int32, device="cuda"))
+    draft = args.profile == "gqa_draft"
+    n_q = 1 if draft else GAMMA + 1
+    mode = qs.QS_DRAFT_UPPER4 if draft else qs.QS_VERIFY_INT8
+    q = torch.from_numpy(synthetic.queries(w, 0, n_q)).cuda()
+    out = torch.empty_like(q)
+    ws = torch.empty(qs.qs_attn_workspace_size_gqa(cache, n_q, w.group), dtype=torch.uint8,
+                     device="cuda")
+    for _ in range(args.profile_calls):
+        qs.qs_attn_decode_gqa(cache, mode, q, w.group, 1 / np.sqrt(w.D), out, None, ws)
+    torch.cuda.synchronize()
+    assert np.all(qs.qs_get_errors(cache) == 0)
+    print("profile run ok: %d %s calls on %s" % (args.profile_calls, args.profile, w.name))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -622,7 +647,8 @@ def main():
     ap.add_argument("--call-iters", type=int, default=30)
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile", choices=["draft", "verify", "flush", "prefill", "step"])
+    ap.add_argument("--profile", choices=["draft", "verify", "flush", "prefill", "step", "gqa_draft",
+                                          "gqa_verify"])
     ap.add_argument("--profile-calls", type=int, default=3)
     args = ap.parse_args()
     if args.profile:

@@ -45,10 +45,19 @@ __device__ __forceinline__ void scale_zero(float mn, float mx, uint16_t &s_bits,
   zf = mn;
 }
 
-__device__ __forceinline__ uint32_t code_of(float x, float zf, float sf) {
+// q = clamp(rne(fl((x - z) / s)), 0, 255) with fl the IEEE fp32 quotient, as
+// QS-RN-v1 defines it, without a divide per element: rf = fl(1 / s) is exact
+// to 2^-24, so u' = fl((x - z) * rf) is within 2^-14 of fl((x - z) / s) for
+// every |u| < 256 (u <= 255 (1 + 2^-23) since s >= r / 255).  Both round to
+// the same integer unless u' lies within 2^-12 of a half-integer; there the
+// exact quotient decides (about one element in 2^11).
+__device__ __forceinline__ uint32_t code_of(float x, float zf, float sf, float rf) {
   if (sf == 0.0f) return 0;
-  const int q = __float2int_rn(__fdiv_rn(__fsub_rn(x, zf), sf));
-  return (uint32_t)min(max(q, 0), 255);
+  const float a = __fsub_rn(x, zf);
+  const float ue = __fmul_rn(a, rf);
+  float k = rintf(ue);
+  if (fabsf(__fsub_rn(ue, k)) > 0.5f - 0x1p-12f) k = rintf(__fdiv_rn(a, sf));
+  return (uint32_t)min(max((int)k, 0), 255);
 }
 
 // Token held by nibble position p of a 16-byte value row (quarter layout).
@@ -115,8 +124,9 @@ __device__ void quantize_part(FlushSmem &S, const __half *gk, const __half *gv, 
       S.vs[t] = sb;
       S.vz[t] = zb;
     }
-    const uint32_t q0 = code_of(a.x, zf, sf), q1 = code_of(a.y, zf, sf);
-    const uint32_t q2 = code_of(bb.x, zf, sf), q3 = code_of(bb.y, zf, sf);
+    const float rf = __frcp_rn(sf);
+    const uint32_t q0 = code_of(a.x, zf, sf, rf), q1 = code_of(a.y, zf, sf, rf);
+    const uint32_t q2 = code_of(bb.x, zf, sf, rf), q3 = code_of(bb.y, zf, sf, rf);
     *reinterpret_cast<uint32_t *>(&S.vc[t][4 * lane]) = q0 | (q1 << 8) | (q2 << 16) | (q3 << 24);
   }
   __syncthreads();
@@ -141,9 +151,10 @@ __device__ void quantize_part(FlushSmem &S, const __half *gk, const __half *gv, 
     const float s1 = __half2float(__ushort_as_half(S.ks[2 * j + 1]));
     const float z0 = __half2float(__ushort_as_half(S.kz[2 * j]));
     const float z1 = __half2float(__ushort_as_half(S.kz[2 * j + 1]));
+    const float r0 = __frcp_rn(s0), r1 = __frcp_rn(s1);
     for (int t = t0; t < t0 + 8; ++t) {
       const float2 x = __half22float2(*reinterpret_cast<const __half2 *>(&S.k[t][2 * j]));
-      const uint32_t q0 = code_of(x.x, z0, s0), q1 = code_of(x.y, z1, s1);
+      const uint32_t q0 = code_of(x.x, z0, s0, r0), q1 = code_of(x.y, z1, s1, r1);
       *reinterpret_cast<uint16_t *>(&S.kc[t][2 * j]) = (uint16_t)(q0 | (q1 << 8));
     }
   }
