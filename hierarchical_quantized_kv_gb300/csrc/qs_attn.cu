@@ -335,13 +335,14 @@ __device__ __forceinline__ void issue_unit(const qs_cache &c, const Tables &T, c
   if (cu.u < ng) {
     if (lane == 0) {
       const size_t grp = bh * c.cap_groups + cu.u;
+      const uint64_t pol = l2_evict_first_policy();  // planes are read once per call
       mbar_arrive_expect_tx(bar, C::kGroupBytes);
-      bulk_g2s(dst + kOffKU, c.k_upper + grp * 8192, 8192, bar);
-      bulk_g2s(dst + kOffVU, c.v_upper + grp * 8192, 8192, bar);
-      bulk_g2s(dst + kOffMeta, c.meta + grp * 512, 1024, bar);
+      bulk_g2s_hint(dst + kOffKU, c.k_upper + grp * 8192, 8192, bar, pol);
+      bulk_g2s_hint(dst + kOffVU, c.v_upper + grp * 8192, 8192, bar, pol);
+      bulk_g2s_hint(dst + kOffMeta, c.meta + grp * 512, 1024, bar, pol);
       if (MODE == QS_VERIFY_INT8) {
-        bulk_g2s(dst + kOffKL, c.k_lower + grp * 8192, 8192, bar);
-        bulk_g2s(dst + kOffVL, c.v_lower + grp * 8192, 8192, bar);
+        bulk_g2s_hint(dst + kOffKL, c.k_lower + grp * 8192, 8192, bar, pol);
+        bulk_g2s_hint(dst + kOffVL, c.v_lower + grp * 8192, 8192, bar, pol);
       }
     }
   } else {
@@ -500,10 +501,12 @@ __device__ __noinline__ void merge_partials(const float *srcA, int cgA, int kstr
       *reinterpret_cast<uint2 *>(mo.out + j * kD + 4 * lane) = h;
       if (mo.lse && lane == 0) mo.lse[j] = (M + log2f(L)) * 0.69314718055994531f;
     } else {
-      __stcg(reinterpret_cast<float4 *>(mo.dst + j * kD) + lane, A);
+      // generic stores (the readers load with ld.volatile, so no L1 line of
+      // theirs can be stale)
+      reinterpret_cast<float4 *>(mo.dst + j * kD)[lane] = A;
       if (lane == 0) {
-        __stcg(mo.dst + mo_off + j, M);
-        __stcg(mo.dst + mo_off + kMaxR + j, L);
+        mo.dst[mo_off + j] = M;
+        mo.dst[mo_off + kMaxR + j] = L;
       }
     }
   }
