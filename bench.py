@@ -208,18 +208,36 @@ class Round:
         # need_flush, flush, GAMMA x (append, draft), rollback, append, verify, rollback
         self.launches_per_step = 2 + GAMMA * 2 + 1 + 1 + 1 + 1
 
-    def step(self, s, host=None):
+    def step(self, s, host=None, ev=None):
+        """One speculative round.  ev: a list that receives (kind, start, end)
+        CUDA events recorded around each attention call (as graph nodes when
+        the step is captured)."""
         qs, c = self.qs, self.cache
+        torch = self.torch
+        if ev is not None:
+            ev.clear()
+
+        def timed(kind, fn):
+            if ev is None:
+                return fn()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            ev.append((kind, e0, e1))
+
         if host is not None:
             host.h2d(self)
         qs.qs_need_flush(c, GAMMA + 1, self.mask)
         qs.qs_quantize_flush(c, self.mask)
         for i in range(GAMMA):
             qs.qs_buffer_append(c, self.kd[i], self.vd[i])
-            qs.qs_attn_decode(c, qs.QS_DRAFT_UPPER4, self.qd[i], self.scale, self.od[i], None, self.ws)
+            timed("draft", lambda i=i: qs.qs_attn_decode(c, qs.QS_DRAFT_UPPER4, self.qd[i], self.scale,
+                                                         self.od[i], None, self.ws))
         qs.qs_buffer_rollback(c, self.drop_draft)
         qs.qs_buffer_append(c, self.kt, self.vt)
-        qs.qs_attn_decode(c, qs.QS_VERIFY_INT8, self.qv, self.scale, self.ov, self.lse, self.ws)
+        timed("verify", lambda: qs.qs_attn_decode(c, qs.QS_VERIFY_INT8, self.qv, self.scale, self.ov,
+                                                  self.lse, self.ws))
         qs.qs_buffer_rollback(c, self.drops[s % len(self.drops)])
         c.state.copy_(self.state0)
         if host is not None:
@@ -408,9 +426,28 @@ def native(args):
                          l2)
     draft_b, verify_b = r.bytes["draft"][0], r.bytes["verify"]
     draft_gbs, verify_gbs = draft_b / draft_us / 1e3, verify_b / verify_us / 1e3
+    # The roofline's launch durations: a second timed region right after the
+    # main one, the same steps launched eagerly (no graph) with CUDA events on
+    # the launch stream around each attention call; the host stays ahead of
+    # the device, so each pair of events brackets that kernel alone.
+    launch = {"draft": [], "verify": []}
+    n_ev = max(8, min(args.steps // 8, 200))
+    recs = []
+    for s in range(n_ev):
+        rec = []
+        r.step(s, ev=rec)
+        recs.append(rec)
+    torch.cuda.synchronize()
+    for rec in recs[2:]:  # the first steps warm the eager path up
+        for kind, e0, e1 in rec:
+            launch[kind].append(e0.elapsed_time(e1) * 1e3)
+    draft_launch_us = float(np.mean(launch["draft"]))
+    verify_launch_us = float(np.mean(launch["verify"]))
+    r.cache.state.copy_(r.state0)
     # dominant kernel by device time within a step
-    dominant = ("draft", draft_gbs, GAMMA * draft_us) if GAMMA * draft_us >= verify_us else \
-        ("verify", verify_gbs, verify_us)
+    dominant = ("draft", draft_b / draft_launch_us / 1e3, draft_launch_us, GAMMA * draft_launch_us) \
+        if GAMMA * draft_launch_us >= verify_launch_us else \
+        ("verify", verify_b / verify_launch_us / 1e3, verify_launch_us, verify_launch_us)
 
     # end to end through host buffers: each step copies its inputs from pinned
     # host memory, runs, copies its outputs back, and the host waits for them
@@ -452,6 +489,7 @@ def native(args):
                    "l2": "step: inputs larger than L2 (%.0f MB of planes per step); per-call numbers: "
                          "L2 evicted before each call by a 256 MB read" % (r.step_bytes / 1e6),
                    "parallelism": "replicas" if world > 1 else "single GPU"},
+        "draft_in_step_us": round(draft_launch_us, 2), "verify_in_step_us": round(verify_launch_us, 2),
         "draft_us": round(draft_us, 2), "draft_gbs": round(draft_gbs, 1),
         "verify_us": round(verify_us, 2), "verify_gbs": round(verify_gbs, 1),
         "flush_us": round(flush_us, 2),
@@ -460,6 +498,10 @@ def native(args):
         "spec_accept_us": round(spec_us, 2),
         "gqa": gqa,
         "roofline": {"bound": "hbm", "kernel": "qs_attn_decode %s (split_kernel: split-KV attention + LSE merge, one launch)" % dominant[0],
+                     "launch_us": round(dominant[2], 2),
+                     "launch_timing": "CUDA events around each call in %d eagerly launched steps "
+                                      "after the timed region (mean of %d calls)"
+                                      % (n_ev - 2, len(launch[dominant[0]])),
                      "achieved": round(dominant[1], 1), "peak": peak,
                      "peak_kind": "%s hbm_gbs (copy, burst)" % peak_kind, "unit": "GB/s",
                      "frac": round(dominant[1] / peak, 4), "traffic": stored_traffic(dominant[0])},
