@@ -191,50 +191,60 @@ struct Seg {
   }
 };
 
-// ---- nibble / byte planes -> exact fp16 integers (half2 per pair) --------
-// Pair p of a 32-bit word holds elements (p, p + 4) of its 8 nibbles.
-// Verify returns the 8-bit code minus 128, C_INT8 - 128 = 16 C_U + C_L - 128
-// (centred).  Centring keeps s * code close to k - (z + 128 s), the middle of
-// the group's range, so the fp16 rounding of p * s_V acts on values of the
-// size of the data instead of their distance to the group minimum; the 128 s
-// goes into the zero-point bias, computed in fp32.  Every subtraction is exact.
+// ---- nibble / byte planes -> exact fp16 operands (half2 per pair) --------
+// Pair p of a 32-bit word holds elements (p, p + 4) of its 8 nibbles.  A code
+// placed in the low mantissa bits of an fp16 whose exponent field is zero is
+// the subnormal code * 2^-24, exactly, so a mask (and a byte permute or one
+// shift for the other half of the word) is the whole conversion: no offset
+// and no subtraction.  The tensor core multiplies these exactly and sums in
+// fp32, where code * 2^-24 * B is a normal number; the 2^-24 comes back in
+// the fp32 score and output scales.
+//
+// Verify: the 8-bit code C_INT8 = 16 C_U + C_L, every element c * 2^-24.
 __device__ __forceinline__ void pairs_int8(uint32_t wu, uint32_t wl, uint32_t (&e)[4]) {
   const uint32_t ev = bitsel(wl, wu << 4, 0x0F0F0F0Fu);   // codes 0,2,4,6
   const uint32_t od = bitsel(wl >> 4, wu, 0x0F0F0F0Fu);   // codes 1,3,5,7
-  // byte c under 0x64: 1024 + c, minus 1152
-  e[0] = hsub2_u32(prmt(ev, 0x64646464u, 0x4240), 0x64806480u);
-  e[1] = hsub2_u32(prmt(od, 0x64646464u, 0x4240), 0x64806480u);
-  e[2] = hsub2_u32(prmt(ev, 0x64646464u, 0x4341), 0x64806480u);
-  e[3] = hsub2_u32(prmt(od, 0x64646464u, 0x4341), 0x64806480u);
+  e[0] = prmt(ev, 0u, 0x4240);  // bytes 0 and 2 over zero high bytes
+  e[1] = prmt(od, 0u, 0x4240);
+  e[2] = prmt(ev, 0u, 0x4341);
+  e[3] = prmt(od, 0u, 0x4341);
 }
 
-// Draft returns each C_U as 1024 + 16 C_U (the nibble under mantissa bits
-// 4-7 of 2^10): three shifts and four LOP3 per word, no subtraction.  The
-// constant 1152 above the centred value 16 C_U - 128 is taken out exactly:
-// for keys through the zero-point bias (B = q * s is carried to ~2^-22, and
-// the ratio 1152 / 16 of offset to code step keeps the fp32 accumulation
-// error negligible), for values by an MMA of ones against the same fp16 P'
-// the codes are multiplied with, so the result equals the centred product.
-__device__ __forceinline__ void pairs_upper_raw(uint32_t w, uint32_t (&e)[4]) {
-  e[0] = and_or(w << 4, 0x00F000F0u, 0x64006400u);
-  e[1] = and_or(w, 0x00F000F0u, 0x64006400u);
-  e[2] = and_or(w >> 4, 0x00F000F0u, 0x64006400u);
-  e[3] = and_or(w >> 8, 0x00F000F0u, 0x64006400u);
+// Draft: the nibble C_U stays where it is.  Even elements (pairs 0 and 2)
+// sit in bits 0-3 of their half (C_U * 2^-24), odd ones (pairs 1 and 3) in
+// bits 4-7 (16 C_U * 2^-24): one shift and four masks per word.  The factor
+// 16 of the odd elements is taken out of their other operand (B = q * s_K / 16
+// for keys, P' / 16 for values), so every product is C_U * 2^-24 * B.
+__device__ __forceinline__ void pairs_upper(uint32_t w, uint32_t (&e)[4]) {
+  const uint32_t t = w >> 8;
+  e[0] = w & 0x000F000Fu;
+  e[1] = w & 0x00F000F0u;
+  e[2] = t & 0x000F000Fu;
+  e[3] = t & 0x00F000F0u;
 }
-constexpr float kRawOff = 1152.f;  // pairs_upper_raw value minus the centred value
 
-// Offset, in units of the scale, that the zero-point terms carry: the
-// centring (verify 128; draft 136, the midpoint 8 included) and, for draft
-// keys read raw, minus 1152.
+// Fixed parts of the dequantized value, in units of the scale, that go into
+// the zero-point biases (fp32).  Codes enter the contractions uncentred
+// (draft 16 C_U, verify C_INT8).  Values are centred on 128 all the same: an
+// MMA of ones against the same fp16 P' the codes are multiplied with takes
+// 128 * sum_t P'_t out of the product, so the fp16 rounding of p * s_V acts
+// on s * (code - 128), of the size of the data, instead of on the distance
+// to the group minimum; the bias then carries 128 + the draft's midpoint 8.
+// Keys need no centring (q * s_K is carried hi + lo to ~2^-22): the bias
+// carries the midpoint alone.
 template <int MODE>
 struct Centre {
-  static constexpr float kOff = (MODE == QS_DRAFT_UPPER4) ? 136.f : 128.f;
-  static constexpr float kOffK = (MODE == QS_DRAFT_UPPER4) ? 136.f - kRawOff : 128.f;
+  static constexpr float kOff = (MODE == QS_DRAFT_UPPER4) ? 136.f : 128.f;  // values
+  static constexpr float kOffK = (MODE == QS_DRAFT_UPPER4) ? 8.f : 0.f;     // keys
+  static constexpr float kMid = 128.f;  // taken out of the value product
+  // true code sum / tensor-core sum: 2^24 (subnormal codes), times 16 for
+  // the draft's nibble steps
+  static constexpr float kScale = (MODE == QS_DRAFT_UPPER4) ? 268435456.f : 16777216.f;
 };
 
 template <int MODE>
 __device__ __forceinline__ void pairs(uint32_t wu, uint32_t wl, uint32_t (&e)[4]) {
-  if (MODE == QS_DRAFT_UPPER4) pairs_upper_raw(wu, e);
+  if (MODE == QS_DRAFT_UPPER4) pairs_upper(wu, e);
   else pairs_int8(wu, wl, e);
 }
 
@@ -261,7 +271,9 @@ constexpr float kExpShift = 6.f;
 // Per-warp online-softmax state for its two queries (columns 2c, 2c+1).
 struct Softmax {
   float m[2], l[2], bv[2];
-  float o[8][4];  // O^T accumulators: rows = channels 16 md + r (+8), cols = queries
+  // O^T accumulators: rows = channels 16 md + r (+8), cols = queries; in
+  // tensor-core units (true O / Centre::kScale), the value bias kept apart
+  float o[8][4];
   __device__ void reset() {
 #pragma unroll
     for (int i = 0; i < 2; ++i) { m[i] = -INFINITY; l[i] = 0.f; bv[i] = 0.f; }
@@ -514,11 +526,12 @@ __device__ __noinline__ void merge_partials(const float *srcA, int cgA, int kstr
 }
 
 // One warp's partial of a piece (unnormalized, log2 domain; m = -inf if the
-// warp saw no visible token) in the layout merge_partials reads: rows
+// warp saw no visible token; O as accumulated times oscale, plus the value
+// bias) in the layout merge_partials reads: rows
 // [8 cg, 8 cg + 8) of R, O at row * 128 + d, m at R * 128 + row, l at
 // R * 128 + 24 + row; dst is in global or shared memory.
-__device__ __forceinline__ void write_partial(const Softmax &sm, float *dst, int R, int cg,
-                                              int lane) {
+__device__ __forceinline__ void write_partial(const Softmax &sm, float oscale, float *dst, int R,
+                                              int cg, int lane) {
   const int r = lane >> 2, cq = lane & 3;
   const float l0 = warp_sum8(sm.l[0]), l1 = warp_sum8(sm.l[1]);
   const float v0 = warp_sum8(sm.bv[0]), v1 = warp_sum8(sm.bv[1]);
@@ -528,8 +541,8 @@ __device__ __forceinline__ void write_partial(const Softmax &sm, float *dst, int
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
       const int d = 16 * md + r + 8 * hh;
-      if (j0 < R) dst[j0 * kD + d] = sm.o[md][2 * hh] + v0;
-      if (j1 < R) dst[j1 * kD + d] = sm.o[md][2 * hh + 1] + v1;
+      if (j0 < R) dst[j0 * kD + d] = fmaf(sm.o[md][2 * hh], oscale, v0);
+      if (j1 < R) dst[j1 * kD + d] = fmaf(sm.o[md][2 * hh + 1], oscale, v1);
     }
   }
   if (r == 0) {
@@ -694,7 +707,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const Params prm) {
       // a new piece: the finished one's partial (empty ones for pieces this
       // warp skipped), then fresh state and this head's queries
       if (cur_ord >= 0) {
-        write_partial(sm, slot(cur_ord, w), R, cg, lane);
+        write_partial(sm, Centre<MODE>::kScale, slot(cur_ord, w), R, cg, lane);
         leave(cur_ord);
       }
       for (int o = cur_ord >= 0 ? cur_ord + 1 : ord_first; o < cur.ord; ++o) {
@@ -731,7 +744,11 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const Params prm) {
         // large score would otherwise carry the 2^-11 rounding of q * s.
         // The key bias comes from one MMA per k-block whose A rows 0-7 hold
         // the zero-points and rows 8-15 the scales.  The meta rows are stored
-        // in fragment order: one 16-byte load gives k-blocks 2i, 2i+1.
+        // in fragment order: one 16-byte load gives k-blocks 2i, 2i+1.  The
+        // second B register of a k-block (k 8-15) meets the odd code
+        // elements; for the draft those are 16 C_U, so its scales are s / 16
+        // (an exact power-of-two step; where s / 16 is subnormal the score
+        // moves by less than 2^-20 * |q|).
         uint32_t bh0[8], bh1[8], bl0[8], bl1[8];
         float bacc[4] = {0.f, 0.f, 0.f, 0.f}, bacc2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -739,22 +756,28 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const Params prm) {
           const uint4 sw = lds128(st + kOffMeta + QS_META_K_SCALE * 256 + 16 * (4 * i4 + cq));
           const uint4 zw = lds128(st + kOffMeta + QS_META_K_ZERO * 256 + 16 * (4 * i4 + cq));
           const int k0 = 2 * i4, k1 = 2 * i4 + 1;
+          uint32_t s1 = sw.y, s3 = sw.w;
+          if (MODE == QS_DRAFT_UPPER4) {
+            s1 = hmul2_u32(s1, 0x2C002C00u);  // fp16 (1/16, 1/16)
+            s3 = hmul2_u32(s3, 0x2C002C00u);
+          }
           bh0[k0] = hmul2_u32(qp0[k0], sw.x);
-          bh1[k0] = hmul2_u32(qp1[k0], sw.y);
+          bh1[k0] = hmul2_u32(qp1[k0], s1);
           bh0[k1] = hmul2_u32(qp0[k1], sw.z);
-          bh1[k1] = hmul2_u32(qp1[k1], sw.w);
+          bh1[k1] = hmul2_u32(qp1[k1], s3);
           bl0[k0] = hfma2_neg_u32(qp0[k0], sw.x, bh0[k0]);
-          bl1[k0] = hfma2_neg_u32(qp1[k0], sw.y, bh1[k0]);
+          bl1[k0] = hfma2_neg_u32(qp1[k0], s1, bh1[k0]);
           bl0[k1] = hfma2_neg_u32(qp0[k1], sw.z, bh0[k1]);
-          bl1[k1] = hfma2_neg_u32(qp1[k1], sw.w, bh1[k1]);
+          bl1[k1] = hfma2_neg_u32(qp1[k1], s3, bh1[k1]);
           if (PK && (r & 1)) {  // odd B columns carry the lo part
             bh0[k0] = bl0[k0]; bh1[k0] = bl1[k0]; bh0[k1] = bl0[k1]; bh1[k1] = bl1[k1];
           }
           mma16816(bacc, zw.x, sw.x, zw.y, sw.y, qp0[k0], qp1[k0]);
           mma16816(bacc2, zw.z, sw.z, zw.w, sw.w, qp0[k1], qp1[k1]);
         }
-        // key dequant s (code - 128) + (z + kOff s) with the code as read
-        // (draft: raw, code - 128 + 1152): bias = sum q z + kOffK sum q s
+        // key dequant s * code + (z + kOffK s), code = 16 C_U or C_INT8:
+        // bias = sum q z + kOffK sum q s; the code part scales by kScale
+        const float sl2q = prm.sl2 * Centre<MODE>::kScale;
         const float bk0 =
             fmaf(Centre<MODE>::kOffK, bacc[2] + bacc2[2], bacc[0] + bacc2[0]) * prm.sl2;
         const float bk1 =
@@ -804,12 +827,13 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const Params prm) {
           g1 = fmaxf(g1, fmaxf(s[mt][1], s[mt][3]));
         }
         float u0, u1, a0, a1;
-        sm.update(fmaf(warp_max8(g0), prm.sl2, bk0), fmaf(warp_max8(g1), prm.sl2, bk1), u0, u1, a0,
-                  a1);
+        sm.update(fmaf(warp_max8(g0), sl2q, bk0), fmaf(warp_max8(g1), sl2q, bk1), u0, u1, a0, a1);
         const float c0 = bk0 - u0, c1 = bk1 - u1;  // p = 2^(raw * sl2 + c)
 
         // probabilities with the value scale folded in, value zero-point as a
-        // bias; each value row holds a lane's four tokens of a quarter together
+        // bias; each value row holds a lane's four tokens of a quarter together.
+        // The second B register of a k-block (tokens 8-15 of a tile, hh = 1)
+        // meets the odd code elements: for the draft P' / 16 there.
         uint32_t bp0[4], bp1[4];
 #pragma unroll
         for (int qq = 0; qq < 2; ++qq) {
@@ -830,35 +854,38 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const Params prm) {
             for (int hh = 0; hh < 2; ++hh) {
               const float sv = svs[2 * ml + hh];
               const float zv = fmaf(Centre<MODE>::kOff, sv, zvs[2 * ml + hh]);
-              const float pa = fast_exp2(fmaf(s[mt][2 * hh], prm.sl2, c0));
-              const float pb = PK ? 0.f : fast_exp2(fmaf(s[mt][2 * hh + 1], prm.sl2, c1));
+              const float pa = fast_exp2(fmaf(s[mt][2 * hh], sl2q, c0));
+              const float pb = PK ? 0.f : fast_exp2(fmaf(s[mt][2 * hh + 1], sl2q, c1));
               sm.l[0] += pa;
               sm.l[1] += pb;
               sm.bv[0] = fmaf(pa, zv, sm.bv[0]);
               sm.bv[1] = fmaf(pb, zv, sm.bv[1]);
               // PK: thread column pair (2c, 2c+1) = queries (2c, 2c+1) of the
               // P' matrix; only c = 0 holds the one real query
-              pv[2 * hh] = (PK && cq != 0) ? 0.f : pa * sv;
-              pv[2 * hh + 1] = pb * sv;
+              const float svp = (MODE == QS_DRAFT_UPPER4 && hh) ? sv * 0.0625f : sv;
+              pv[2 * hh] = (PK && cq != 0) ? 0.f : pa * svp;
+              pv[2 * hh + 1] = pb * svp;
             }
             bp0[mt] = movmatrix_trans(pack_half2(pv[0], pv[1]));
             bp1[mt] = movmatrix_trans(pack_half2(pv[2], pv[3]));
           }
         }
-        if (MODE == QS_DRAFT_UPPER4) {
-          // value codes are read raw (1152 above their centred value): take
-          // 1152 * sum_t P'_t out of the value bias, the sum formed by the
-          // tensor core from the same fp16 P' it multiplies the codes with
+        {
+          // centre the value codes on 128: take 128 * sum_t P'_t out of the
+          // value bias, the sum formed by the tensor core from the same fp16
+          // P' it multiplies the codes with (A = 1, and 16 against the
+          // draft's P' / 16), so the result equals the centred product
           constexpr uint32_t kOnes = 0x3C003C00u;  // fp16 (1, 1)
+          constexpr uint32_t kHi = MODE == QS_DRAFT_UPPER4 ? 0x4C004C00u : kOnes;  // (16, 16)
           float sp[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int mt = 0; mt < 4; ++mt) mma16816(sp, kOnes, kOnes, kOnes, kOnes, bp0[mt], bp1[mt]);
+          for (int mt = 0; mt < 4; ++mt) mma16816(sp, kOnes, kOnes, kHi, kHi, bp0[mt], bp1[mt]);
           // every row of the product holds the column sum, while the value
           // bias is a per-lane partial summed over the eight row lanes later:
           // one lane per column takes it
           if (r == 0) {
-            sm.bv[0] = fmaf(-kRawOff, sp[0], sm.bv[0]);
-            sm.bv[1] = fmaf(-kRawOff, sp[1], sm.bv[1]);
+            sm.bv[0] = fmaf(-Centre<MODE>::kMid, sp[0], sm.bv[0]);
+            sm.bv[1] = fmaf(-Centre<MODE>::kMid, sp[1], sm.bv[1]);
           }
         }
         // O^T = a O^T + V^T P'  (values: quarters 2hw and 2hw+1, channel-major)
@@ -956,6 +983,9 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const Params prm) {
               ldmatrix_x4_trans(addr, f0, f1, f2, f3);
               mma16816(d, f0, f1, f2, f3, bq0[tl], bq1[tl]);
             }
+            // fp16 values: true units, the accumulators hold O / kScale
+#pragma unroll
+            for (int k = 0; k < 4; ++k) d[k] *= 1.f / Centre<MODE>::kScale;
             sm.merge(md, d, a0, a1);
           }
         }
@@ -983,7 +1013,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const Params prm) {
   // this warp's partials for the pieces after its last unit's piece are empty
   // (all but the range's last piece go to the workspace)
   if (cur_ord >= 0 && cur_ord < ord_last) {
-    write_partial(sm, slot(cur_ord, w), R, cg, lane);
+    write_partial(sm, Centre<MODE>::kScale, slot(cur_ord, w), R, cg, lane);
     leave(cur_ord);
   }
   for (int o = cur_ord >= 0 ? cur_ord + 1 : ord_first; o < ord_last; ++o) {
@@ -1017,7 +1047,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const Params prm) {
   const bool aborted = s_abort != 0;
   float *red = reinterpret_cast<float *>(smem);                 // stage memory, free now
   float *last_part = reinterpret_cast<float *>(smem + 16384);  // kWarps partials
-  if (cur_ord == ord_last) write_partial(sm, last_part + w * stride, R, cg, lane);
+  if (cur_ord == ord_last) write_partial(sm, Centre<MODE>::kScale, last_part + w * stride, R, cg, lane);
   else write_empty(last_part + w * stride, R, cg, lane);
   __syncthreads();
   if (s_first_fin && !aborted) {

@@ -189,13 +189,6 @@ __device__ __forceinline__ void ldmatrix_x4_trans(uint32_t addr, uint32_t &r0, u
                : "memory");
 }
 
-// (a & b) | c in one LOP3 (the compiler otherwise splits and/or with two
-// immediates into two instructions).
-__device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t b, uint32_t c) {
-  uint32_t d;
-  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-  return d;
-}
 // Bit select (a & m) | (b & ~m) in one LOP3.
 __device__ __forceinline__ uint32_t bitsel(uint32_t a, uint32_t b, uint32_t m) {
   uint32_t d;
@@ -212,9 +205,6 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
 __device__ __forceinline__ uint32_t h2_as_u32(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
 __device__ __forceinline__ __half2 u32_as_h2(uint32_t u) { return *reinterpret_cast<__half2 *>(&u); }
 
-__device__ __forceinline__ uint32_t hsub2_u32(uint32_t a, uint32_t b) {
-  return h2_as_u32(__hsub2(u32_as_h2(a), u32_as_h2(b)));
-}
 __device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
   return h2_as_u32(__hmul2(u32_as_h2(a), u32_as_h2(b)));
 }
