@@ -651,8 +651,11 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const Params prm) {
   const bool shared_first = ord_first != ord_last && first.s0 < x0;
   auto leave = [&](int o) {
     if (!shared_first || o != ord_first) return;
+    // This warp's partial is ordered before its count at CTA scope; the last
+    // warp's device-scope fence below is cumulative, so it publishes the
+    // partials of every warp whose count it has seen before the arrival.
     __syncwarp();
-    __threadfence();  // this warp's partial is visible before it counts
+    __threadfence_block();
     int last = 0;
     if (lane == 0) last = atomicAdd(&s_left_first, 1) == kWarps - 1;
     if (!__shfl_sync(0xffffffffu, last, 0)) return;
@@ -666,6 +669,13 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const Params prm) {
       s_first_fin = 1;
     }
   };
+
+  // the warps reach the range's last segment mid-range: start its queries
+  // towards L1 now (two 128-byte lines per row)
+  if (ord_last != ord_first && threadIdx.x < 2 * R) {
+    const size_t bh = (size_t)lastseg.b * c.H + lastseg.h;
+    prefetch_l1(prm.q + (bh * R) * kD + threadIdx.x * 64);
+  }
 
   // units i and i + S share stage i % S; warp 0 issues the first S
   if (w == 0) {
