@@ -59,6 +59,7 @@ def run_attn(torch, cache, mode, q, scale=None, lse=True):
     ws = torch.empty(qs.qs_attn_workspace_size(cache, n_q), dtype=torch.uint8, device="cuda")
     qs.qs_attn_decode(cache, mode, qd, scale, out, l_, ws)
     torch.cuda.synchronize()
+    assert int(cache.arrive.abs().sum().item()) == 0, "segment counters not back at zero"
     return out.double().cpu().numpy(), (l_.double().cpu().numpy() if lse else None)
 
 
@@ -247,6 +248,83 @@ def test_attn_ragged_small(torch):
         # sequences with fill < n_q are flagged on both sides
         assert np.array_equal(qs.qs_get_errors(cache), oc.state[:, oracle.ERR])
         oc.state[:, oracle.ERR] = 0
+
+
+@pytest.mark.parametrize("H,n_groups,fill", [(1, 100, 70), (2, 300, 129), (8, 130, 5),
+                                              (40, 30, 250)])
+def test_attn_split_spans(torch, H, n_groups, fill):
+    """Segments split over few and over many CTAs (fewer units than CTAs;
+    about 76, 19 and 4 CTAs per segment), with 1, 2 and 5 query rows: both
+    ways of finishing a split segment (from every warp's partial, or from
+    one partial per CTA), each call twice (the segment counters must be back
+    at zero for the next call)."""
+    rng = np.random.default_rng(H * 1000 + n_groups)
+    B = 1
+    oc = _oracle_state(rng, B, H, [n_groups], [fill], cap=n_groups)
+    cache = qs.Cache(B, H, n_groups)
+    layout.load_into(cache, oc)
+    for n_q in (1, 2, 5):
+        q = h16(rng, (B, H, n_q, 128))
+        for mode in (DRAFT, VERIFY):
+            ref, rl = oc.attn(q, upper_only=(mode == DRAFT))
+            for rep in range(2):
+                got, gl = run_attn(torch, cache, mode, q)
+                assert_close(got, ref, gl, rl, "n_q %d mode %d call %d" % (n_q, mode, rep))
+
+
+@pytest.mark.parametrize("B,H,n_groups,fill", [(1, 32, 40, 253), (3, 8, 60, 252)])
+def test_chained_round_no_host_sync(torch, B, H, n_groups, fill):
+    """A speculative round launched back to back on one stream, as a serving
+    loop runs it (flush mask, flush, then append + draft four times,
+    rollback, append five, verify), with no host synchronization in between:
+    kernels overlap through programmatic dependent launch, and attention
+    starts copying quantized groups before its grid dependency wait.  Every
+    output equals the oracle's for the state at its point in the round."""
+    rng = np.random.default_rng(B * 100 + H)
+    oc = _oracle_state(rng, B, H, [n_groups] * B, [fill] * B, cap=n_groups + 2)
+    cache = qs.Cache(B, H, n_groups + 2)
+    layout.load_into(cache, oc)
+    g = 4
+    kd = [h16(rng, (B, H, 1, 128), 2.0) for _ in range(g)]
+    vd = [h16(rng, (B, H, 1, 128)) for _ in range(g)]
+    qd = [h16(rng, (B, H, 1, 128)) for _ in range(g)]
+    kt, vt = h16(rng, (B, H, g + 1, 128), 2.0), h16(rng, (B, H, g + 1, 128))
+    qv = h16(rng, (B, H, g + 1, 128))
+    drop = np.full(B, g, np.int32)
+    dev = [to_dev(torch, a) for a in kd + vd + qd + [kt, vt, qv, drop]]
+    kdd, vdd, qdd = dev[:g], dev[g:2 * g], dev[2 * g:3 * g]
+    ktd, vtd, qvd, dropd = dev[3 * g:]
+    outs = [torch.full_like(q, float("nan")) for q in qdd]
+    outv = torch.full_like(qvd, float("nan"))
+    lse = torch.full((B, H, g + 1), float("nan"), dtype=torch.float32, device="cuda")
+    ws = torch.empty(qs.qs_attn_workspace_size(cache, g + 1), dtype=torch.uint8, device="cuda")
+    mask = torch.zeros(B, dtype=torch.uint8, device="cuda")
+    scale = 1.0 / np.sqrt(128)
+    torch.cuda.synchronize()
+    qs.qs_need_flush(cache, g + 1, mask)
+    qs.qs_quantize_flush(cache, mask)
+    for i in range(g):
+        qs.qs_buffer_append(cache, kdd[i], vdd[i])
+        qs.qs_attn_decode(cache, DRAFT, qdd[i], scale, outs[i], None, ws)
+    qs.qs_buffer_rollback(cache, dropd)
+    qs.qs_buffer_append(cache, ktd, vtd)
+    qs.qs_attn_decode(cache, VERIFY, qvd, scale, outv, lse, ws)
+    torch.cuda.synchronize()
+
+    m = oc.need_flush(g + 1)
+    assert m.all() and np.array_equal(mask.cpu().numpy(), m)  # fill + 5 > 256: a flush
+    oc.flush(m)
+    for i in range(g):
+        oc.append(kd[i], vd[i])
+        ref, _ = oc.attn(qd[i], upper_only=True)
+        assert_close(outs[i].double().cpu().numpy(), ref, what="draft %d" % i)
+    oc.rollback(drop)
+    oc.append(kt, vt)
+    ref, rl = oc.attn(qv, upper_only=False)
+    assert_close(outv.double().cpu().numpy(), ref, lse.double().cpu().numpy(), rl, "verify")
+    assert np.array_equal(cache.state.cpu().numpy()[:, :4], oc.state[:, :4])
+    assert int(cache.arrive.abs().sum().item()) == 0
+    assert np.all(qs.qs_get_errors(cache) == 0)
 
 
 @pytest.mark.parametrize("mode", [DRAFT, VERIFY])
@@ -482,6 +560,7 @@ def run_attn_gqa(torch, cache, mode, q, group):
                      device="cuda")
     qs.qs_attn_decode_gqa(cache, mode, qd, group, 1.0 / np.sqrt(D), out, lse, ws)
     torch.cuda.synchronize()
+    assert int(cache.arrive.abs().sum().item()) == 0, "segment counters not back at zero"
     return out.double().cpu().numpy(), lse.double().cpu().numpy()
 
 
