@@ -76,13 +76,14 @@ def load_peaks():
 
 # ---------------------------------------------------------------- bytes
 
-def attn_bytes(ng, fill, n_q, mode_draft, BH, group=1):
+def attn_bytes(ng, fill, n_q, mode_draft, BH, group=1, upper_bits=4):
     """Algorithmic bytes of one decode-attention call per the method: the
     quantized planes it must read (draft: C_U + scales/zeros = 136 B per
-    token-head; verify: C_U + C_L + scales/zeros = 264 B), the fp16 buffer
-    tokens (512 B each), the queries and the outputs (group query heads per
-    KV head)."""
-    grp = (8 * KB + 8 * KB + KB) if mode_draft else (4 * 8 * KB + KB)
+    token-head, or with the two-bit draft C_U2 + scales/zeros = 72 B;
+    verify: all 8 bits + scales/zeros = 264 B), the fp16 buffer tokens (512 B
+    each), the queries and the outputs (group query heads per KV head)."""
+    up = 8 * KB * upper_bits // 4
+    grp = (up + up + KB) if mode_draft else (4 * 8 * KB + KB)
     return BH * (ng * grp + fill * 512 + group * n_q * 256 * 2)
 
 
@@ -168,12 +169,12 @@ class ClockSampler:
 class Round:
     """Device state and inputs of the benchmark step on one GPU."""
 
-    def __init__(self, torch, w, seed):
+    def __init__(self, torch, w, seed, upper_bits=4):
         from hierarchical_quantized_kv_gb300 import driver, qs, synthetic
         self.torch, self.qs, self.w = torch, qs, w
         dev = torch.device("cuda")
         B, H, D = w.B, w.H, w.D
-        self.cache = qs.Cache(B, H, max(w.n_groups) + 2)
+        self.cache = qs.Cache(B, H, max(w.n_groups) + 2, upper_bits=upper_bits)
         driver.prefill(self.cache, w)
         torch.cuda.synchronize()
         self.state0 = self.cache.state.clone()
@@ -302,6 +303,25 @@ def time_calls(torch, fn, setup, iters, l2_scratch):
     return statistics.mean(ts[1:]) if len(ts) > 1 else ts[0]
 
 
+def two_bit_calls(torch, qs, synthetic, w, l2, it):
+    """The two-bit draft layout (upper_bits 2: the draft reads the top two
+    bits of each code) on the benchmark workload: per-call draft and 5-query
+    verify times and GB/s, L2 evicted before each call."""
+    r = Round(torch, w, seed=1, upper_bits=2)
+    res = {"workload": w.name, "upper_bits": 2}
+    for name, mode, q, out, lse, n_q, fill in (
+            ("draft", qs.QS_DRAFT_UPPER4, r.qd[0], r.od[0], None, 1, r.f1 + 1),
+            ("verify", qs.QS_VERIFY_INT8, r.qv, r.ov, r.lse, GAMMA + 1, r.f1 + GAMMA + 1)):
+        us = time_calls(torch, lambda: qs.qs_attn_decode(r.cache, mode, q, r.scale, out, lse, r.ws),
+                        lambda: r.set_state(r.ng1, fill), it, l2)
+        nb = attn_bytes(r.ng1, fill, n_q, mode == qs.QS_DRAFT_UPPER4, w.B * w.H, 1, 2)
+        res[name + "_us"] = round(us, 2)
+        res[name + "_gbs"] = round(nb / us / 1e3, 1)
+    assert np.all(qs.qs_get_errors(r.cache) == 0)
+    del r
+    return res
+
+
 def gqa_calls(torch, qs, synthetic, l2, it):
     """Grouped-query decode attention on the Llama-3.1-8B shape (8 KV heads,
     32 query heads, 32k context): per-call draft (4 rows per KV head) and
@@ -412,6 +432,8 @@ def native(args):
         prefill_gbs = prefill_bytes(T, w.H) / prefill_us / 1e3
         del kp, vp, pc
     gqa = gqa_calls(torch, qs, synthetic, l2, it) if w.name == synthetic.llama_32k().name else None
+    two_bit = (two_bit_calls(torch, qs, synthetic, w, l2, it)
+               if w.name == synthetic.llama_32k().name else None)
     # speculative acceptance for the round (synthetic probabilities over a
     # 32,000-token vocabulary): accept/reject, the emitted token, n_drop
     V = 32000
@@ -497,6 +519,7 @@ def native(args):
         "prefill_gbs": None if prefill_gbs is None else round(prefill_gbs, 1),
         "spec_accept_us": round(spec_us, 2),
         "gqa": gqa,
+        "two_bit_draft": two_bit,
         "roofline": {"bound": "hbm", "kernel": "qs_attn_decode %s (split_kernel: split-KV attention + LSE merge, one launch)" % dominant[0],
                      "launch_us": round(dominant[2], 2),
                      "launch_timing": "CUDA events around each call in %d eagerly launched steps "

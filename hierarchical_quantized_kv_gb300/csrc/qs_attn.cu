@@ -232,14 +232,17 @@ __device__ __forceinline__ void pairs_upper(uint32_t w, uint32_t (&e)[4]) {
 // to the group minimum; the bias then carries 128 + the draft's midpoint 8.
 // Keys need no centring (q * s_K is carried hi + lo to ~2^-22): the bias
 // carries the midpoint alone.
-template <int MODE>
+// UB: the top bits the draft reads (4: 16 C_U + 8; 2: 64 C_U2 + 32).
+template <int MODE, int UB = 4>
 struct Centre {
-  static constexpr float kOff = (MODE == QS_DRAFT_UPPER4) ? 136.f : 128.f;  // values
-  static constexpr float kOffK = (MODE == QS_DRAFT_UPPER4) ? 8.f : 0.f;     // keys
+  static constexpr bool kDraft = MODE == QS_DRAFT_UPPER4;
+  static constexpr float kStep = UB == 2 ? 64.f : 16.f;  // draft code step
+  static constexpr float kOff = kDraft ? 128.f + kStep / 2 : 128.f;  // values
+  static constexpr float kOffK = kDraft ? kStep / 2 : 0.f;           // keys
   static constexpr float kMid = 128.f;  // taken out of the value product
-  // true code sum / tensor-core sum: 2^24 (subnormal codes), times 16 for
-  // the draft's nibble steps
-  static constexpr float kScale = (MODE == QS_DRAFT_UPPER4) ? 268435456.f : 16777216.f;
+  // true code sum / tensor-core sum: 2^24 (subnormal codes), times the
+  // draft's code step
+  static constexpr float kScale = 16777216.f * (kDraft ? kStep : 1.f);
 };
 
 template <int MODE>
@@ -248,9 +251,40 @@ __device__ __forceinline__ void pairs(uint32_t wu, uint32_t wl, uint32_t (&e)[4]
   else pairs_int8(wu, wl, e);
 }
 
+// Two-bit draft layout (see include/qs.h): word k of the C_U2 plane holds
+// the top two bits of nibble j of 4-bit words 2k (bits 4j..4j+1) and 2k+1
+// (bits 4j+2..4j+3).  The draft converts them as pairs_upper converts
+// nibbles, with C_U2 in place of C_U (field sh = 0 for word 2k, 2 for 2k+1):
+// even elements C_U2 * 2^-24, odd ones 16 C_U2 * 2^-24.
+template <int SH>
+__device__ __forceinline__ void pairs_upper2(uint32_t x, uint32_t (&e)[4]) {
+  const uint32_t w = x >> SH, t = x >> (SH + 8);
+  e[0] = w & 0x00030003u;
+  e[1] = w & 0x00300030u;
+  e[2] = t & 0x00030003u;
+  e[3] = t & 0x00300030u;
+}
+__device__ __forceinline__ void pairs_upper2_rt(uint32_t x, int sh, uint32_t (&e)[4]) {
+  const uint32_t w = x >> sh, t = w >> 8;
+  e[0] = w & 0x00030003u;
+  e[1] = w & 0x00300030u;
+  e[2] = t & 0x00030003u;
+  e[3] = t & 0x00300030u;
+}
+// Verify: the 4-bit word 2k + sh/2 rebuilt from C_U2 word u and M2 word m
+// (C_U = 4 C_U2 + M2).
+__device__ __forceinline__ uint32_t upper_from2(uint32_t u, uint32_t m, int sh) {
+  return ((u << (2 - sh)) & 0xCCCCCCCCu) | ((m >> sh) & 0x33333333u);
+}
+
 __device__ __forceinline__ uint32_t lds32(uint32_t a) {
   uint32_t v;
   asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint2 lds64(uint32_t a) {
+  uint2 v;
+  asm volatile("ld.shared.v2.b32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
   return v;
 }
 __device__ __forceinline__ uint4 lds128(uint32_t a) {
@@ -337,7 +371,10 @@ __device__ __forceinline__ void load_q_pairs(const uint16_t *qrow, bool valid, i
 // ------------------------------------------------------------ split kernel
 
 // Issue the bulk copies of one unit into a stage (called by one whole warp).
-template <int MODE>
+// A two-bit draft copies only the C_U2 half (4 KB) of each upper plane into
+// the stage's upper slots; verify copies both halves (the slots' layout is
+// then C_U2 | M2 instead of C_U).
+template <int MODE, int UB>
 __device__ __forceinline__ void issue_unit(const qs_cache &c, const Tables &T, const Seg &cu,
                                            uint32_t dst, uint32_t bar, int lane) {
   using C = Cfg<MODE>;
@@ -348,9 +385,10 @@ __device__ __forceinline__ void issue_unit(const qs_cache &c, const Tables &T, c
     if (lane == 0) {
       const size_t grp = bh * c.cap_groups + cu.u;
       const uint64_t pol = l2_evict_first_policy();  // planes are read once per call
-      mbar_arrive_expect_tx(bar, C::kGroupBytes);
-      bulk_g2s_hint(dst + kOffKU, c.k_upper + grp * 8192, 8192, bar, pol);
-      bulk_g2s_hint(dst + kOffVU, c.v_upper + grp * 8192, 8192, bar, pol);
+      constexpr int kUp = (MODE == QS_DRAFT_UPPER4 && UB == 2) ? 4096 : 8192;
+      mbar_arrive_expect_tx(bar, C::kGroupBytes - 2 * (8192 - kUp));
+      bulk_g2s_hint(dst + kOffKU, c.k_upper + grp * 8192, kUp, bar, pol);
+      bulk_g2s_hint(dst + kOffVU, c.v_upper + grp * 8192, kUp, bar, pol);
       bulk_g2s_hint(dst + kOffMeta, c.meta + grp * 512, 1024, bar, pol);
       if (MODE == QS_VERIFY_INT8) {
         bulk_g2s_hint(dst + kOffKL, c.k_lower + grp * 8192, 8192, bar, pol);
@@ -576,7 +614,7 @@ __device__ __forceinline__ bool wait_issued(volatile int *issued, int i) {
 // so column 2j carries the hi part of B = q * s and column 2j + 1 the lo part
 // for query j = lane / 8 (thread column pair 2c, 2c + 1 = query c): one MMA
 // per k-block instead of two.
-template <int MODE, bool PK>
+template <int MODE, bool PK, int UB>
 __global__ void __launch_bounds__(kThreads, 1) split_kernel(const Params prm) {
   using C = Cfg<MODE>;
   using L = Layout<MODE>;
@@ -683,7 +721,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const Params prm) {
     for (int k = 0; k < S && k < n; ++k) {
       a.seek(x0 + k, T, c.B);
       if (lane == 0) issued[k] = k;
-      issue_unit<MODE>(c, T, a, sbase + k * L::kStageBytes, full0 + 8 * k, lane);
+      issue_unit<MODE, UB>(c, T, a, sbase + k * L::kStageBytes, full0 + 8 * k, lane);
     }
   }
 
@@ -717,7 +755,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const Params prm) {
       // a new piece: the finished one's partial (empty ones for pieces this
       // warp skipped), then fresh state and this head's queries
       if (cur_ord >= 0) {
-        write_partial(sm, Centre<MODE>::kScale, slot(cur_ord, w), R, cg, lane);
+        write_partial(sm, Centre<MODE, UB>::kScale, slot(cur_ord, w), R, cg, lane);
         leave(cur_ord);
       }
       for (int o = cur_ord >= 0 ? cur_ord + 1 : ord_first; o < cur.ord; ++o) {
@@ -787,32 +825,62 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const Params prm) {
         }
         // key dequant s * code + (z + kOffK s), code = 16 C_U or C_INT8:
         // bias = sum q z + kOffK sum q s; the code part scales by kScale
-        const float sl2q = prm.sl2 * Centre<MODE>::kScale;
+        const float sl2q = prm.sl2 * Centre<MODE, UB>::kScale;
         const float bk0 =
-            fmaf(Centre<MODE>::kOffK, bacc[2] + bacc2[2], bacc[0] + bacc2[0]) * prm.sl2;
+            fmaf(Centre<MODE, UB>::kOffK, bacc[2] + bacc2[2], bacc[0] + bacc2[0]) * prm.sl2;
         const float bk1 =
-            fmaf(Centre<MODE>::kOffK, bacc[3] + bacc2[3], bacc[1] + bacc2[1]) * prm.sl2;
+            fmaf(Centre<MODE, UB>::kOffK, bacc[3] + bacc2[3], bacc[1] + bacc2[1]) * prm.sl2;
 
         // raw scores (q.k before scale and bias): four m-tiles of 16 tokens
         float s[4][4];
 #pragma unroll
         for (int mt = 0; mt < 4; ++mt) {
           const int t0 = 64 * hw + 16 * mt + r;
-          const uint4 u0 = lds128(st + kOffKU + t0 * 64 + 16 * cq);
-          const uint4 u1 = lds128(st + kOffKU + (t0 + 8) * 64 + 16 * cq);
+          // the lane's four 4-bit words of rows t0 and t0 + 8 (two-bit
+          // layout: two C_U2 words each, plus two M2 words for verify)
+          uint32_t wu0[4], wu1[4];
+          if (UB == 4) {
+            const uint4 u0 = lds128(st + kOffKU + t0 * 64 + 16 * cq);
+            const uint4 u1 = lds128(st + kOffKU + (t0 + 8) * 64 + 16 * cq);
+            wu0[0] = u0.x; wu0[1] = u0.y; wu0[2] = u0.z; wu0[3] = u0.w;
+            wu1[0] = u1.x; wu1[1] = u1.y; wu1[2] = u1.z; wu1[3] = u1.w;
+          } else {
+            const uint2 a0 = lds64(st + kOffKU + t0 * 32 + 8 * cq);
+            const uint2 a1 = lds64(st + kOffKU + (t0 + 8) * 32 + 8 * cq);
+            if (MODE == QS_VERIFY_INT8) {
+              const uint2 m0 = lds64(st + kOffKU + 4096 + t0 * 32 + 8 * cq);
+              const uint2 m1 = lds64(st + kOffKU + 4096 + (t0 + 8) * 32 + 8 * cq);
+              wu0[0] = upper_from2(a0.x, m0.x, 0); wu0[1] = upper_from2(a0.x, m0.x, 2);
+              wu0[2] = upper_from2(a0.y, m0.y, 0); wu0[3] = upper_from2(a0.y, m0.y, 2);
+              wu1[0] = upper_from2(a1.x, m1.x, 0); wu1[1] = upper_from2(a1.x, m1.x, 2);
+              wu1[2] = upper_from2(a1.y, m1.y, 0); wu1[3] = upper_from2(a1.y, m1.y, 2);
+            } else {  // draft: converted straight from the C_U2 words below
+              wu0[0] = wu0[1] = a0.x; wu0[2] = wu0[3] = a0.y;
+              wu1[0] = wu1[1] = a1.x; wu1[2] = wu1[3] = a1.y;
+            }
+          }
           uint4 l0 = make_uint4(0, 0, 0, 0), l1 = l0;
           if (MODE == QS_VERIFY_INT8) {
             l0 = lds128(st + kOffKL + t0 * 64 + 16 * cq);
             l1 = lds128(st + kOffKL + (t0 + 8) * 64 + 16 * cq);
           }
           float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};
-          const uint32_t wu0[4] = {u0.x, u0.y, u0.z, u0.w}, wu1[4] = {u1.x, u1.y, u1.z, u1.w};
           const uint32_t wl0[4] = {l0.x, l0.y, l0.z, l0.w}, wl1[4] = {l1.x, l1.y, l1.z, l1.w};
 #pragma unroll
           for (int j = 0; j < 4; ++j) {  // two independent MMA chains: even / odd k-blocks
             uint32_t a[4], b8[4];
-            pairs<MODE>(wu0[j], wl0[j], a);
-            pairs<MODE>(wu1[j], wl1[j], b8);
+            if (MODE == QS_DRAFT_UPPER4 && UB == 2) {
+              if (j & 1) {
+                pairs_upper2<2>(wu0[j], a);
+                pairs_upper2<2>(wu1[j], b8);
+              } else {
+                pairs_upper2<0>(wu0[j], a);
+                pairs_upper2<0>(wu1[j], b8);
+              }
+            } else {
+              pairs<MODE>(wu0[j], wl0[j], a);
+              pairs<MODE>(wu1[j], wl1[j], b8);
+            }
             mma16816(acc, a[0], b8[0], a[1], b8[1], bh0[2 * j], bh1[2 * j]);
             mma16816(acc2, a[2], b8[2], a[3], b8[3], bh0[2 * j + 1], bh1[2 * j + 1]);
             if (!PK) {
@@ -863,7 +931,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const Params prm) {
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
               const float sv = svs[2 * ml + hh];
-              const float zv = fmaf(Centre<MODE>::kOff, sv, zvs[2 * ml + hh]);
+              const float zv = fmaf(Centre<MODE, UB>::kOff, sv, zvs[2 * ml + hh]);
               const float pa = fast_exp2(fmaf(s[mt][2 * hh], sl2q, c0));
               const float pb = PK ? 0.f : fast_exp2(fmaf(s[mt][2 * hh + 1], sl2q, c1));
               sm.l[0] += pa;
@@ -894,8 +962,8 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const Params prm) {
           // bias is a per-lane partial summed over the eight row lanes later:
           // one lane per column takes it
           if (r == 0) {
-            sm.bv[0] = fmaf(-Centre<MODE>::kMid, sp[0], sm.bv[0]);
-            sm.bv[1] = fmaf(-Centre<MODE>::kMid, sp[1], sm.bv[1]);
+            sm.bv[0] = fmaf(-Centre<MODE, UB>::kMid, sp[0], sm.bv[0]);
+            sm.bv[1] = fmaf(-Centre<MODE, UB>::kMid, sp[1], sm.bv[1]);
           }
         }
         // O^T = a O^T + V^T P'  (values: quarters 2hw and 2hw+1, channel-major)
@@ -904,16 +972,35 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const Params prm) {
           float d[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
           for (int qq = 0; qq < 2; ++qq) {
-            const uint32_t ra = st + kOffVU + ((2 * hw + qq) * 128 + 16 * md + r) * 16 + 4 * cq;
-            const uint32_t vu0 = lds32(ra), vu1 = lds32(ra + 8 * 16);
-            uint32_t vl0 = 0, vl1 = 0;
+            const int vrow = (2 * hw + qq) * 128 + 16 * md + r;  // (quarter, channel) row
+            uint32_t vu0, vu1, vl0 = 0, vl1 = 0;
+            const int sh = 2 * (cq & 1);  // two-bit layout: the lane's half of a C_U2 word
+            const uint32_t ra2 = st + kOffVU + vrow * 8 + 4 * (cq >> 1);
+            if (UB == 4) {
+              const uint32_t ra = st + kOffVU + vrow * 16 + 4 * cq;
+              vu0 = lds32(ra);
+              vu1 = lds32(ra + 8 * 16);
+            } else {
+              vu0 = lds32(ra2);
+              vu1 = lds32(ra2 + 8 * 8);
+              if (MODE == QS_VERIFY_INT8) {
+                vu0 = upper_from2(vu0, lds32(ra2 + 4096), sh);
+                vu1 = upper_from2(vu1, lds32(ra2 + 4096 + 8 * 8), sh);
+              }
+            }
             if (MODE == QS_VERIFY_INT8) {
-              vl0 = lds32(ra - kOffVU + kOffVL);
-              vl1 = lds32(ra - kOffVU + kOffVL + 8 * 16);
+              const uint32_t rl = st + kOffVL + vrow * 16 + 4 * cq;
+              vl0 = lds32(rl);
+              vl1 = lds32(rl + 8 * 16);
             }
             uint32_t a[4], b8[4];
-            pairs<MODE>(vu0, vl0, a);
-            pairs<MODE>(vu1, vl1, b8);
+            if (MODE == QS_DRAFT_UPPER4 && UB == 2) {
+              pairs_upper2_rt(vu0, sh, a);
+              pairs_upper2_rt(vu1, sh, b8);
+            } else {
+              pairs<MODE>(vu0, vl0, a);
+              pairs<MODE>(vu1, vl1, b8);
+            }
             mma16816(d, a[0], b8[0], a[1], b8[1], bp0[2 * qq], bp1[2 * qq]);
             mma16816(d, a[2], b8[2], a[3], b8[3], bp0[2 * qq + 1], bp1[2 * qq + 1]);
           }
@@ -995,7 +1082,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const Params prm) {
             }
             // fp16 values: true units, the accumulators hold O / kScale
 #pragma unroll
-            for (int k = 0; k < 4; ++k) d[k] *= 1.f / Centre<MODE>::kScale;
+            for (int k = 0; k < 4; ++k) d[k] *= 1.f / Centre<MODE, UB>::kScale;
             sm.merge(md, d, a0, a1);
           }
         }
@@ -1016,14 +1103,14 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const Params prm) {
         fence_proxy_async_smem();
         if (lane == 0) issued[stage] = i + S;
         __syncwarp();
-        issue_unit<MODE>(c, T, ahead, sbase + stage * L::kStageBytes, full0 + 8 * stage, lane);
+        issue_unit<MODE, UB>(c, T, ahead, sbase + stage * L::kStageBytes, full0 + 8 * stage, lane);
       }
     }
   }
   // this warp's partials for the pieces after its last unit's piece are empty
   // (all but the range's last piece go to the workspace)
   if (cur_ord >= 0 && cur_ord < ord_last) {
-    write_partial(sm, Centre<MODE>::kScale, slot(cur_ord, w), R, cg, lane);
+    write_partial(sm, Centre<MODE, UB>::kScale, slot(cur_ord, w), R, cg, lane);
     leave(cur_ord);
   }
   for (int o = cur_ord >= 0 ? cur_ord + 1 : ord_first; o < ord_last; ++o) {
@@ -1057,7 +1144,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const Params prm) {
   const bool aborted = s_abort != 0;
   float *red = reinterpret_cast<float *>(smem);                 // stage memory, free now
   float *last_part = reinterpret_cast<float *>(smem + 16384);  // kWarps partials
-  if (cur_ord == ord_last) write_partial(sm, Centre<MODE>::kScale, last_part + w * stride, R, cg, lane);
+  if (cur_ord == ord_last) write_partial(sm, Centre<MODE, UB>::kScale, last_part + w * stride, R, cg, lane);
   else write_empty(last_part + w * stride, R, cg, lane);
   __syncthreads();
   if (s_first_fin && !aborted) {
@@ -1129,25 +1216,25 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const Params prm) {
 
 // --------------------------------------------------------------- host side
 struct DevInfo {
-  int ready[4];
-  int grid[4];
+  int ready[8];
+  int grid[8];
 };
 DevInfo g_dev[64];
 
 // Resident CTAs of one split-kernel variant on a device (set up once).
-template <int MODE, bool PK>
+template <int MODE, bool PK, int UB>
 qs_status grid_for_device(int dev, int &P) {
   DevInfo &di = g_dev[dev];
-  constexpr int v = 2 * MODE + (PK ? 1 : 0);
+  constexpr int v = 2 * MODE + (PK ? 1 : 0) + (UB == 2 ? 4 : 0);
   if (!__atomic_load_n(&di.ready[v], __ATOMIC_ACQUIRE)) {
     const int smem = Layout<MODE>::kSmemBytes;
-    if (cudaFuncSetAttribute(split_kernel<MODE, PK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(split_kernel<MODE, PK, UB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              smem) != cudaSuccess)
       return QS_ERR_CUDA;
     int sms = 0, occ = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       return QS_ERR_CUDA;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, split_kernel<MODE, PK>, kThreads,
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, split_kernel<MODE, PK, UB>, kThreads,
                                                       smem) != cudaSuccess)
       return QS_ERR_CUDA;
     if (occ < 1) return QS_ERR_CUDA;
@@ -1158,14 +1245,20 @@ qs_status grid_for_device(int dev, int &P) {
   return QS_OK;
 }
 
-qs_status grid_size(qs_mode mode, bool packed, int &P) {
+template <int UB>
+qs_status grid_size_ub(int dev, qs_mode mode, bool packed, int &P) {
+  if (mode == QS_DRAFT_UPPER4)
+    return packed ? grid_for_device<QS_DRAFT_UPPER4, true, UB>(dev, P)
+                  : grid_for_device<QS_DRAFT_UPPER4, false, UB>(dev, P);
+  return grid_for_device<QS_VERIFY_INT8, false, UB>(dev, P);
+}
+
+qs_status grid_size(qs_mode mode, bool packed, int upper_bits, int &P) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return QS_ERR_CUDA;
   if (dev < 0 || dev >= 64) return QS_ERR_UNSUPPORTED;
-  if (mode == QS_DRAFT_UPPER4)
-    return packed ? grid_for_device<QS_DRAFT_UPPER4, true>(dev, P)
-                  : grid_for_device<QS_DRAFT_UPPER4, false>(dev, P);
-  return grid_for_device<QS_VERIFY_INT8, false>(dev, P);
+  return upper_bits == 2 ? grid_size_ub<2>(dev, mode, packed, P)
+                         : grid_size_ub<4>(dev, mode, packed, P);
 }
 
 // Workspace: (P + B H) x 12 warp slots of R rows (R = group x n_q).
@@ -1173,10 +1266,17 @@ size_t ws_bytes(int P, int B, int H, int R) {
   return (size_t)(P + (size_t)B * H) * kWarps * (size_t)(R * kD + 2 * kMaxR) * sizeof(float);
 }
 
-template <int MODE, bool PK>
+template <int MODE, bool PK, int UB>
 qs_status launch(const Params &prm, cudaStream_t s) {
-  return launch_pdl(split_kernel<MODE, PK>, dim3(prm.P), dim3(kThreads), Layout<MODE>::kSmemBytes, s,
-                    prm);
+  return launch_pdl(split_kernel<MODE, PK, UB>, dim3(prm.P), dim3(kThreads),
+                    Layout<MODE>::kSmemBytes, s, prm);
+}
+
+template <int UB>
+qs_status launch_ub(qs_mode mode, bool packed, const Params &prm, cudaStream_t st) {
+  if (mode == QS_VERIFY_INT8) return launch<QS_VERIFY_INT8, false, UB>(prm, st);
+  return packed ? launch<QS_DRAFT_UPPER4, true, UB>(prm, st)
+                : launch<QS_DRAFT_UPPER4, false, UB>(prm, st);
 }
 
 }  // namespace
@@ -1192,9 +1292,9 @@ qs_status qs_attn_workspace_size_gqa(const qs_cache *c, int32_t n_q, int32_t gro
   if (s != QS_OK) return s;
   if (!bytes || n_q < 1 || n_q > kMaxQ || group < 1 || group * n_q > kMaxR) return QS_ERR_ARG;
   int P0 = 0, P1 = 0, P2 = 0;
-  if ((s = grid_size(QS_DRAFT_UPPER4, false, P0)) != QS_OK) return s;
-  if ((s = grid_size(QS_DRAFT_UPPER4, true, P1)) != QS_OK) return s;
-  if ((s = grid_size(QS_VERIFY_INT8, false, P2)) != QS_OK) return s;
+  if ((s = grid_size(QS_DRAFT_UPPER4, false, c->upper_bits, P0)) != QS_OK) return s;
+  if ((s = grid_size(QS_DRAFT_UPPER4, true, c->upper_bits, P1)) != QS_OK) return s;
+  if ((s = grid_size(QS_VERIFY_INT8, false, c->upper_bits, P2)) != QS_OK) return s;
   const int P = P0 > P1 ? (P0 > P2 ? P0 : P2) : (P1 > P2 ? P1 : P2);
   *bytes = ws_bytes(P, c->B, c->H, group * n_q);
   return QS_OK;
@@ -1223,14 +1323,14 @@ qs_status qs_attn_decode_gqa(const qs_cache *c, qs_mode mode, const uint16_t *q,
   prm.ncg = (prm.R + 7) / 8;
   prm.sl2 = softmax_scale * 1.4426950408889634f;
   const bool packed = (mode == QS_DRAFT_UPPER4 && prm.R == 1);
-  if ((s = grid_size(mode, packed, prm.P)) != QS_OK) return s;
+  if ((s = grid_size(mode, packed, c->upper_bits, prm.P)) != QS_OK) return s;
   if (!workspace || !aligned16(workspace) ||
       workspace_bytes < ws_bytes(prm.P, c->B, c->H, prm.R))
     return QS_ERR_WORKSPACE;
   prm.ws = static_cast<float *>(workspace);
   cudaStream_t st = (cudaStream_t)stream;
-  if (mode == QS_VERIFY_INT8) return launch<QS_VERIFY_INT8, false>(prm, st);
-  return packed ? launch<QS_DRAFT_UPPER4, true>(prm, st) : launch<QS_DRAFT_UPPER4, false>(prm, st);
+  return c->upper_bits == 2 ? launch_ub<2>(mode, packed, prm, st)
+                            : launch_ub<4>(mode, packed, prm, st);
 }
 
 qs_status qs_attn_decode(const qs_cache *c, qs_mode mode, const uint16_t *q, int32_t n_q,

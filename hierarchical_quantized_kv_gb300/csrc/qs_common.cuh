@@ -28,6 +28,7 @@ inline qs_status check_cache(const qs_cache *c) {
   if (c->B <= 0 || c->H <= 0 || c->cap_groups <= 0) return QS_ERR_SHAPE;
   if (c->D != kD || c->G != kG) return QS_ERR_UNSUPPORTED;
   if (c->B > kMaxB) return QS_ERR_UNSUPPORTED;
+  if (c->upper_bits != 4 && c->upper_bits != 2) return QS_ERR_ARG;
   if (!c->k_upper || !c->k_lower || !c->v_upper || !c->v_lower || !c->meta) return QS_ERR_ARG;
   const void *ps[] = {c->k_upper, c->k_lower, c->v_upper, c->v_lower,
                       c->meta,    c->buf_k,   c->buf_v,   c->state, c->arrive};

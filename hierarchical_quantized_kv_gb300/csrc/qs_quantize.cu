@@ -78,6 +78,23 @@ __device__ __forceinline__ int vmeta_pos(int t) {
   return ((t >> 3) & 1) | (((t >> 4) & 1) << 1) | ((t & 7) << 2) | ((t >> 5) << 5);
 }
 
+// Two-bit draft layout: four consecutive 32-bit words w[0..3] of a 4-bit
+// upper plane (nibble C_U = 4 C_U2 + M2) become two words of the group's
+// C_U2 plane and two of its M2 plane (second 4 KB of the group's 8 KB).
+// Word k of each holds, in nibble position j, the two-bit field of word 2k's
+// nibble j in bits 4j..4j+1 and of word 2k+1's nibble j in bits 4j+2..4j+3.
+// base: the group's upper plane; off: byte offset of w[0] in the 4-bit plane
+// (a multiple of 16), so the two words go to off / 2.
+__device__ __forceinline__ void store_upper2(uint8_t *base, size_t off, const uint32_t (&w)[4]) {
+  uint2 u, m;
+  u.x = ((w[0] >> 2) & 0x33333333u) | (w[1] & 0xCCCCCCCCu);
+  u.y = ((w[2] >> 2) & 0x33333333u) | (w[3] & 0xCCCCCCCCu);
+  m.x = (w[0] & 0x33333333u) | ((w[1] & 0x33333333u) << 2);
+  m.y = (w[2] & 0x33333333u) | ((w[3] & 0x33333333u) << 2);
+  *reinterpret_cast<uint2 *>(base + off / 2) = u;
+  *reinterpret_cast<uint2 *>(base + (size_t)kG * kD / 4 + off / 2) = m;
+}
+
 // One CTA's share of quantizing a group of G tokens whose fp16 key and value
 // rows (D channels each, row stride D) start at gk and gv: key channels
 // [32 part, 32 part + 32) and value tokens [32 part, 32 part + 32), written
@@ -169,8 +186,11 @@ __device__ void quantize_part(FlushSmem &S, const __half *gk, const __half *gv, 
       wu[i >> 2] |= ((c0 >> 4) | (c1 & 0xF0u)) << (8 * (i & 3));
       wl[i >> 2] |= ((c0 & 15u) | ((c1 & 15u) << 4)) << (8 * (i & 3));
     }
-    reinterpret_cast<uint4 *>(c.k_upper + (grp * kG + tid) * (kD / 2))[part] =
-        make_uint4(wu[0], wu[1], wu[2], wu[3]);
+    if (c.upper_bits == 2)
+      store_upper2(c.k_upper + grp * kG * (kD / 2), 16 * (4 * tid + part), wu);
+    else
+      reinterpret_cast<uint4 *>(c.k_upper + (grp * kG + tid) * (kD / 2))[part] =
+          make_uint4(wu[0], wu[1], wu[2], wu[3]);
     reinterpret_cast<uint4 *>(c.k_lower + (grp * kG + tid) * (kD / 2))[part] =
         make_uint4(wl[0], wl[1], wl[2], wl[3]);
   } else {
@@ -184,7 +204,10 @@ __device__ void quantize_part(FlushSmem &S, const __half *gk, const __half *gv, 
       wl[q >> 3] |= (code & 15u) << (4 * (q & 7));
     }
     const size_t row = (grp * 4 + part) * kD + d;
-    reinterpret_cast<uint4 *>(c.v_upper)[row] = make_uint4(wu[0], wu[1], wu[2], wu[3]);
+    if (c.upper_bits == 2)
+      store_upper2(c.v_upper + grp * kG * (kD / 2), 16 * (part * kD + d), wu);
+    else
+      reinterpret_cast<uint4 *>(c.v_upper)[row] = make_uint4(wu[0], wu[1], wu[2], wu[3]);
     reinterpret_cast<uint4 *>(c.v_lower)[row] = make_uint4(wl[0], wl[1], wl[2], wl[3]);
   }
   // 7. metadata: key scale / zero of the channel slice, value scale / zero of the quarter

@@ -30,7 +30,7 @@ _I32 = ctypes.c_int32
 
 class QsCacheStruct(ctypes.Structure):
     _fields_ = [("B", _I32), ("H", _I32), ("D", _I32), ("G", _I32), ("cap_groups", _I32),
-                ("k_upper", _P), ("k_lower", _P), ("v_upper", _P), ("v_lower", _P),
+                ("upper_bits", _I32), ("k_upper", _P), ("k_lower", _P), ("v_upper", _P), ("v_lower", _P),
                 ("meta", _P), ("buf_k", _P), ("buf_v", _P), ("state", _P), ("arrive", _P)]
 
 
@@ -121,9 +121,12 @@ class Cache:
     """A hierarchical quantized KV cache in torch-owned device memory, laid
     out as include/qs.h describes (shapes below are the C layouts)."""
 
-    def __init__(self, B, H, cap_groups, device="cuda", D=128, G=128):
+    def __init__(self, B, H, cap_groups, device="cuda", D=128, G=128, upper_bits=4):
+        """upper_bits: the top bits of each 8-bit code the draft reads (4, or
+        2 for the two-bit draft layout of include/qs.h)."""
         import torch
         self.B, self.H, self.D, self.G, self.cap = B, H, D, G, cap_groups
+        self.upper_bits = upper_bits
         qs_cache_bytes(B, H, cap_groups, D, G)  # validates the sizes
         u8 = dict(dtype=torch.uint8, device=device)
         f16 = dict(dtype=torch.float16, device=device)
@@ -136,7 +139,7 @@ class Cache:
         self.buf_v = torch.zeros((B, H, 2 * G, D), **f16)
         self.state = torch.zeros((B, STATE_WORDS), dtype=torch.int32, device=device)
         self.arrive = torch.zeros((B, H), dtype=torch.int32, device=device)
-        self.struct = QsCacheStruct(B, H, D, G, cap_groups,
+        self.struct = QsCacheStruct(B, H, D, G, cap_groups, upper_bits,
                                     self.k_upper.data_ptr(), self.k_lower.data_ptr(),
                                     self.v_upper.data_ptr(), self.v_lower.data_ptr(),
                                     self.meta.data_ptr(), self.buf_k.data_ptr(),

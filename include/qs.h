@@ -71,7 +71,10 @@ typedef enum {
 } qs_status;
 
 typedef enum {
-  QS_DRAFT_UPPER4 = 0, /* keys/values from C_U only: s * (16 C_U + 8) + z */
+  QS_DRAFT_UPPER4 = 0, /* the draft: keys/values from the top upper_bits bits of
+                          the code only, at the middle of the codes sharing them:
+                          s * (16 C_U + 8) + z (upper_bits 4), or
+                          s * (64 C_U2 + 32) + z (upper_bits 2) */
   QS_VERIFY_INT8 = 1   /* keys/values from C_U and C_L: s * (16 C_U + C_L) + z */
 } qs_mode;
 
@@ -107,6 +110,7 @@ enum { QS_META_K_SCALE = 0, QS_META_K_ZERO = 1, QS_META_V_SCALE = 2, QS_META_V_Z
  * aligned.  Logical buffer token i of sequence b lives in slot
  * (half_base * G + i) mod 2G.  Sizes for each array: qs_cache_bytes.
  *
+ *  upper_bits  4 or 2: how many top bits of C_INT8 the draft reads (below).
  *  k_upper, k_lower  uint8 [B][H][cap][G tokens][D/2]: C_U / C_L of the keys,
  *      token-major; byte i of a token row holds channel 2i in bits 0-3 and
  *      channel 2i+1 in bits 4-7 (64 bytes per token).
@@ -124,6 +128,17 @@ enum { QS_META_K_SCALE = 0, QS_META_K_ZERO = 1, QS_META_V_SCALE = 2, QS_META_V_Z
  *          32*((p>>3)&3) + 8*(p>>5) + 2*((p>>2)&1) + ((p>>1)&1) + 4*(p&1);
  *        value rows: position p holds token
  *          32*(p>>5) + ((p>>2)&7) + 16*((p>>1)&1) + 8*(p&1).
+ *  With upper_bits = 2 (C_INT8 = 64 C_U2 + 16 M2 + C_L, the draft reading
+ *      the top two bits only; source: Pith review page, "Editorial
+ *      extensions", "Reading between the lines": the 4/8 split generalizes to
+ *      the top k bits for the draft) the 8 KB of k_upper / v_upper per group hold
+ *      the same nibbles C_U = 4 C_U2 + M2 re-packed: regard the 4-bit plane
+ *      above as a sequence of 32-bit words w_0, w_1, ... (8 nibbles each,
+ *      nibble j in bits 4j..4j+3).  Word k of the first 4 KB (the C_U2 plane)
+ *      holds, in nibble position j, C_U2 of w_2k's nibble j in bits 4j..4j+1
+ *      and C_U2 of w_2k+1's nibble j in bits 4j+2..4j+3; word k of the second
+ *      4 KB (the M2 plane) holds M2 the same way.  k_lower, v_lower and meta
+ *      are the same for both.
  *  buf_k, buf_v  fp16 [B][H][2G][D]: the double full-precision buffer.
  *  state  int32 [B][QS_STATE_WORDS]: counters above; zero it (qs_state_reset)
  *      before first use.
@@ -134,6 +149,7 @@ enum { QS_META_K_SCALE = 0, QS_META_K_ZERO = 1, QS_META_V_SCALE = 2, QS_META_V_Z
  */
 typedef struct {
   int32_t B, H, D, G, cap_groups;
+  int32_t upper_bits;     /* 4 or 2 */
   uint8_t *k_upper, *k_lower, *v_upper, *v_lower;
   uint16_t *meta;         /* fp16 bits */
   uint16_t *buf_k, *buf_v; /* fp16 bits */
@@ -246,7 +262,8 @@ qs_status qs_attn_workspace_size(const qs_cache *c, int32_t n_q, size_t *bytes);
  *   q      fp16 [B][H][n_q][D] device, 1 <= n_q <= 8; query j of sequence b sits
  *          at buffer position fill - n_q + j and sees every token at or before
  *          it (all quantized tokens plus a causal prefix of the buffer);
- *   mode   QS_DRAFT_UPPER4 (reads C_U planes only) or QS_VERIFY_INT8;
+ *   mode   QS_DRAFT_UPPER4 (reads the upper planes only: C_U, or with
+ *          upper_bits 2 their C_U2 half) or QS_VERIFY_INT8;
  *   softmax_scale  multiplies q . k (usually 1/sqrt(D));
  *   out    fp16 [B][H][n_q][D] device: softmax-weighted sum of the values;
  *   lse    float [B][H][n_q] device or NULL: natural log of the softmax

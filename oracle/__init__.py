@@ -122,8 +122,11 @@ def split_code(q):
     return u.value, l_.value
 
 
-def dequant(q, scale_bits, zero_bits, upper_only):
-    return lib().qso_dequant(int(q), int(scale_bits), int(zero_bits), int(bool(upper_only)))
+def dequant(q, scale_bits, zero_bits, upper_only, upper_bits=4):
+    """fp64 dequantized value of code q: the INT8 code, or (upper_only) the
+    draft's reconstruction from the top upper_bits bits."""
+    return lib().qso_dequant(int(q), int(scale_bits), int(zero_bits),
+                             int(upper_bits) if upper_only else 0)
 
 
 def spec_accept(p, q, draft, u, e):
@@ -206,10 +209,11 @@ class OracleCache:
         c = self._c()
         lib().qso_prefill(ctypes.byref(c), _ptr(kb), _ptr(vb), kb.shape[2], _ptr(n))
 
-    def attn(self, q, upper_only, scale=None, group=1):
+    def attn(self, q, upper_only, scale=None, group=1, upper_bits=4):
         """Decode attention in fp64: q [B, H*group, n_q, D] fp16 ->
         (out [B, H*group, n_q, D] float64, lse [B, H*group, n_q] float64);
-        query head h*group + i reads KV head h."""
+        query head h*group + i reads KV head h.  upper_only: the draft, which
+        reconstructs each code from its top upper_bits bits."""
         qb = _as_half_bits(q)
         assert qb.shape[1] == self.H * group
         n_q = qb.shape[2]
@@ -219,7 +223,8 @@ class OracleCache:
         out = np.zeros((self.B, self.H * group, n_q, self.D), np.float64)
         lse = np.zeros((self.B, self.H * group, n_q), np.float64)
         c = self._c()
-        lib().qso_attn(ctypes.byref(c), int(bool(upper_only)), _ptr(qb), n_q, int(group), scale,
+        lib().qso_attn(ctypes.byref(c), int(upper_bits) if upper_only else 0, _ptr(qb), n_q,
+                       int(group), scale,
                        _ptr(out), _ptr(lse))
         return out, lse
 

@@ -35,6 +35,12 @@
  *   q_i = s == 0 ? 0 : clamp(rne((fp32(x_i) - fp32(z)) / fp32(s)), 0, 255)
  *   C_U = q >> 4, C_L = q & 15
  *   deq8 = s * (16*C_U + C_L) + z,   deqU = s * (16*C_U + 8) + z
+ * A draft that reads the top k bits instead of four ([P3], "Editorial
+ * extensions", "Reading between the lines": the 4/8 split generalizes to the
+ * top k bits for the draft; the pages show k = 4 only) reconstructs, as our
+ * reading, at the middle of the 2^(8-k) codes
+ * sharing those bits, as the k = 4 midpoint does: with sh = 8 - k,
+ *   deqK = s * (2^sh * (q >> sh) + 2^(sh-1)) + z     (k = 2: 64*C_U2 + 32).
  */
 #include <math.h>
 #include <stdint.h>
@@ -172,10 +178,16 @@ void qso_split_code(uint8_t q, uint8_t *upper, uint8_t *lower) {
   *lower = (uint8_t)(q & 15);
 }
 
-/* Dequantized value in fp64: mode 0 = INT8 (verify), 1 = upper only (draft). */
-double qso_dequant(uint8_t q, uint16_t scale, uint16_t zero, int upper_only) {
+/* Dequantized value in fp64: draft_bits = 0, the INT8 code (verify); k in
+ * 1..7, the draft's reconstruction from the top k bits (deqK above; k = 4 is
+ * 16*C_U + 8). */
+double qso_dequant(uint8_t q, uint16_t scale, uint16_t zero, int draft_bits) {
   double s = qso_half_to_double(scale), z = qso_half_to_double(zero);
-  double c = upper_only ? 16.0 * (double)(q >> 4) + 8.0 : (double)q;
+  double c = (double)q;
+  if (draft_bits > 0) {
+    int sh = 8 - draft_bits;
+    c = (double)((q >> sh) << sh) + (double)(1 << (sh - 1));
+  }
   return s * c + z;
 }
 
@@ -428,7 +440,8 @@ void qso_spec_accept(const float *p, const float *q, const int32_t *draft,
  * of the `group` query heads that share KV head h (grouped-query attention;
  * group = 1 is multi-head): q is [B][H*group][n_q][D] fp16, query head
  * h*group + i reads KV head h.  Keys/values are the dequantized groups
- * (upper_only = 1: draft, 16*C_U + 8; 0: verify, INT8) followed by the fp16
+ * (draft_bits = k > 0: draft from the top k bits, deqK; 0: verify, INT8)
+ * followed by the fp16
  * buffer tokens.  Query j sits at the position of buffer token
  * fill - n_q + j and sees every token at or before it.  Writes
  * out [B][H*group][n_q][D] and lse [B][H*group][n_q] (natural log of the
@@ -436,7 +449,7 @@ void qso_spec_accept(const float *p, const float *q, const int32_t *draft,
  * QSO_DEV_NQ_GT_FILL, zero output and lse = -inf.
  * [P1] "Hierarchical Two-Level Quantization" (draft loads upper 4 bits,
  * target reconstructs INT8); [P3] "What carries the argument". */
-void qso_attn(qso_cache *c, int upper_only, const uint16_t *q, int n_q, int group,
+void qso_attn(qso_cache *c, int draft_bits, const uint16_t *q, int n_q, int group,
               double scale, double *out, double *lse) {
   int G = c->G, D = c->D;
   for (int b = 0; b < c->B; ++b)
@@ -463,10 +476,10 @@ void qso_attn(qso_cache *c, int upper_only, const uint16_t *q, int n_q, int grou
         for (int d = 0; d < D; ++d) {
           K[t * D + d] = qso_dequant(c->kq[(grp * G + i) * D + d],
                                      c->ks[grp * D + d], c->kz[grp * D + d],
-                                     upper_only);
+                                     draft_bits);
           V[t * D + d] = qso_dequant(c->vq[(grp * G + i) * D + d],
                                      c->vs[grp * G + i], c->vz[grp * G + i],
-                                     upper_only);
+                                     draft_bits);
         }
       }
       for (int i = 0; i < fill; ++i) {

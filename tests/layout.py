@@ -60,10 +60,29 @@ def meta(ks, kz, vs, vz):
     return np.stack([ks[..., kp], kz[..., kp], vs[..., vp], vz[..., vp]], axis=-2).astype(np.uint16)
 
 
-def device_arrays(oc: oracle.OracleCache):
-    """The oracle state in the device layout (numpy)."""
+def repack_upper2(plane):
+    """A 4-bit upper plane (8 KB per group, any group shape) in the two-bit
+    draft layout of include/qs.h: per group, words 2k and 2k+1 of the nibble
+    plane give word k of the C_U2 plane (first 4 KB) and of the M2 plane
+    (second 4 KB); nibble j of word k holds word 2k's field in bits 0-1 and
+    word 2k+1's in bits 2-3 (C_U = 4 C_U2 + M2)."""
+    shp = plane.shape
+    w = np.ascontiguousarray(plane).reshape(-1, 2048).view(np.uint8)
+    w = w.reshape(-1, 8192).copy().view("<u4")  # [groups, 2048] words
+    a, b = w[:, 0::2], w[:, 1::2]
+    u2 = ((a >> 2) & 0x33333333) | (b & 0xCCCCCCCC)
+    m2 = (a & 0x33333333) | ((b & 0x33333333) << 2)
+    out = np.concatenate([u2, m2], axis=1).astype("<u4")
+    return out.view(np.uint8).reshape(shp)
+
+
+def device_arrays(oc: oracle.OracleCache, upper_bits=4):
+    """The oracle state in the device layout (numpy); upper_bits = 2 gives the
+    two-bit draft layout of the upper planes."""
     ku, kl = pack_k(oc.kq)
     vu, vl = pack_v(oc.vq)
+    if upper_bits == 2:
+        ku, vu = repack_upper2(ku), repack_upper2(vu)
     return dict(k_upper=ku, k_lower=kl, v_upper=vu, v_lower=vl,
                 meta=meta(oc.ks, oc.kz, oc.vs, oc.vz),
                 buf_k=oc.bk, buf_v=oc.bv, state=oc.state)
@@ -72,7 +91,7 @@ def device_arrays(oc: oracle.OracleCache):
 def load_into(cache, oc: oracle.OracleCache):
     """Copy the oracle's state into a device cache (qs.Cache)."""
     import torch
-    arrs = device_arrays(oc)
+    arrs = device_arrays(oc, getattr(cache, "upper_bits", 4))
     for name, a in arrs.items():
         t = getattr(cache, name)
         src = torch.from_numpy(np.ascontiguousarray(a))

@@ -46,7 +46,7 @@ def test_cache_bytes_and_unsupported_sizes(L):
 
 
 def _fake_cache(**kw):
-    c = qs.QsCacheStruct(1, 2, 128, 128, 4, *([0x10000] * 9))
+    c = qs.QsCacheStruct(1, 2, 128, 128, 4, 4, *([0x10000] * 9))
     for k, v in kw.items():
         setattr(c, k, v)
     return c
@@ -62,6 +62,9 @@ def test_host_validation_before_any_cuda_call(L):
     assert L.qs_state_reset(ctypes.byref(c), None) == qs.QS_ERR_ARG
     c = _fake_cache(D=96)
     assert L.qs_state_reset(ctypes.byref(c), None) == qs.QS_ERR_UNSUPPORTED
+    for ub in (0, 1, 3, 8):
+        c = _fake_cache(upper_bits=ub)
+        assert L.qs_state_reset(ctypes.byref(c), None) == qs.QS_ERR_ARG
     c = _fake_cache(B=300)
     assert L.qs_quantize_flush(ctypes.byref(c), None, None) == qs.QS_ERR_UNSUPPORTED
     c = _fake_cache()

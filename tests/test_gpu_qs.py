@@ -40,7 +40,7 @@ def to_dev(torch, a):
 
 def assert_state_equal(cache, oc, what=""):
     got = layout.read_device(cache)
-    want = layout.device_arrays(oc)
+    want = layout.device_arrays(oc, cache.upper_bits)
     for name in want:
         g, w_ = got[name], want[name]
         if name == "state":
@@ -423,6 +423,58 @@ def test_prefill_bit_exact_then_decode(torch):
     assert np.all(qs.qs_get_errors(cache) == 0)
 
 
+def test_two_bit_draft_layout(torch):
+    """upper_bits = 2 (a draft from the top two bits of each code): prefill
+    and flush write the C_U2 / M2 planes bit for bit; draft (one query and
+    three) and verify attention match the oracle, before and after a flush
+    and an append; the same cache read with the 4-bit draft differs."""
+    rng = np.random.default_rng(37)
+    B, H, T, cap = 3, 2, 700, 6
+    lens = np.array([300, 129, 700], np.int32)
+    k, v = _prompt(rng, B, H, T)
+    cache = qs.Cache(B, H, cap, upper_bits=2)
+    qs.qs_prefill(cache, to_dev(torch, k), to_dev(torch, v), to_dev(torch, lens))
+    oc = oracle.OracleCache(B, H, 128, 128, cap)
+    oc.prefill(k, v, lens)
+    assert_state_equal(cache, oc, "two-bit prefill")
+
+    def both(what):
+        for mode, n_q in ((DRAFT, 1), (DRAFT, 3), (VERIFY, 5)):
+            q = h16(rng, (B, H, n_q, 128))
+            got, gl = run_attn(torch, cache, mode, q)
+            ref, rl = oc.attn(q, upper_only=(mode == DRAFT), upper_bits=2)
+            assert_close(got, ref, gl, rl, "%s, mode %d, n_q %d" % (what, mode, n_q))
+            if mode == DRAFT:
+                ref4, _ = oc.attn(q, upper_only=True, upper_bits=4)
+                assert np.abs(got - ref4).max() > 10 * ATOL
+    both("after prefill")
+    mask = torch.zeros(B, dtype=torch.uint8, device="cuda")
+    qs.qs_need_flush(cache, 130, mask)
+    qs.qs_quantize_flush(cache, mask)
+    oc.flush(oc.need_flush(130))
+    k5, v5 = _prompt(rng, B, H, 5)
+    qs.qs_buffer_append(cache, to_dev(torch, k5), to_dev(torch, v5))
+    oc.append(k5, v5)
+    assert_state_equal(cache, oc, "two-bit flush + append")
+    both("after flush")
+    assert np.all(qs.qs_get_errors(cache) == 0)
+
+
+@pytest.mark.parametrize("n_groups,fill,n_q", [(0, 8, 1), (1, 33, 5), (2, 128, 2), (5, 255, 8),
+                                               (3, 65, 1)])
+def test_two_bit_attn_edge_cases(torch, n_groups, fill, n_q):
+    rng = np.random.default_rng(500 + 10 * n_groups + n_q)
+    B, H = 2, 3
+    oc = _oracle_state(rng, B, H, [n_groups, n_groups], [fill, fill], cap=max(n_groups, 1))
+    cache = qs.Cache(B, H, max(n_groups, 1), upper_bits=2)
+    layout.load_into(cache, oc)
+    q = h16(rng, (B, H, n_q, 128))
+    for mode in (DRAFT, VERIFY):
+        got, gl = run_attn(torch, cache, mode, q)
+        ref, rl = oc.attn(q, upper_only=(mode == DRAFT), upper_bits=2)
+        assert_close(got, ref, gl, rl, "mode %d" % mode)
+
+
 def test_prefill_error_paths(torch):
     rng = np.random.default_rng(7)
     H, T = 1, 400
@@ -488,23 +540,25 @@ def _sampled_oracle(w, bs, hs):
     return oc
 
 
-@pytest.mark.parametrize("cfg,bs,hs", [
-    ("32k", [0], list(range(32))),
-    ("128k", [0], [0, 7, 19, 31]),
-    ("batched32k", [0, 5, 7], [1, 30]),
-    ("ragged", [0, 3, 9, 15], [2, 17]),
+@pytest.mark.parametrize("cfg,bs,hs,ub", [
+    ("32k", [0], list(range(32)), 4),
+    ("128k", [0], [0, 7, 19, 31], 4),
+    ("batched32k", [0, 5, 7], [1, 30], 4),
+    ("ragged", [0, 3, 9, 15], [2, 17], 4),
+    ("32k", [0], [0, 13, 31], 2),
 ])
-def test_full_size_sampled(torch, cfg, bs, hs):
+def test_full_size_sampled(torch, cfg, bs, hs, ub):
     """Full-size workloads in the launch configuration the benchmark times;
-    the oracle recomputes the sampled (sequence, head) pairs."""
+    the oracle recomputes the sampled (sequence, head) pairs.  ub: the top
+    bits the draft reads (2: the two-bit draft layout)."""
     w = synthetic.CONFIGS[cfg]()
     cap = max(w.n_groups) + 1
-    cache = qs.Cache(w.B, w.H, cap)
+    cache = qs.Cache(w.B, w.H, cap, upper_bits=ub)
     driver.prefill(cache, w)
     oc = _sampled_oracle(w, bs, hs)
     # quantized planes of the sampled heads, bit for bit
     dev = layout.read_device(cache)
-    want = layout.device_arrays(oc)
+    want = layout.device_arrays(oc, ub)
     for name in ("k_upper", "k_lower", "v_upper", "v_lower", "meta"):
         g = dev[name][np.ix_(bs, hs)]
         assert np.array_equal(g[:, :, :oc.cap], want[name]), name
@@ -513,7 +567,8 @@ def test_full_size_sampled(torch, cfg, bs, hs):
     def both(call, mode, n_q):
         q = synthetic.queries(w, call, n_q)
         got, gl = run_attn(torch, cache, mode, q)
-        ref, rl = oc.attn(np.ascontiguousarray(q[np.ix_(bs, hs)]), upper_only=(mode == DRAFT))
+        ref, rl = oc.attn(np.ascontiguousarray(q[np.ix_(bs, hs)]), upper_only=(mode == DRAFT),
+                          upper_bits=ub)
         assert_close(got[np.ix_(bs, hs)], ref, gl[np.ix_(bs, hs)], rl, "%s mode %d" % (cfg, mode))
 
     both(0, DRAFT, 1)
@@ -532,7 +587,7 @@ def test_full_size_sampled(torch, cfg, bs, hs):
     qs.qs_buffer_append(cache, to_dev(torch, k), to_dev(torch, v))
     oc.append(np.ascontiguousarray(k[np.ix_(bs, hs)]), np.ascontiguousarray(v[np.ix_(bs, hs)]))
     dev = layout.read_device(cache)
-    want = layout.device_arrays(oc)
+    want = layout.device_arrays(oc, ub)
     for name in ("k_upper", "v_lower", "meta"):
         g = dev[name][np.ix_(bs, hs)]
         assert np.array_equal(g[:, :, :want[name].shape[2]], want[name]), name
@@ -564,24 +619,25 @@ def run_attn_gqa(torch, cache, mode, q, group):
     return out.double().cpu().numpy(), lse.double().cpu().numpy()
 
 
-@pytest.mark.parametrize("group,n_q", [(4, 1), (8, 1), (4, 5), (2, 5), (3, 8), (1, 5), (5, 4),
-                                       (24, 1)])
-def test_gqa_attention(torch, group, n_q):
+@pytest.mark.parametrize("group,n_q,ub", [(4, 1, 4), (8, 1, 4), (4, 5, 4), (2, 5, 4), (3, 8, 4),
+                                          (1, 5, 4), (5, 4, 4), (24, 1, 4), (4, 1, 2), (4, 5, 2),
+                                          (3, 8, 2)])
+def test_gqa_attention(torch, group, n_q, ub):
     """Grouped-query attention (query head h*g + i on KV head h) against the
     oracle for 1, 2 and 3 column groups of query rows (up to 24 rows per KV
-    head), ragged prompts, both modes."""
+    head), ragged prompts, both modes, 4- and 2-bit drafts."""
     rng = np.random.default_rng(70 + 10 * group + n_q)
     B, H, T, cap = 3, 2, 2200, 17
     lens = np.array([1000, 333, 2200], np.int32)
     k, v = h16(rng, (B, H, T, 128), 2.0), h16(rng, (B, H, T, 128))
-    cache = qs.Cache(B, H, cap)
+    cache = qs.Cache(B, H, cap, upper_bits=ub)
     qs.qs_prefill(cache, to_dev(torch, k), to_dev(torch, v), to_dev(torch, lens))
     oc = oracle.OracleCache(B, H, 128, 128, cap)
     oc.prefill(k, v, lens)
     for mode in (DRAFT, VERIFY):
         q = h16(rng, (B, H * group, n_q, 128))
         got, gl = run_attn_gqa(torch, cache, mode, q, group)
-        ref, rl = oc.attn(q, upper_only=(mode == DRAFT), group=group)
+        ref, rl = oc.attn(q, upper_only=(mode == DRAFT), group=group, upper_bits=ub)
         assert_close(got, ref, gl, rl, "gqa g=%d n_q=%d mode %d" % (group, n_q, mode))
     assert np.all(qs.qs_get_errors(cache) == 0)
 

@@ -159,6 +159,34 @@ def test_dequant_error_bounds(scale_exp):
     assert worst8 > 0.49 and worstU > 8.3
 
 
+@pytest.mark.parametrize("scale_exp", [-6, 0, 4])
+def test_two_bit_draft_error_bound(scale_exp):
+    """Top-2-bit draft (a k-bit draft in general, the pages show k = 4 only):
+    the reconstruction sits at the middle of the 64 codes sharing the top two
+    bits, so |x - deq2| <= s (32.5 + eps), and the bound is reached."""
+    r = np.random.default_rng(30 + scale_exp)
+    worst = 0.0
+    for _ in range(300):
+        x = h(r.standard_normal(128) * 2.0 ** scale_exp + r.uniform(-3, 3) * 2.0 ** scale_exp)
+        s, z, q = oracle.quantize_group(x)
+        d2 = np.array([oracle.dequant(c, s, z, True, upper_bits=2) for c in q])
+        e = np.max(np.abs(x.astype(np.float64) - d2)) / f16(s)
+        assert e <= 32.5 + 2.0 ** -13
+        worst = max(worst, e)
+    assert worst > 31.5
+
+
+def test_k_bit_draft_is_the_int8_code_at_the_bucket_middle():
+    """For every code, the k-bit draft value is the INT8 value of the code
+    with the same top k bits and the low bits at the middle (k = 4: | 0x08;
+    k = 2: | 0x20), and the draft reads no bit below the top k."""
+    s, z = int(hbits(0.0625)), int(hbits(-3.0))
+    for q in range(256):
+        assert oracle.dequant(q, s, z, True, 4) == oracle.dequant((q & 0xF0) | 0x08, s, z, False)
+        assert oracle.dequant(q, s, z, True, 2) == oracle.dequant((q & 0xC0) | 0x20, s, z, False)
+        assert oracle.dequant(q, s, z, True, 2) == oracle.dequant(q & 0xC0, s, z, True, 2)
+
+
 def test_codes_stay_in_range_for_extreme_groups():
     for x in ([-65504.0, 65504.0] + [0.0] * 126, [-1e-3, 6e4] * 64):
         s, z, q = oracle.quantize_group(h(x))
@@ -363,6 +391,30 @@ def test_draft_equals_verify_when_every_lower_level_is_eight():
     o_v2, _ = c.attn(q, upper_only=False)
     o_d2, _ = c.attn(q, upper_only=True)
     assert np.array_equal(o_d2, o_d) and not np.allclose(o_v2, o_d)
+
+
+def test_two_bit_draft_equals_verify_when_the_low_six_bits_are_32():
+    rng = np.random.default_rng(13)
+    H, D, G = 2, 128, 128
+    c = oracle.OracleCache(1, H, D, G, cap=3)
+    c.append(h(rng.standard_normal((1, H, 20, D))), h(rng.standard_normal((1, H, 20, D))))
+    c.state[0, oracle.N_GROUPS] = 3
+    c.kq[:] = (rng.integers(0, 4, c.kq.shape) * 64 + 32).astype(np.uint8)
+    c.vq[:] = (rng.integers(0, 4, c.vq.shape) * 64 + 32).astype(np.uint8)
+    for a in (c.ks, c.vs):
+        a[:] = hbits(2.0 ** rng.integers(-8, -3, a.shape))
+    for a in (c.kz, c.vz):
+        a[:] = hbits(rng.uniform(-2, 2, a.shape))
+    q = h(rng.standard_normal((1, H, 4, D)))
+    o_d, l_d = c.attn(q, upper_only=True, upper_bits=2)
+    o_v, l_v = c.attn(q, upper_only=False)
+    assert np.array_equal(o_d, o_v) and np.array_equal(l_d, l_v)
+    # codes with other low bits move the verify result but not the draft's
+    c.kq[:] ^= (rng.integers(0, 32, c.kq.shape)).astype(np.uint8)
+    o_d2, _ = c.attn(q, upper_only=True, upper_bits=2)
+    o_v2, _ = c.attn(q, upper_only=False)
+    o_d4, _ = c.attn(q, upper_only=True, upper_bits=4)
+    assert np.array_equal(o_d2, o_d) and not np.allclose(o_v2, o_d) and not np.allclose(o_d4, o_d)
 
 
 def test_causal_mask_matches_single_query_after_rollback():
