@@ -188,6 +188,29 @@ class Round:
         self.od = [torch.empty_like(q) for q in self.qd]
         self.ov = torch.empty_like(self.qv)
         self.lse = torch.empty((B, H, GAMMA + 1), dtype=torch.float32, device=dev)
+
+        # The step's inputs live in one device buffer and its outputs in
+        # another (views at 16-byte aligned offsets), so the end-to-end run
+        # moves each with a single copy.
+        def arena(tensors):
+            sizes = [t.numel() * t.element_size() for t in tensors]
+            offs, o = [], 0
+            for n in sizes:
+                offs.append(o)
+                o += -(-n // 16) * 16
+            buf = torch.empty(o, dtype=torch.uint8, device=dev)
+            views = []
+            for t, off, n in zip(tensors, offs, sizes):
+                v = buf[off:off + n].view(t.dtype).view(t.shape)
+                v.copy_(t)
+                views.append(v)
+            return buf, views
+        self.in_arena, v = arena(self.kd + self.vd + [self.kt, self.vt] + self.qd + [self.qv])
+        self.kd, self.vd = v[:GAMMA], v[GAMMA:2 * GAMMA]
+        self.kt, self.vt = v[2 * GAMMA], v[2 * GAMMA + 1]
+        self.qd, self.qv = v[2 * GAMMA + 2:3 * GAMMA + 2], v[3 * GAMMA + 2]
+        self.out_arena, v = arena(self.od + [self.ov, self.lse])
+        self.od, self.ov, self.lse = v[:GAMMA], v[GAMMA], v[GAMMA + 1]
         n_ws = max(qs.qs_attn_workspace_size(self.cache, 1), qs.qs_attn_workspace_size(self.cache, GAMMA + 1))
         self.ws = torch.empty(n_ws, dtype=torch.uint8, device=dev)
         self.mask = torch.zeros(B, dtype=torch.uint8, device=dev)
@@ -253,12 +276,13 @@ class Round:
 
 class HostIO:
     """Pinned host buffers for the end-to-end number: every step copies its
-    inputs host -> device and its outputs device -> host."""
+    inputs host -> device and its outputs device -> host (one copy each: the
+    step's inputs and outputs are packed in one device buffer each)."""
 
     def __init__(self, torch, r):
         pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t.cpu())
-        self.ins = [(pin(t), t) for t in r.kd + r.vd + [r.kt, r.vt] + r.qd + [r.qv]]
-        self.outs = [(t, torch.empty(t.shape, dtype=t.dtype, pin_memory=True)) for t in r.od + [r.ov, r.lse]]
+        self.ins = [(pin(r.in_arena), r.in_arena)]
+        self.outs = [(r.out_arena, torch.empty(r.out_arena.shape, dtype=torch.uint8, pin_memory=True))]
         self.h2d_bytes = sum(h.numel() * h.element_size() for h, _ in self.ins)
         self.d2h_bytes = sum(h.numel() * h.element_size() for _, h in self.outs)
 
