@@ -65,6 +65,22 @@ def stored_traffic(kind):
         return None
 
 
+def rank_max(dist, world, x, device):
+    """x maximized over the ranks: the slowest replica sets the job's time."""
+    if world == 1:
+        return x
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_gbs(step_bytes_per_rank, world, ms):
+    """Whole-job throughput: every replica's bytes per step over the slowest
+    replica's step time (weak scaling)."""
+    return step_bytes_per_rank * world / (ms * 1e-3) / 1e9
+
+
 def load_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -421,12 +437,8 @@ def native(args):
     if world > 1:
         dist.barrier()
     sampler.stop()
-    ms = ev0.elapsed_time(ev1) / args.steps
+    ms = rank_max(dist, world, ev0.elapsed_time(ev1) / args.steps, "cuda")
     clocks = sampler.summary(t0, t1)
-    if world > 1:
-        tt = torch.tensor([ms], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
 
     # per-call timing with L2 flushed (draft, verify, flush)
     l2 = torch.ones(64 << 20, dtype=torch.float32, device="cuda")  # 256 MB
@@ -507,11 +519,7 @@ def native(args):
     for s in range(e_steps):
         egraphs[s % len(egraphs)].replay()
         torch.cuda.current_stream().synchronize()  # the host reads the step's result
-    e2e_ms = (time.perf_counter() - te0) * 1e3 / e_steps
-    if world > 1:
-        tt = torch.tensor([e2e_ms], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
+    e2e_ms = rank_max(dist, world, (time.perf_counter() - te0) * 1e3 / e_steps, "cuda")
 
     errs = qs.qs_get_errors(r.cache)
     assert np.all(errs == 0), errs
@@ -522,7 +530,7 @@ def native(args):
         dist.destroy_process_group()
     if rank != 0:
         return
-    gbs = r.step_bytes * world / (ms * 1e-3) / 1e9
+    gbs = aggregate_gbs(r.step_bytes, world, ms)
     line = {
         "metric": METRIC, "value": round(gbs, 1), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
@@ -552,7 +560,7 @@ def native(args):
                      "achieved": round(dominant[1], 1), "peak": peak,
                      "peak_kind": "%s hbm_gbs (copy, burst)" % peak_kind, "unit": "GB/s",
                      "frac": round(dominant[1] / peak, 4), "traffic": stored_traffic(dominant[0])},
-        "e2e": {"value": round(r.step_bytes * world / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+        "e2e": {"value": round(aggregate_gbs(r.step_bytes, world, e2e_ms), 1), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": host.h2d_bytes,
                 "d2h_bytes_per_step": host.d2h_bytes},
         "gpu_launches": r.launches_per_step * args.steps,
