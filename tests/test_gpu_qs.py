@@ -139,6 +139,46 @@ def test_append_overflow_is_a_no_op(torch):
     assert np.all(qs.qs_get_errors(cache) == 0)  # read-back clears
 
 
+def test_corrupted_counters_written_from_the_host(torch):
+    """Host-side fault injection: counters past every limit (negative, past
+    the capacity, past the ring, an odd half base) written straight into the
+    state.  Every call stays in bounds (device counters are validated or
+    clamped before they index anything): no CUDA error, each sequence's
+    error word flags it, attention outputs are finite, the segment counters
+    end at zero, and after qs_state_reset a normal round works again."""
+    rng = np.random.default_rng(91)
+    B, H, cap = 4, 2, 3
+    cache = qs.Cache(B, H, cap)
+    qs.qs_state_reset(cache)
+    bad = np.zeros((B, qs.STATE_WORDS), np.int32)
+    bad[:, :4] = [[-5, 300, -2, 7], [99, -1, 5, 1], [2, 1000, 1000, 0], [1 << 30, 128, -3, 3]]
+    cache.state.copy_(torch.from_numpy(bad))
+    mask = torch.zeros(B, dtype=torch.uint8, device="cuda")
+    qs.qs_need_flush(cache, 1, mask)
+    qs.qs_quantize_flush(cache, mask)
+    k1, v1 = h16(rng, (B, H, 1, 128)), h16(rng, (B, H, 1, 128))
+    qs.qs_buffer_append(cache, to_dev(torch, k1), to_dev(torch, v1))
+    qs.qs_buffer_rollback(cache, to_dev(torch, np.zeros(B, np.int32)))
+    q = h16(rng, (B, H, 1, 128))
+    for mode in (DRAFT, VERIFY):
+        got, gl = run_attn(torch, cache, mode, q)  # also checks the segment counters
+        assert np.all(np.isfinite(got))
+    errs = qs.qs_get_errors(cache)
+    assert np.all(errs != 0), errs
+    assert errs[0] & qs.DEV_OVERFLOW and errs[1] & qs.DEV_NQ_GT_FILL
+    assert errs[2] & qs.DEV_FLUSH_UNCOMMITTED and errs[3] & qs.DEV_OVER_ROLLBACK
+    # recovery: an emptied cache runs a normal append + attention
+    qs.qs_state_reset(cache)
+    oc = oracle.OracleCache(B, H, 128, 128, cap)
+    k, v = h16(rng, (B, H, 40, 128)), h16(rng, (B, H, 40, 128))
+    qs.qs_buffer_append(cache, to_dev(torch, k), to_dev(torch, v))
+    oc.append(k, v)
+    got, gl = run_attn(torch, cache, VERIFY, q)
+    ref, rl = oc.attn(q, upper_only=False)
+    assert_close(got, ref, gl, rl, "after reset")
+    assert np.all(qs.qs_get_errors(cache) == 0)
+
+
 def test_host_argument_errors(torch):
     cache = qs.Cache(1, 1, 1)
     with pytest.raises(qs.QsError) as e:
