@@ -131,3 +131,22 @@ def test_prefill_and_spec_accept_host_validation(L):
     a = list(args)
     a[3] = ctypes.c_void_p(0x20002)
     assert f(*a) == qs.QS_ERR_ALIGN
+
+
+def test_header_is_plain_c_and_links(L, tmp_path):
+    """include/qs.h compiled as C11 by gcc; the program links against the
+    library and calls its pure host functions (no GPU needed)."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    libdir = os.path.dirname(qs.LIB_PATH)
+    exe = str(tmp_path / "abi_check")
+    subprocess.run([gcc, "-std=c11", "-Wall", "-Werror", "-pedantic",
+                    "-I" + os.path.join(root, "include"),
+                    os.path.join(root, "tests", "abi_check.c"), "-L" + libdir, "-lqs",
+                    "-Wl,-rpath," + libdir, "-o", exe], check=True)
+    out = subprocess.run([exe], capture_output=True, text=True)
+    assert out.returncode == 0 and out.stdout.strip() == "abi ok", (out.returncode, out.stdout)
