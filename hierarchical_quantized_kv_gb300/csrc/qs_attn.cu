@@ -1,6 +1,7 @@
 // qs_attn.cu -- split-KV decode attention over the hierarchical quantized KV
-// cache (draft: C_U only; verify: INT8 = 16 C_U + C_L) plus the fp16 buffer,
-// with the log-sum-exp combine of the splits in the same kernel.
+// cache (draft: C_U only, or C_U2 in the two-bit layout; verify: INT8 =
+// 16 C_U + C_L) plus the fp16 buffer, with the log-sum-exp combine of the
+// splits in the same kernel.
 //
 // Sources: "QuantSpec Guide: Self-Speculative Decoding & Quantized KV",
 // "1. Hierarchical Two-Level Quantization with Bit-Sharing" (draft loads only
@@ -18,15 +19,16 @@
 //  * Each unit's contiguous plane blocks arrive by bulk async copies
 //    (cp.async.bulk, TMA engine) in a ring of shared-memory stages guarded by
 //    mbarriers; draft units copy only the C_U planes (8 KB keys + 8 KB values
-//    + 1 KB scales/zeros).  There is no producer warp: the last warp to finish
+//    + 1 KB scales/zeros; 4 + 4 + 1 KB for the two-bit draft).  There is no
+//    producer warp: the last warp to finish
 //    with a stage (a shared-memory arrival counter) issues its refill, so all
 //    twelve warps compute.
 //  * Warps claim half-units (64 tokens of a group) from a shared counter, so
 //    the SM's warps finish together; per-unit fixed costs amortize over 64
-//    tokens.  Nibbles become
-//    exact fp16 integers in registers (bit tricks, no conversion
-//    instructions), and the dense contractions q.K^T and P.V run on
-//    m16n8k16 tensor-core MMAs with fp32 accumulation.  Scales are folded:
+//    tokens.  Codes become subnormal fp16 operands (code * 2^-24) by masks
+//    and byte permutes, no conversion instructions, and the dense
+//    contractions q.K^T and P.V run on m16n8k16 tensor-core MMAs with fp32
+//    accumulation (the 2^-24 returns in the fp32 scales).  Scales are folded:
 //    B = q * s_K per channel, P' = p * s_V per token, zero-point terms as
 //    per-query biases, so the inner loops touch codes only.
 //  * Each warp keeps its own online softmax and writes one partial per piece
