@@ -12,7 +12,8 @@
 // works with Flash Decoding: split-KV partial softmax, then an LSE combine).
 //
 // Design (GB300):
-//  * One persistent CTA of twelve warps per SM.  All (sequence, head)
+//  * One persistent CTA of twelve warps per SM (eight for a verify tile of
+//    at most 16 rows).  All (sequence, head)
 //    segments are laid end to end as units (a quantized group of 128 tokens,
 //    or a chunk of fp16 buffer tokens) and every CTA takes an equal
 //    contiguous range, so ragged batches balance without a host round trip.
@@ -46,8 +47,13 @@ namespace {
 constexpr int kPairs = 6;               // units in compute at once (two half-units each)
 constexpr int kMaxR = 24;              // query rows per KV head (three column groups of 8)
 constexpr int kWarps = 2 * kPairs;
-constexpr int kThreads = kWarps * 32;  // one CTA per SM
-constexpr int kVerifyWarps = 8;        // warps that compute a verify tile of <= 16 rows
+// A verify tile of at most 16 rows (one or two column groups) runs with
+// eight warps: its ring (six stages of 34 KB, all the shared memory) then
+// holds four units in compute and two in flight instead of six in compute
+// and none in flight, and 256 threads may hold 255 registers each, so the
+// five-query tile does not spill (32k: 63 against 71 µs per call; 128k:
+// 175 against 192).  Three column groups keep twelve warps (four per group).
+constexpr int kVerifyWarps = 8;
 constexpr int kTailRow = 272;  // padded fp16 row stride (bytes) of buffer tiles
 constexpr int kOffKU = 0, kOffVU = 8192, kOffMeta = 16384, kOffKL = 17408, kOffVL = 25600;
 
@@ -451,9 +457,9 @@ __device__ __forceinline__ float4 ld_part4(const float *p) {
   return v;
 }
 
-// CTA-wide: lanes hold four channels each; the twelve warps take jpr rows
-// at once (the smallest divisor of twelve >= R, or twelve in rounds) and
-// split the partials into 12 / jpr phases.  Each thread loads its partials
+// CTA-wide: lanes hold four channels each; the nw warps take jpr rows at
+// once (the smallest divisor of nw >= R, or nw in rounds) and split the
+// partials into nw / jpr phases.  Each thread loads its partials
 // four at a time, all four in flight before the first is used; the phases
 // then meet in `red` (384 x 6 floats of shared memory): the largest m first,
 // then one independent rescale per phase.  Row j's partials start at
@@ -463,11 +469,16 @@ __device__ __forceinline__ float4 ld_part4(const float *p) {
 // than the call.
 __device__ __noinline__ void merge_partials(const float *srcA, int cgA, int kstrideA, int nA,
                                             const float *srcB, int cgB, int kstrideB, int ns,
-                                            int R, const MergeOut &mo, float *red) {
+                                            int R, const MergeOut &mo, float *red, int nw) {
   constexpr int kBatch = 4;
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int jpr = R <= 4 ? R : (R <= 6 ? 6 : 12);  // rows at once
-  const int ph = kWarps / jpr, phase = w / jpr;
+  int jpr = nw;  // rows at once: the smallest divisor of nw that is >= min(R, nw)
+  for (int d = 1; d < nw; ++d)
+    if (nw % d == 0 && d >= min(R, nw)) {
+      jpr = d;
+      break;
+    }
+  const int ph = nw / jpr, phase = w / jpr;
   const int mo_off = R * kD;
 #pragma unroll 1
   for (int j = w % jpr; j - w % jpr < R; j += jpr) {  // rounds of jpr rows
@@ -617,8 +628,9 @@ __device__ __forceinline__ bool wait_issued(volatile int *issued, int i) {
 // so column 2j carries the hi part of B = q * s and column 2j + 1 the lo part
 // for query j = lane / 8 (thread column pair 2c, 2c + 1 = query c): one MMA
 // per k-block instead of two.
-template <int MODE, bool PK, int UB>
-__global__ void __launch_bounds__(kThreads, 1) split_kernel(const Params prm) {
+// NW: warps per CTA (12, or kVerifyWarps for a verify tile of <= 16 rows).
+template <int MODE, bool PK, int UB, int NW>
+__global__ void __launch_bounds__(NW * 32, 1) split_kernel(const Params prm) {
   using C = Cfg<MODE>;
   using L = Layout<MODE>;
   constexpr int TT = C::kTailTok, S = C::kStages;
@@ -667,9 +679,9 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const Params prm) {
     if (T.len[b] != 0) continue;
     const size_t nh = (size_t)c.H * R;
     uint4 *o = reinterpret_cast<uint4 *>(prm.out + (size_t)b * nh * kD);
-    for (size_t i = threadIdx.x; i < nh * (kD / 8); i += kThreads) o[i] = make_uint4(0, 0, 0, 0);
+    for (size_t i = threadIdx.x; i < nh * (kD / 8); i += (NW * 32)) o[i] = make_uint4(0, 0, 0, 0);
     if (prm.lse)
-      for (size_t i = threadIdx.x; i < nh; i += kThreads) prm.lse[(size_t)b * nh + i] = -INFINITY;
+      for (size_t i = threadIdx.x; i < nh; i += (NW * 32)) prm.lse[(size_t)b * nh + i] = -INFINITY;
     if (threadIdx.x == 0) atomicOr(&c.state[(size_t)b * QS_STATE_WORDS + QS_ST_ERR], QS_DEV_NQ_GT_FILL);
   }
 
@@ -681,14 +693,14 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const Params prm) {
   lastseg.seek(x1 - 1, T, c.B);
   const int ord_first = first.ord, ord_last = lastseg.ord;
   // partial slot of warp ww for the piece of segment ordinal o
-  auto slot = [&](int o, int ww) { return prm.ws + ((size_t)(o + p) * kWarps + ww) * stride; };
+  auto slot = [&](int o, int ww) { return prm.ws + ((size_t)(o + p) * NW + ww) * stride; };
   // A segment split across CTAs p_lo..p_hi is finished by whichever CTA
   // arrives last on its counter.  CTAs p_lo..p_hi-1 hold it as their last
   // piece and arrive with one merged CTA partial at the end.  CTA p_hi holds
   // it as its first piece; when its range goes on past the segment it does
   // not merge it at all: the warp that leaves the piece last arrives for the
-  // CTA (the twelve warp partials are all written and fenced by then), and
-  // the finishing CTA reads those twelve partials directly.
+  // CTA (its NW warp partials are all written and fenced by then), and
+  // the finishing CTA reads those partials directly.
   const bool shared_first = ord_first != ord_last && first.s0 < x0;
   auto leave = [&](int o) {
     if (!shared_first || o != ord_first) return;
@@ -698,7 +710,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const Params prm) {
     __syncwarp();
     __threadfence_block();
     int last = 0;
-    if (lane == 0) last = atomicAdd(&s_left_first, 1) == kWarps - 1;
+    if (lane == 0) last = atomicAdd(&s_left_first, 1) == NW - 1;
     if (!__shfl_sync(0xffffffffu, last, 0)) return;
     __threadfence();
     const long long seg = (long long)first.b * c.H + first.h;
@@ -740,17 +752,11 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const Params prm) {
   // one ahead, so the atomic's latency hides behind a unit's compute; verify,
   // whose ring holds only as many units as are in compute, claims when free
   // (a claim made ahead would wait on a copy that cannot start yet).
-  // Verify with at most two column groups computes on kVerifyWarps of the
-  // twelve warps: its ring (six stages of 34 KB) then holds four units in
-  // compute and two in flight instead of six in compute and none in flight
-  // (128k: 188 against 196 µs per call).  The other warps only take part in
-  // the merges.  Three column groups keep all twelve (four warps per group).
   constexpr bool kAhead = MODE == QS_DRAFT_UPPER4;
-  const bool idle = MODE == QS_VERIFY_INT8 && ncg <= 2 && w >= kVerifyWarps;
   auto claim = [&]() {
     int h = 0;
     if (lane == 0)
-      h = (idle || *reinterpret_cast<volatile int *>(&s_abort)) ? 2 * n : atomicAdd(&s_next[cg], 1);
+      h = *reinterpret_cast<volatile int *>(&s_abort) ? 2 * n : atomicAdd(&s_next[cg], 1);
     return __shfl_sync(0xffffffffu, h, 0);
   };
   int h_next = kAhead ? claim() : 0;
@@ -1143,7 +1149,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const Params prm) {
   __syncthreads();
 
   // ---- log-sum-exp merge.  Per piece of this CTA's range (but a shared
-  // first piece, see above): merge the twelve warp partials (the last piece's
+  // first piece, see above): merge the NW warp partials (the last piece's
   // straight from registers through shared memory); a segment that lies
   // wholly in the range is final here.  A segment shared with other CTAs gets
   // one CTA partial (in warp slot 0) and an arrival on its counter; the CTA
@@ -1152,7 +1158,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const Params prm) {
   // shared.
   const bool aborted = s_abort != 0;
   float *red = reinterpret_cast<float *>(smem);                 // stage memory, free now
-  float *last_part = reinterpret_cast<float *>(smem + 16384);  // kWarps partials
+  float *last_part = reinterpret_cast<float *>(smem + 16384);  // NW partials
   if (cur_ord == ord_last) write_partial(sm, Centre<MODE, UB>::kScale, last_part + w * stride, R, cg, lane);
   else write_empty(last_part + w * stride, R, cg, lane);
   __syncthreads();
@@ -1162,8 +1168,8 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const Params prm) {
     const int plo = cta_of(first.s0, U, prm.P);
     const MergeOut fo{true, prm.out + (size_t)seg * R * kD,
                       prm.lse ? prm.lse + (size_t)seg * R : nullptr, nullptr};
-    merge_partials(prm.ws + (size_t)(ord_first + plo) * kWarps * stride, 0, kWarps * stride, p - plo,
-                   slot(ord_first, 0), stride, ncg * stride, p - plo + kWarps / ncg, R, fo, red);
+    merge_partials(prm.ws + (size_t)(ord_first + plo) * NW * stride, 0, NW * stride, p - plo,
+                   slot(ord_first, 0), stride, ncg * stride, p - plo + NW / ncg, R, fo, red, NW);
   }
   int n_arr = 0;
   {
@@ -1178,7 +1184,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const Params prm) {
                         prm.lse ? prm.lse + (size_t)seg * R : nullptr, slot(pc.ord, 0)};
       if (!aborted)
         merge_partials(pc.ord == ord_last ? last_part : slot(pc.ord, 0), stride, ncg * stride,
-                       kWarps / ncg, nullptr, 0, 0, kWarps / ncg, R, mo, red);
+                       NW / ncg, nullptr, 0, 0, NW / ncg, R, mo, red, NW);
       if (plo != phi) {
         if (threadIdx.x == 0) {
           s_seg[n_arr] = (int)seg;
@@ -1212,38 +1218,38 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const Params prm) {
     const MergeOut mo{true, prm.out + (size_t)seg * R * kD,
                       prm.lse ? prm.lse + (size_t)seg * R : nullptr, nullptr};
     // CTA pp's partial of this segment is in its warp slot 0, except that
-    // CTA p_hi left its twelve warp partials when the segment was only the
+    // CTA p_hi left its NW warp partials when the segment was only the
     // first piece of its range
     const bool raw = S0 < range_lo(phi, U, prm.P) && E0 < range_lo(phi + 1, U, prm.P);
-    const float *cta0 = prm.ws + ((size_t)(s_ord[a] + plo) * kWarps) * stride;
-    const float *raw0 = prm.ws + ((size_t)(s_ord[a] + phi) * kWarps) * stride;
+    const float *cta0 = prm.ws + ((size_t)(s_ord[a] + plo) * NW) * stride;
+    const float *raw0 = prm.ws + ((size_t)(s_ord[a] + phi) * NW) * stride;
     const int nA = raw ? phi - plo : phi - plo + 1;
-    merge_partials(cta0, 0, kWarps * stride, nA, raw0, stride, ncg * stride,
-                   nA + (raw ? kWarps / ncg : 0), R, mo, red);
+    merge_partials(cta0, 0, NW * stride, nA, raw0, stride, ncg * stride,
+                   nA + (raw ? NW / ncg : 0), R, mo, red, NW);
   }
 }
 
 // --------------------------------------------------------------- host side
 struct DevInfo {
-  int ready[8];
-  int grid[8];
+  int ready[16];
+  int grid[16];
 };
 DevInfo g_dev[64];
 
 // Resident CTAs of one split-kernel variant on a device (set up once).
-template <int MODE, bool PK, int UB>
+template <int MODE, bool PK, int UB, int NW>
 qs_status grid_for_device(int dev, int &P) {
   DevInfo &di = g_dev[dev];
-  constexpr int v = 2 * MODE + (PK ? 1 : 0) + (UB == 2 ? 4 : 0);
+  constexpr int v = 2 * MODE + (PK ? 1 : 0) + (UB == 2 ? 4 : 0) + (NW == 8 ? 8 : 0);
   if (!__atomic_load_n(&di.ready[v], __ATOMIC_ACQUIRE)) {
     const int smem = Layout<MODE>::kSmemBytes;
-    if (cudaFuncSetAttribute(split_kernel<MODE, PK, UB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(split_kernel<MODE, PK, UB, NW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              smem) != cudaSuccess)
       return QS_ERR_CUDA;
     int sms = 0, occ = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       return QS_ERR_CUDA;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, split_kernel<MODE, PK, UB>, kThreads,
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, split_kernel<MODE, PK, UB, NW>, NW * 32,
                                                       smem) != cudaSuccess)
       return QS_ERR_CUDA;
     if (occ < 1) return QS_ERR_CUDA;
@@ -1255,37 +1261,41 @@ qs_status grid_for_device(int dev, int &P) {
 }
 
 template <int UB>
-qs_status grid_size_ub(int dev, qs_mode mode, bool packed, int &P) {
+qs_status grid_size_ub(int dev, qs_mode mode, bool packed, int ncg, int &P) {
   if (mode == QS_DRAFT_UPPER4)
-    return packed ? grid_for_device<QS_DRAFT_UPPER4, true, UB>(dev, P)
-                  : grid_for_device<QS_DRAFT_UPPER4, false, UB>(dev, P);
-  return grid_for_device<QS_VERIFY_INT8, false, UB>(dev, P);
+    return packed ? grid_for_device<QS_DRAFT_UPPER4, true, UB, kWarps>(dev, P)
+                  : grid_for_device<QS_DRAFT_UPPER4, false, UB, kWarps>(dev, P);
+  return ncg <= 2 ? grid_for_device<QS_VERIFY_INT8, false, UB, kVerifyWarps>(dev, P)
+                  : grid_for_device<QS_VERIFY_INT8, false, UB, kWarps>(dev, P);
 }
 
-qs_status grid_size(qs_mode mode, bool packed, int upper_bits, int &P) {
+qs_status grid_size(qs_mode mode, bool packed, int upper_bits, int ncg, int &P) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return QS_ERR_CUDA;
   if (dev < 0 || dev >= 64) return QS_ERR_UNSUPPORTED;
-  return upper_bits == 2 ? grid_size_ub<2>(dev, mode, packed, P)
-                         : grid_size_ub<4>(dev, mode, packed, P);
+  return upper_bits == 2 ? grid_size_ub<2>(dev, mode, packed, ncg, P)
+                         : grid_size_ub<4>(dev, mode, packed, ncg, P);
 }
 
-// Workspace: (P + B H) x 12 warp slots of R rows (R = group x n_q).
+// Workspace: (P + B H) x 12 warp slots of R rows (R = group x n_q); an
+// eight-warp launch packs its pieces eight slots apart, inside that size.
 size_t ws_bytes(int P, int B, int H, int R) {
   return (size_t)(P + (size_t)B * H) * kWarps * (size_t)(R * kD + 2 * kMaxR) * sizeof(float);
 }
 
-template <int MODE, bool PK, int UB>
+template <int MODE, bool PK, int UB, int NW>
 qs_status launch(const Params &prm, cudaStream_t s) {
-  return launch_pdl(split_kernel<MODE, PK, UB>, dim3(prm.P), dim3(kThreads),
+  return launch_pdl(split_kernel<MODE, PK, UB, NW>, dim3(prm.P), dim3(NW * 32),
                     Layout<MODE>::kSmemBytes, s, prm);
 }
 
 template <int UB>
 qs_status launch_ub(qs_mode mode, bool packed, const Params &prm, cudaStream_t st) {
-  if (mode == QS_VERIFY_INT8) return launch<QS_VERIFY_INT8, false, UB>(prm, st);
-  return packed ? launch<QS_DRAFT_UPPER4, true, UB>(prm, st)
-                : launch<QS_DRAFT_UPPER4, false, UB>(prm, st);
+  if (mode == QS_VERIFY_INT8)
+    return prm.ncg <= 2 ? launch<QS_VERIFY_INT8, false, UB, kVerifyWarps>(prm, st)
+                        : launch<QS_VERIFY_INT8, false, UB, kWarps>(prm, st);
+  return packed ? launch<QS_DRAFT_UPPER4, true, UB, kWarps>(prm, st)
+                : launch<QS_DRAFT_UPPER4, false, UB, kWarps>(prm, st);
 }
 
 }  // namespace
@@ -1301,9 +1311,9 @@ qs_status qs_attn_workspace_size_gqa(const qs_cache *c, int32_t n_q, int32_t gro
   if (s != QS_OK) return s;
   if (!bytes || n_q < 1 || n_q > kMaxQ || group < 1 || group * n_q > kMaxR) return QS_ERR_ARG;
   int P0 = 0, P1 = 0, P2 = 0;
-  if ((s = grid_size(QS_DRAFT_UPPER4, false, c->upper_bits, P0)) != QS_OK) return s;
-  if ((s = grid_size(QS_DRAFT_UPPER4, true, c->upper_bits, P1)) != QS_OK) return s;
-  if ((s = grid_size(QS_VERIFY_INT8, false, c->upper_bits, P2)) != QS_OK) return s;
+  if ((s = grid_size(QS_DRAFT_UPPER4, false, c->upper_bits, 1, P0)) != QS_OK) return s;
+  if ((s = grid_size(QS_DRAFT_UPPER4, true, c->upper_bits, 1, P1)) != QS_OK) return s;
+  if ((s = grid_size(QS_VERIFY_INT8, false, c->upper_bits, (group * n_q + 7) / 8, P2)) != QS_OK) return s;
   const int P = P0 > P1 ? (P0 > P2 ? P0 : P2) : (P1 > P2 ? P1 : P2);
   *bytes = ws_bytes(P, c->B, c->H, group * n_q);
   return QS_OK;
@@ -1332,7 +1342,7 @@ qs_status qs_attn_decode_gqa(const qs_cache *c, qs_mode mode, const uint16_t *q,
   prm.ncg = (prm.R + 7) / 8;
   prm.sl2 = softmax_scale * 1.4426950408889634f;
   const bool packed = (mode == QS_DRAFT_UPPER4 && prm.R == 1);
-  if ((s = grid_size(mode, packed, c->upper_bits, prm.P)) != QS_OK) return s;
+  if ((s = grid_size(mode, packed, c->upper_bits, prm.ncg, prm.P)) != QS_OK) return s;
   if (!workspace || !aligned16(workspace) ||
       workspace_bytes < ws_bytes(prm.P, c->B, c->H, prm.R))
     return QS_ERR_WORKSPACE;
