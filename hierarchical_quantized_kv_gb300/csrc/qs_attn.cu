@@ -583,11 +583,13 @@ __device__ __noinline__ void merge_partials(const float *srcA, int cgA, int kstr
 // [8 cg, 8 cg + 8) of R, O at row * 128 + d, m at R * 128 + row, l at
 // R * 128 + 24 + row; dst is in global or shared memory.
 __device__ __forceinline__ void write_partial(const Softmax &sm, float oscale, float *dst, int R,
-                                              int cg, int lane) {
+                                              int cg, int lane, bool pk) {
   const int r = lane >> 2, cq = lane & 3;
   const float l0 = warp_sum8(sm.l[0]), l1 = warp_sum8(sm.l[1]);
   const float v0 = warp_sum8(sm.bv[0]), v1 = warp_sum8(sm.bv[1]);
-  const int j0 = 8 * cg + 2 * cq, j1 = j0 + 1;
+  // the thread's columns 2 cq, 2 cq + 1: rows 8 cg + 2 cq and the next, or
+  // packed, row cq alone (its hi and lo columns)
+  const int j0 = pk ? cq : 8 * cg + 2 * cq, j1 = pk ? R : j0 + 1;
 #pragma unroll
   for (int md = 0; md < 8; ++md) {
 #pragma unroll
@@ -624,10 +626,11 @@ __device__ __forceinline__ bool wait_issued(volatile int *issued, int i) {
   return true;
 }
 
-// PK (draft, one query): the MMA's eight query columns hold one real query,
-// so column 2j carries the hi part of B = q * s and column 2j + 1 the lo part
-// for query j = lane / 8 (thread column pair 2c, 2c + 1 = query c): one MMA
-// per k-block instead of two.
+// PK (draft, R <= 4 query rows): the MMA's eight columns hold four query
+// rows, column 2j the hi part of B = q * s and column 2j + 1 the lo part of
+// row j (B column r = lane / 4 reads row r / 2; thread column pair 2c, 2c + 1
+// = row c): one MMA per k-block instead of two, and one softmax column per
+// thread.
 // NW: warps per CTA (12, or kVerifyWarps for a verify tile of <= 16 rows).
 template <int MODE, bool PK, int UB, int NW>
 __global__ void __launch_bounds__(NW * 32, 1) split_kernel(const Params prm) {
@@ -770,7 +773,7 @@ __global__ void __launch_bounds__(NW * 32, 1) split_kernel(const Params prm) {
       // a new piece: the finished one's partial (empty ones for pieces this
       // warp skipped), then fresh state and this head's queries
       if (cur_ord >= 0) {
-        write_partial(sm, Centre<MODE, UB>::kScale, slot(cur_ord, w), R, cg, lane);
+        write_partial(sm, Centre<MODE, UB>::kScale, slot(cur_ord, w), R, cg, lane, PK);
         leave(cur_ord);
       }
       for (int o = cur_ord >= 0 ? cur_ord + 1 : ord_first; o < cur.ord; ++o) {
@@ -953,10 +956,10 @@ __global__ void __launch_bounds__(NW * 32, 1) split_kernel(const Params prm) {
               sm.l[1] += pb;
               sm.bv[0] = fmaf(pa, zv, sm.bv[0]);
               sm.bv[1] = fmaf(pb, zv, sm.bv[1]);
-              // PK: thread column pair (2c, 2c+1) = queries (2c, 2c+1) of the
-              // P' matrix; only c = 0 holds the one real query
+              // PK: P' column 2c holds row c (c < R), column 2c + 1 (the lo
+              // column of the scores) stays zero (pb = 0)
               const float svp = (MODE == QS_DRAFT_UPPER4 && hh) ? sv * 0.0625f : sv;
-              pv[2 * hh] = (PK && cq != 0) ? 0.f : pa * svp;
+              pv[2 * hh] = (PK && cq >= R) ? 0.f : pa * svp;
               pv[2 * hh + 1] = pb * svp;
             }
             bp0[mt] = movmatrix_trans(pack_half2(pv[0], pv[1]));
@@ -1075,7 +1078,7 @@ __global__ void __launch_bounds__(NW * 32, 1) split_kernel(const Params prm) {
             float pv[4];
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-              pv[k] = (PK && cq != 0) ? 0.f : fast_exp2(sv[tl][k] - ((k & 1) ? u1 : u0));
+              pv[k] = (PK && cq >= R) ? 0.f : fast_exp2(sv[tl][k] - ((k & 1) ? u1 : u0));
               sm.l[k & 1] += pv[k];
             }
             bq0[tl] = movmatrix_trans(pack_half2(pv[0], pv[1]));
@@ -1125,7 +1128,7 @@ __global__ void __launch_bounds__(NW * 32, 1) split_kernel(const Params prm) {
   // this warp's partials for the pieces after its last unit's piece are empty
   // (all but the range's last piece go to the workspace)
   if (cur_ord >= 0 && cur_ord < ord_last) {
-    write_partial(sm, Centre<MODE, UB>::kScale, slot(cur_ord, w), R, cg, lane);
+    write_partial(sm, Centre<MODE, UB>::kScale, slot(cur_ord, w), R, cg, lane, PK);
     leave(cur_ord);
   }
   for (int o = cur_ord >= 0 ? cur_ord + 1 : ord_first; o < ord_last; ++o) {
@@ -1159,7 +1162,7 @@ __global__ void __launch_bounds__(NW * 32, 1) split_kernel(const Params prm) {
   const bool aborted = s_abort != 0;
   float *red = reinterpret_cast<float *>(smem);                 // stage memory, free now
   float *last_part = reinterpret_cast<float *>(smem + 16384);  // NW partials
-  if (cur_ord == ord_last) write_partial(sm, Centre<MODE, UB>::kScale, last_part + w * stride, R, cg, lane);
+  if (cur_ord == ord_last) write_partial(sm, Centre<MODE, UB>::kScale, last_part + w * stride, R, cg, lane, PK);
   else write_empty(last_part + w * stride, R, cg, lane);
   __syncthreads();
   if (s_first_fin && !aborted) {
@@ -1341,7 +1344,7 @@ qs_status qs_attn_decode_gqa(const qs_cache *c, qs_mode mode, const uint16_t *q,
   prm.R = group * n_q;
   prm.ncg = (prm.R + 7) / 8;
   prm.sl2 = softmax_scale * 1.4426950408889634f;
-  const bool packed = (mode == QS_DRAFT_UPPER4 && prm.R == 1);
+  const bool packed = (mode == QS_DRAFT_UPPER4 && prm.R <= 4);
   if ((s = grid_size(mode, packed, c->upper_bits, prm.ncg, prm.P)) != QS_OK) return s;
   if (!workspace || !aligned16(workspace) ||
       workspace_bytes < ws_bytes(prm.P, c->B, c->H, prm.R))
