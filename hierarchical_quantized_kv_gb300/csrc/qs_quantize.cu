@@ -51,13 +51,18 @@ __device__ __forceinline__ void scale_zero(float mn, float mx, uint16_t &s_bits,
 // every |u| < 256 (u <= 255 (1 + 2^-23) since s >= r / 255).  Both round to
 // the same integer unless u' lies within 2^-12 of a half-integer; there the
 // exact quotient decides (about one element in 2^11).
+// Called by whole warps (the vote): the exact quotient is computed only
+// when some lane of the warp is that close to a tie, and rounding, clamping
+// to [0, 255] and conversion are one saturating conversion.  A zero scale
+// gives code 0 (then rf is +inf and a is 0 or positive: the code is forced).
 __device__ __forceinline__ uint32_t code_of(float x, float zf, float sf, float rf) {
-  if (sf == 0.0f) return 0;
   const float a = __fsub_rn(x, zf);
-  const float ue = __fmul_rn(a, rf);
-  float k = rintf(ue);
-  if (fabsf(__fsub_rn(ue, k)) > 0.5f - 0x1p-12f) k = rintf(__fdiv_rn(a, sf));
-  return (uint32_t)min(max((int)k, 0), 255);
+  float ue = __fmul_rn(a, rf);
+  const bool near = fabsf(__fsub_rn(ue, rintf(ue))) > 0.5f - 0x1p-12f;
+  if (__any_sync(0xffffffffu, near) && near) ue = __fdiv_rn(a, sf);
+  uint32_t q;
+  asm("cvt.rni.sat.u8.f32 %0, %1;" : "=r"(q) : "f"(ue));
+  return sf == 0.0f ? 0u : q;
 }
 
 // Token held by nibble position p of a 16-byte value row (quarter layout).
