@@ -20,15 +20,21 @@ namespace {
 
 constexpr int kParts = 4;           // CTAs per (head, sequence)
 constexpr int kSlice = kD / kParts;  // key channels / value tokens per CTA
+// Warps per CTA: a flush is one wave of small CTAs, so its time is one
+// CTA's chain of phases, and sixteen warps halve the per-thread work of
+// every phase but the packing (flush 14 -> 11.5 µs); a prefill is many
+// waves, where eight warps keep more CTAs resident (379 against 426 µs).
+constexpr int kFlushWarps = 16, kPrefillWarps = 8;
 
 // One CTA owns key channels [32p, 32p+32) (one 16-byte column of every key
 // row) and value tokens [32p, 32p+32) (value quarter p).
+template <int QW>
 struct FlushSmem {
   __half k[kG][kSlice];     // keys of the slice   [token][channel - 32p]
   __half v[kSlice][kD];     // values of the slice [token - 32p][channel]
   uint8_t kc[kG][kSlice];   // key codes
   uint8_t vc[kSlice][kD];   // value codes
-  float kmin[8][kSlice], kmax[8][kSlice];
+  float kmin[QW][kSlice], kmax[QW][kSlice];
   uint16_t ks[kSlice], kz[kSlice], vs[kSlice], vz[kSlice];
   int act, base, g;
 };
@@ -103,25 +109,28 @@ __device__ __forceinline__ void store_upper2(uint8_t *base, size_t off, const ui
 // One CTA's share of quantizing a group of G tokens whose fp16 key and value
 // rows (D channels each, row stride D) start at gk and gv: key channels
 // [32 part, 32 part + 32) and value tokens [32 part, 32 part + 32), written
-// as group `grp` (index into the [B][H][cap] group arrays).  256 threads.
-__device__ void quantize_part(FlushSmem &S, const __half *gk, const __half *gv, const qs_cache &c,
-                              size_t grp, int part, int tid) {
+// as group `grp` (index into the [B][H][cap] group arrays).  32 QW threads.
+template <int QW>
+__device__ void quantize_part(FlushSmem<QW> &S, const __half *gk, const __half *gv,
+                              const qs_cache &c, size_t grp, int part, int tid) {
+  constexpr int kQWarps = QW, kQThreads = 32 * QW;
   const int warp = tid >> 5, lane = tid & 31;
   // 1. loads: the key column slice (64 B of each of 128 rows), 32 value rows
-  for (int e = tid; e < kG * 4; e += 256) {  // 4 x 16 B per key row
+  for (int e = tid; e < kG * 4; e += kQThreads) {  // 4 x 16 B per key row
     const int t = e >> 2, q = e & 3;
     reinterpret_cast<uint4 *>(&S.k[t][0])[q] =
         reinterpret_cast<const uint4 *>(gk + (size_t)t * kD + part * kSlice)[q];
   }
-  for (int e = tid; e < kSlice * kD / 8; e += 256)
+  for (int e = tid; e < kSlice * kD / 8; e += kQThreads)
     reinterpret_cast<uint4 *>(&S.v[0][0])[e] =
         reinterpret_cast<const uint4 *>(gv + (size_t)part * kSlice * kD)[e];
   __syncthreads();
 
-  // 2. keys: min / max per channel, warp w over tokens 16w..16w+15
+  // 2. keys: min / max per channel, warp w over tokens kG/kQWarps w onwards
   {
+    constexpr int kTw = kG / kQWarps;
     float mn = INFINITY, mx = -INFINITY;
-    for (int t = 16 * warp; t < 16 * warp + 16; ++t) {
+    for (int t = kTw * warp; t < kTw * warp + kTw; ++t) {
       const float x = __half2float(S.k[t][lane]);
       mn = fminf(mn, x);
       mx = fmaxf(mx, x);
@@ -130,7 +139,7 @@ __device__ void quantize_part(FlushSmem &S, const __half *gk, const __half *gv, 
     S.kmax[warp][lane] = mx;
   }
   // 3. values: one warp per token, min / max over the 128 channels, codes
-  for (int t = warp; t < kSlice; t += 8) {
+  for (int t = warp; t < kSlice; t += kQWarps) {
     const __half2 *row = reinterpret_cast<const __half2 *>(&S.v[t][4 * lane]);
     const float2 a = __half22float2(row[0]), bb = __half22float2(row[1]);
     float mn = fminf(fminf(a.x, a.y), fminf(bb.x, bb.y));
@@ -154,7 +163,7 @@ __device__ void quantize_part(FlushSmem &S, const __half *gk, const __half *gv, 
   __syncthreads();
   if (tid < kSlice) {
     float mn = S.kmin[0][tid], mx = S.kmax[0][tid];
-    for (int w = 1; w < 8; ++w) {
+    for (int w = 1; w < kQWarps; ++w) {
       mn = fminf(mn, S.kmin[w][tid]);
       mx = fmaxf(mx, S.kmax[w][tid]);
     }
@@ -166,15 +175,16 @@ __device__ void quantize_part(FlushSmem &S, const __half *gk, const __half *gv, 
   }
   __syncthreads();
 
-  // 4. key codes: thread = channel pair j (16 pairs) x 8 tokens
+  // 4. key codes: thread = channel pair j (16 pairs) x kTc tokens
   {
-    const int j = tid & 15, t0 = (tid >> 4) * 8;
+    constexpr int kTc = kG * 16 / kQThreads;
+    const int j = tid & 15, t0 = (tid >> 4) * kTc;
     const float s0 = __half2float(__ushort_as_half(S.ks[2 * j]));
     const float s1 = __half2float(__ushort_as_half(S.ks[2 * j + 1]));
     const float z0 = __half2float(__ushort_as_half(S.kz[2 * j]));
     const float z1 = __half2float(__ushort_as_half(S.kz[2 * j + 1]));
     const float r0 = __frcp_rn(s0), r1 = __frcp_rn(s1);
-    for (int t = t0; t < t0 + 8; ++t) {
+    for (int t = t0; t < t0 + kTc; ++t) {
       const float2 x = __half22float2(*reinterpret_cast<const __half2 *>(&S.k[t][2 * j]));
       const uint32_t q0 = code_of(x.x, z0, s0, r0), q1 = code_of(x.y, z1, s1, r1);
       *reinterpret_cast<uint16_t *>(&S.kc[t][2 * j]) = (uint16_t)(q0 | (q1 << 8));
@@ -198,7 +208,7 @@ __device__ void quantize_part(FlushSmem &S, const __half *gk, const __half *gv, 
           make_uint4(wu[0], wu[1], wu[2], wu[3]);
     reinterpret_cast<uint4 *>(c.k_lower + (grp * kG + tid) * (kD / 2))[part] =
         make_uint4(wl[0], wl[1], wl[2], wl[3]);
-  } else {
+  } else if (tid < kG + kD) {
     // 6. value quarter p: row d = 16 bytes, nibble position q holds token vperm(q)
     const int d = tid - kG;
     uint32_t wu[4] = {0, 0, 0, 0}, wl[4] = {0, 0, 0, 0};
@@ -228,9 +238,10 @@ __device__ void quantize_part(FlushSmem &S, const __half *gk, const __half *gv, 
 
 }  // namespace
 
-__global__ void __launch_bounds__(256) flush_kernel(qs_cache c, const uint8_t *__restrict__ mask) {
+__global__ void __launch_bounds__(32 * kFlushWarps)
+    flush_kernel(qs_cache c, const uint8_t *__restrict__ mask) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
-  FlushSmem &S = *reinterpret_cast<FlushSmem *>(smem_raw);
+  FlushSmem<kFlushWarps> &S = *reinterpret_cast<FlushSmem<kFlushWarps> *>(smem_raw);
   const int part = blockIdx.x, h = blockIdx.y, b = blockIdx.z, tid = threadIdx.x;
   pdl_trigger();
   pdl_wait();
@@ -277,11 +288,11 @@ __global__ void __launch_bounds__(256) flush_kernel(qs_cache c, const uint8_t *_
 // x / 4 (if the sequence has that group); the last two blocks copy buffer
 // halves 0 and 1.  The CTA that arrives last on the sequence's ticket writes
 // the counters, so every CTA reads the old (empty) ones first.
-__global__ void __launch_bounds__(256) prefill_kernel(qs_cache c, const uint16_t *__restrict__ k,
+__global__ void __launch_bounds__(32 * kPrefillWarps) prefill_kernel(qs_cache c, const uint16_t *__restrict__ k,
                                                      const uint16_t *__restrict__ v, int T,
                                                      const int32_t *__restrict__ len, int gmax) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
-  FlushSmem &S = *reinterpret_cast<FlushSmem *>(smem_raw);
+  FlushSmem<kPrefillWarps> &S = *reinterpret_cast<FlushSmem<kPrefillWarps> *>(smem_raw);
   const int x = blockIdx.x, h = blockIdx.y, b = blockIdx.z, tid = threadIdx.x;
   pdl_trigger();
   pdl_wait();
@@ -323,7 +334,7 @@ __global__ void __launch_bounds__(256) prefill_kernel(qs_cache c, const uint16_t
     const uint4 *vs = reinterpret_cast<const uint4 *>(vp + (size_t)ng * kG * kD);
     uint4 *kd = reinterpret_cast<uint4 *>(c.buf_k + bh * kRing * kD);
     uint4 *vd = reinterpret_cast<uint4 *>(c.buf_v + bh * kRing * kD);
-    for (int e = i0 * (kD / 8) + tid; e < i1 * (kD / 8); e += 256) {
+    for (int e = i0 * (kD / 8) + tid; e < i1 * (kD / 8); e += 32 * kPrefillWarps) {
       kd[e] = ks[e];
       vd[e] = vs[e];
     }
@@ -369,10 +380,10 @@ extern "C" qs_status qs_prefill(const qs_cache *c, const uint16_t *k, const uint
   if (s != QS_OK) return s;
   if (!k || !v || !d_len || T < 0 || T > (1 << 26)) return QS_ERR_ARG;
   if (!aligned16(k) || !aligned16(v)) return QS_ERR_ALIGN;
-  const int smem = (int)sizeof(FlushSmem);
+  const int smem = (int)sizeof(FlushSmem<kPrefillWarps>);
   if ((s = set_smem_once((const void *)prefill_kernel, smem, &g_prefill_ready)) != QS_OK) return s;
   const int gmax = T > 2 * kG ? (T - 2 * kG + kG - 1) / kG : 0;
-  return launch_pdl(prefill_kernel, dim3(4 * gmax + 2, c->H, c->B), dim3(256), smem,
+  return launch_pdl(prefill_kernel, dim3(4 * gmax + 2, c->H, c->B), dim3(32 * kPrefillWarps), smem,
                     (cudaStream_t)stream, *c, k, v, (int)T, d_len, gmax);
 }
 
@@ -380,8 +391,8 @@ extern "C" qs_status qs_quantize_flush(const qs_cache *c, const uint8_t *d_mask,
                                        qs_stream_t stream) {
   qs_status s = check_cache(c);
   if (s != QS_OK) return s;
-  const int smem = (int)sizeof(FlushSmem);
+  const int smem = (int)sizeof(FlushSmem<kFlushWarps>);
   if ((s = set_smem_once((const void *)flush_kernel, smem, &g_flush_ready)) != QS_OK) return s;
-  return launch_pdl(flush_kernel, dim3(kParts, c->H, c->B), dim3(256), smem, (cudaStream_t)stream,
-                    *c, d_mask);
+  return launch_pdl(flush_kernel, dim3(kParts, c->H, c->B), dim3(32 * kFlushWarps), smem,
+                    (cudaStream_t)stream, *c, d_mask);
 }
