@@ -103,7 +103,7 @@ def attn_bytes(ng, fill, n_q, mode_draft, BH, group=1, upper_bits=4):
     return BH * (ng * grp + fill * 512 + group * n_q * 256 * 2)
 
 
-FLUSH_BYTES_PER_HEAD = 2 * 128 * 256 + 4 * 8 * KB + KB   # read both halves' rows, write planes + meta
+FLUSH_BYTES_PER_HEAD = 2 * 128 * 256 + 4 * 8 * KB + KB   # read the oldest half (K, V), write planes + meta
 
 
 def append_bytes(n, BH):
