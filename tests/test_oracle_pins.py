@@ -370,6 +370,66 @@ def test_verify_attention_on_lossless_groups_equals_plain_attention():
             np.testing.assert_allclose(out[0, hh, j], ref, rtol=1e-11, atol=1e-12)
 
 
+def _dequantized_context(c, b, hh, upper_bits):
+    """Brute force, from the stored arrays alone: every quantized group
+    dequantized as s * code + z in fp64 (keys: scale and zero per channel;
+    values: per token), followed by the logical buffer tokens.  upper_bits:
+    None for the INT8 code, k for the k-bit draft (top k bits, low bits at
+    their middle)."""
+    ng = c.counters(b)["n_groups"]
+    ks, kz = f16(c.ks[b, hh, :ng]), f16(c.kz[b, hh, :ng])     # [ng, D]
+    vs, vz = f16(c.vs[b, hh, :ng]), f16(c.vz[b, hh, :ng])     # [ng, G]
+    kq = c.kq[b, hh, :ng].astype(np.int64)                   # [ng, G, D]
+    vq = c.vq[b, hh, :ng].astype(np.int64)
+    if upper_bits is not None:
+        low = 8 - upper_bits
+        kq = ((kq >> low) << low) + (1 << (low - 1))
+        vq = ((vq >> low) << low) + (1 << (low - 1))
+    K = ks[:, None, :] * kq + kz[:, None, :]
+    V = vs[:, :, None] * vq + vz[:, :, None]
+    bk, bv = c.buffer_tokens(b, hh)
+    K = np.concatenate([K.reshape(-1, c.D), f16(bk)])
+    V = np.concatenate([V.reshape(-1, c.D), f16(bv)])
+    return K, V
+
+
+@pytest.mark.parametrize("group", [1, 2])
+def test_attention_equals_brute_force_over_dequantized_groups(group):
+    """Random (lossy) groups: both modes, n_q of 1 and 5, ragged sequences and
+    a grouped-query layout, against textbook attention over the brute-force
+    dequantized context, with query j of n_q seeing the context up to its own
+    position."""
+    rng = np.random.default_rng(17 + group)
+    B, H, D, G = 2, 2, 128, 128
+    c = oracle.OracleCache(B, H, D, G, cap=4)
+    for n in (G, G, G, 77):
+        k = h(rng.standard_normal((B, H, n, D)) * rng.uniform(0.2, 3, (B, H, 1, D))
+              + rng.uniform(-2, 2, (B, H, 1, D)))
+        v = h(rng.standard_normal((B, H, n, D)))
+        c.flush(c.need_flush(n))
+        c.append(k, v)
+        c.rollback([0, n // 2])     # sequence 1 keeps half of each piece
+    c.flush([1, 0])                 # ragged: sequence 0 gains one more group
+    assert [c.counters(b)["n_groups"] for b in range(B)] == [3, 1]
+    assert [c.counters(b)["fill"] for b in range(B)] == [77, 103]
+    assert not c.state[:, oracle.ERR].any()
+    scale = 1 / np.sqrt(D)
+    for n_q in (1, 5):
+        q = h(rng.standard_normal((B, H * group, n_q, D)))
+        for ub in (None, 4, 2):
+            out, lse = c.attn(q, upper_only=ub is not None, scale=scale, group=group,
+                              upper_bits=ub or 4)
+            for b in range(B):
+                for qh in range(H * group):
+                    K, V = _dequantized_context(c, b, qh // group, ub)
+                    for j in range(n_q):
+                        last = len(K) - n_q + j
+                        ref, rl = naive_attention(q[b, qh, j].astype(np.float64), K[:last + 1],
+                                                  V[:last + 1], float(np.float32(scale)))
+                        np.testing.assert_allclose(out[b, qh, j], ref, rtol=1e-10, atol=1e-12)
+                        assert abs(lse[b, qh, j] - rl) < 1e-10
+
+
 def test_draft_equals_verify_when_every_lower_level_is_eight():
     rng = np.random.default_rng(12)
     H, D, G = 2, 128, 128
