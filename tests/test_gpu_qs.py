@@ -123,6 +123,123 @@ def test_buffer_and_flush_bit_exact(torch, seed):
     assert oc.state[:, oracle.N_GROUPS].sum() >= 4
 
 
+def _degenerate_line(p, n, rng, extreme):
+    """n fp16 values of pattern p: the groups QS-RN-v1 treats specially
+    (constant, signed zeros, two-valued, a range that gives a subnormal
+    scale, fp16 subnormal inputs, exact ties, the fp16 extremes, a single
+    outlier) and a few plain ones."""
+    E = 65504.0 if extreme else 3.0       # moderate: value rows stay O(1), so the
+    C = 60000.0 if extreme else 10.0      # fp16 rounding of p * s_V stays far inside 1e-2
+    W = 1e3 if extreme else 3.0
+    x = np.zeros(n)
+    if p == 0:
+        x[:] = 1.5
+    elif p == 1:
+        x[:] = 0.0
+    elif p == 2:
+        x[:] = -0.0
+    elif p == 3:
+        x[:] = np.where(np.arange(n) % 2 == 0, 0.0, -0.0)
+    elif p == 4:
+        x[:] = np.where(np.arange(n) % 2 == 0, -3.0, 7.0)
+    elif p == 5:
+        x[:] = np.where(np.arange(n) % 2 == 0, 1.0, 1.0 + 2.0 ** -10)
+    elif p == 6:
+        x[:] = rng.uniform(-E, E, n)
+        x[0], x[1] = -E, E
+    elif p == 7:
+        x[:] = rng.integers(-100, 101, n) * 2.0 ** -24
+    elif p == 8:   # s = 2^-6 exactly, every other code an exact tie
+        x[:] = (rng.integers(0, 255, n) + 0.5) * 2.0 ** -6
+        x[0], x[1] = 0.0, 255 * 2.0 ** -6
+    elif p == 9:
+        x[:] = C
+        x[5] = -C
+    elif p == 10:
+        x[17 % n] = 2.5
+    elif p == 11:
+        x[:] = rng.standard_normal(n) * 1e-3
+    elif p == 12:
+        x[:] = rng.standard_normal(n) * W
+    elif p == 13:
+        x[:] = rng.standard_normal(n) + 100.0
+    elif p == 14:
+        x[:] = rng.integers(0, 256, n) * 0.125
+        x[0], x[1] = 0.0, 255 * 0.125
+    else:
+        x[:] = rng.standard_normal(n)
+    return x.astype(np.float16)
+
+
+def _degenerate_tokens(rng, H, extreme):
+    """[1, H, 128, 128] keys and values whose groups are the degenerate
+    patterns: key channel d follows pattern d mod 16 over the 128 tokens,
+    value token t follows pattern t mod 16 over the 128 channels; head 1
+    negates head 0 (+0 becomes -0)."""
+    k = np.zeros((1, H, 128, 128), np.float16)
+    v = np.zeros_like(k)
+    for d in range(128):
+        k[0, 0, :, d] = _degenerate_line(d % 16, 128, rng, extreme)
+    for t in range(128):
+        v[0, 0, t, :] = _degenerate_line(t % 16, 128, rng, extreme)
+    for hh in range(1, H):
+        k[0, hh], v[0, hh] = -k[0, 0], -v[0, 0]
+    return k, v
+
+
+@pytest.mark.parametrize("extreme", [False, True])
+@pytest.mark.parametrize("ub", [4, 2])
+def test_degenerate_groups_bit_exact(torch, extreme, ub):
+    """Groups QS-RN-v1 treats specially, quantized by the flush (16-warp
+    CTAs) and by the prefill (8-warp CTAs): planes, scales and zeros bit for
+    bit against the oracle in both plane layouts; then attention over them
+    with moderate ranges.  With the fp16 extremes only the bytes are
+    compared: the value path rounds p * s_V to fp16, an absolute error that
+    grows with the value range, while the attention tolerance is absolute."""
+    rng = np.random.default_rng(41 + extreme)
+    H = 2
+    kd, vd = _degenerate_tokens(rng, H, extreme)
+    knew, vnew = h16(rng, (1, H, 256, 128), 2.0), h16(rng, (1, H, 256, 128))
+    k = np.concatenate([kd, knew], axis=2)
+    v = np.concatenate([vd, vnew], axis=2)
+    # flush path: the 128 degenerate tokens are the oldest half
+    cache = qs.Cache(1, H, 2, upper_bits=ub)
+    qs.qs_state_reset(cache)
+    oc = oracle.OracleCache(1, H, 128, 128, 2)
+    qs.qs_buffer_append(cache, to_dev(torch, k[:, :, :256]), to_dev(torch, v[:, :, :256]))
+    oc.append(k[:, :, :256], v[:, :, :256])
+    zero = to_dev(torch, np.zeros(1, np.int32))
+    qs.qs_buffer_rollback(cache, zero)
+    oc.rollback([0])
+    qs.qs_quantize_flush(cache, None)
+    oc.flush()
+    torch.cuda.synchronize()
+    assert oc.counters(0)["n_groups"] == 1
+    assert_state_equal(cache, oc, "flush of degenerate groups")
+    # the patterns do reach the special cases: zero scales and subnormal scales
+    ks = oc.ks[0, 0, 0].view(np.float16).astype(np.float64)
+    assert np.any(ks == 0) and np.any((ks > 0) & (ks < 2.0 ** -14))
+    # prefill path: 384 prompt tokens, group 0 is the degenerate half
+    pc = qs.Cache(1, H, 2, upper_bits=ub)
+    qs.qs_state_reset(pc)
+    op = oracle.OracleCache(1, H, 128, 128, 2)
+    lens = np.array([384], np.int32)
+    qs.qs_prefill(pc, to_dev(torch, k), to_dev(torch, v), to_dev(torch, lens))
+    op.prefill(k, v, lens)
+    torch.cuda.synchronize()
+    assert op.counters(0)["n_groups"] == 1
+    assert_state_equal(pc, op, "prefill of degenerate groups")
+    assert np.all(qs.qs_get_errors(cache) == 0) and np.all(qs.qs_get_errors(pc) == 0)
+    assert not oc.state[:, oracle.ERR].any() and not op.state[:, oracle.ERR].any()
+    if extreme:
+        return
+    for mode, n_q in ((DRAFT, 1), (VERIFY, 5)):
+        q = h16(rng, (1, H, n_q, 128))
+        got, gl = run_attn(torch, cache, mode, q)
+        ref, rl = oc.attn(q, upper_only=(mode == DRAFT), upper_bits=ub)
+        assert_close(got, ref, gl, rl, "degenerate groups, mode %d" % mode)
+
+
 def test_append_overflow_is_a_no_op(torch):
     rng = np.random.default_rng(5)
     cache = qs.Cache(2, 2, 2)
