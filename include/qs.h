@@ -31,9 +31,11 @@
  *   verify: deq = s * (16 C_U + C_L) + z,   draft: deq = s * (16 C_U + 8) + z.
  *
  * Ownership: every array is caller-owned device memory; the library never
- * allocates and keeps no global state.  Every call is asynchronous on the
- * given stream except qs_get_errors.  Calls on different caches may run
- * concurrently; calls on one cache must be ordered by the caller (one stream).
+ * allocates and keeps no global state, except the fixed scratch array behind
+ * qs_attn_decode_static_ws (see there).  Every call that launches work is
+ * asynchronous on the given stream, except qs_get_errors, which synchronizes
+ * it.  Calls on different caches may run concurrently; calls on one cache
+ * must be ordered by the caller (one stream).
  *
  * Host-side errors are returned as qs_status before anything is launched.
  * Preconditions that depend on device-resident counters (overflow, rollback
