@@ -132,8 +132,8 @@ enum { QS_META_K_SCALE = 0, QS_META_K_ZERO = 1, QS_META_V_SCALE = 2, QS_META_V_Z
  *          32*(p>>5) + ((p>>2)&7) + 16*((p>>1)&1) + 8*(p&1).
  *  With upper_bits = 2 (C_INT8 = 64 C_U2 + 16 M2 + C_L, the draft reading
  *      the top two bits only; source: Pith review page, "Editorial
- *      extensions", "Reading between the lines": the 4/8 split generalizes to
- *      the top k bits for the draft) the 8 KB of k_upper / v_upper per group hold
+ *      extensions", "Reading between the lines", which leaves drafts from
+ *      other numbers of leading bits open) the 8 KB of k_upper / v_upper per group hold
  *      the same nibbles C_U = 4 C_U2 + M2 re-packed: regard the 4-bit plane
  *      above as a sequence of 32-bit words w_0, w_1, ... (8 nibbles each,
  *      nibble j in bits 4j..4j+3).  Word k of the first 4 KB (the C_U2 plane)

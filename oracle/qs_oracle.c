@@ -36,8 +36,8 @@
  *   C_U = q >> 4, C_L = q & 15
  *   deq8 = s * (16*C_U + C_L) + z,   deqU = s * (16*C_U + 8) + z
  * A draft that reads the top k bits instead of four ([P3], "Editorial
- * extensions", "Reading between the lines": the 4/8 split generalizes to the
- * top k bits for the draft; the pages show k = 4 only) reconstructs, as our
+ * extensions", "Reading between the lines" raises other values of k as an
+ * open question; only k = 4 is evaluated on the pages) reconstructs, as our
  * reading, at the middle of the 2^(8-k) codes
  * sharing those bits, as the k = 4 midpoint does: with sh = 8 - k,
  *   deqK = s * (2^sh * (q >> sh) + 2^(sh-1)) + z     (k = 2: 64*C_U2 + 32).
