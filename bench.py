@@ -11,13 +11,18 @@ tokens):
     verify decode attention (5 queries, INT8), rollback of 4 - a (a seeded),
 then the counters are restored to the starting state (a device copy) so every
 step does the same work.  ``value`` is algorithmic bytes per step / step time
-(GB/s), summed over ranks.
+(GB/s), summed over ranks.  Bytes are counted per sequence from its own
+counters (a flush only for the sequences whose mask is set).
 
-Per-call numbers (draft_us, verify_us, flush_us and the roofline object) time
-one call at a time (CUDA-graph replay) with the L2 evicted before each call
-by reading a 256 MB buffer.
+Per-call numbers (draft_us, verify_us, flush_us) time one call at a time
+(CUDA-graph replay) with the L2 evicted before each call by reading a 256 MB
+buffer; the roofline object uses the calls' durations inside the step.  The
+``configs`` object reports the other workloads (tiny, 128k, batched 32k,
+ragged): the same round on each, with the durations of the attention calls
+inside it and the round's own time.
 """
 import argparse
+import ctypes
 import json
 import os
 import statistics
@@ -25,6 +30,7 @@ import subprocess
 import sys
 import threading
 import time
+from concurrent.futures import ThreadPoolExecutor
 
 import numpy as np
 
@@ -34,6 +40,8 @@ sys.path.insert(0, ROOT)
 METRIC = "decode-attn µs/step & HBM GB/s (draft 4-bit / verify 8-bit) at 32k ctx"
 GAMMA = 4
 KB = 1024
+G_TOK = 128
+RING = 2 * G_TOK
 
 
 def kernel_source_hash():
@@ -117,81 +125,255 @@ def prefill_bytes(L, BH, G=128):
     return BH * (L * 512 + ng * 33792 + (L - ng * G) * 512)
 
 
+def round_plan(ng0, f0, H, gamma=GAMMA, upper_bits=4):
+    """The counters of every sequence through one speculative round and the
+    algorithmic bytes of each call, counted per sequence: the flush only for
+    sequences whose buffer cannot take the gamma + 1 target tokens
+    (fill + gamma + 1 > 2G), then gamma drafts over fill1 + 1 .. fill1 + gamma
+    buffered tokens and a (gamma + 1)-query verify over fill1 + gamma + 1."""
+    ng0 = np.asarray(ng0, np.int64)
+    f0 = np.asarray(f0, np.int64)
+    B = len(ng0)
+    mask = (f0 + gamma + 1 > RING).astype(np.int64)
+    ng1 = ng0 + mask
+    f1 = f0 - G_TOK * mask
+    draft = [int(sum(attn_bytes(int(n), int(f) + i + 1, 1, True, H, upper_bits=upper_bits)
+                     for n, f in zip(ng1, f1))) for i in range(gamma)]
+    verify = int(sum(attn_bytes(int(n), int(f) + gamma + 1, gamma + 1, False, H)
+                     for n, f in zip(ng1, f1)))
+    b = {"flush": FLUSH_BYTES_PER_HEAD * H * int(mask.sum()), "draft": draft, "verify": verify,
+         "append": append_bytes(gamma, B * H) + append_bytes(gamma + 1, B * H)}
+    step = b["flush"] + sum(b["draft"]) + b["verify"] + b["append"]
+    return {"mask": mask, "ng1": ng1, "f1": f1, "bytes": b, "step": step}
+
+
 # --------------------------------------------------------------- clocks
 
-class ClockSampler:
-    """nvidia-smi samples (100 ms) with host timestamps; read the ones that
-    fall inside the timed window."""
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
-              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
-              "clocks_event_reasons.sw_power_cap")
+# NVML clock-event reason bits (read-only queries)
+_REASONS = (("sw_power_cap", 0x4), ("hw_slowdown", 0x8 | 0x80), ("sw_thermal_slowdown", 0x20),
+            ("hw_thermal_slowdown", 0x40))
 
-    def __init__(self, index):
+
+def nvml_reader(torch=None, index=0):
+    """A callable returning (sm_mhz, sm_max_mhz, power_w, reasons) for the
+    benchmark's GPU through NVML's read-only queries, or None when NVML is not
+    available.  The device is found by its UUID (CUDA and NVML may number
+    devices differently), else by index."""
+    try:
+        nv = ctypes.CDLL("libnvidia-ml.so.1")
+    except OSError:
+        return None
+    try:
+        if nv.nvmlInit_v2() != 0:
+            return None
+        h = ctypes.c_void_p()
+        ok = False
+        if torch is not None:
+            try:
+                uuid = str(torch.cuda.get_device_properties(index).uuid)
+                uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+                ok = nv.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(h)) == 0
+            except Exception:
+                ok = False
+        if not ok and nv.nvmlDeviceGetHandleByIndex_v2(index, ctypes.byref(h)) != 0:
+            return None
+        try:
+            reasons_fn = nv.nvmlDeviceGetCurrentClocksEventReasons
+        except AttributeError:
+            reasons_fn = nv.nvmlDeviceGetCurrentClocksThrottleReasons
+        smax = ctypes.c_uint()
+        if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(smax)) != 0:
+            return None
+    except Exception:
+        return None
+
+    def read():
+        sm, mw, bits = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        if nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(sm)) != 0:
+            return None
+        power = mw.value / 1e3 if nv.nvmlDeviceGetPowerUsage(h, ctypes.byref(mw)) == 0 else None
+        reasons = frozenset()
+        if reasons_fn(h, ctypes.byref(bits)) == 0:
+            reasons = frozenset(n for n, m in _REASONS if bits.value & m)
+        return float(sm.value), float(smax.value), power, reasons
+    return read
+
+
+class ClockSampler:
+    """SM clock, power and throttle reasons sampled during the timed region.
+
+    With a reader (NVML) a thread samples every ``period_s`` (1 ms), so even a
+    few-millisecond timed region holds several samples; without one it falls
+    back to ``nvidia-smi -lms 100``.  Samples are (host time, sm_mhz,
+    sm_max_mhz, power_w, reasons)."""
+
+    def __init__(self, reader=None, period_s=0.001, smi_index=None):
         self.samples = []
         self.proc = None
-        try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(index), "--query-gpu=" + self.FIELDS,
-                 "--format=csv,noheader,nounits", "-lms", "100"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-        except Exception:
-            return
-        self.t = threading.Thread(target=self._read, daemon=True)
-        self.t.start()
+        self.thread = None
+        self._halt = threading.Event()
+        self.source = None
+        if reader is not None:
+            self.source = "nvml %.0f ms" % (period_s * 1e3)
 
-    def _read(self):
-        for line in self.proc.stdout:
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) >= 7:
-                self.samples.append((time.time(), parts))
-
-    def stop(self):
-        if self.proc:
-            self.proc.terminate()
+            def loop():
+                while not self._halt.is_set():
+                    s = reader()
+                    if s is not None:
+                        self.samples.append((time.time(),) + tuple(s))
+                    time.sleep(period_s)
+            self.thread = threading.Thread(target=loop, daemon=True)
+            self.thread.start()
+        elif smi_index is not None:
+            self.source = "nvidia-smi 100 ms"
+            fields = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+                      "clocks_event_reasons.hw_thermal_slowdown,"
+                      "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
             try:
-                self.proc.wait(timeout=5)
+                self.proc = subprocess.Popen(
+                    ["nvidia-smi", "-i", str(smi_index), "--query-gpu=" + fields,
+                     "--format=csv,noheader,nounits", "-lms", "100"],
+                    stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             except Exception:
-                self.proc.kill()
+                self.proc = None
+                return
+            self.thread = threading.Thread(target=self._read_smi, daemon=True)
+            self.thread.start()
 
-    def summary(self, t0, t1):
-        inside = [p for (t, p) in self.samples if t0 <= t <= t1]
-        note = "inside timed region"
-        if not inside and self.samples:  # very short region: nearest samples after it started
-            inside = [p for (t, p) in self.samples if t >= t0][:3]
-            note = "timed region shorter than the sampling period; nearest samples"
-        if not inside:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+    @classmethod
+    def from_samples(cls, samples):
+        """A sampler holding the given samples (no thread, no process)."""
+        s = cls()
+        s.samples = list(samples)
+        return s
+
+    @staticmethod
+    def parse_smi(line):
+        """One nvidia-smi CSV line -> (sm, sm_max, power, reasons), None where
+        a field does not parse."""
+        p = [x.strip() for x in line.split(",")]
+        if len(p) < 7:
+            return None
 
         def num(x):
             try:
                 return float(x)
             except ValueError:
                 return None
-        sm = [num(p[0]) for p in inside if num(p[0]) is not None]
-        reasons = set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for p in inside:
-            for n, v in zip(names, p[3:7]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": num(inside[0][1]), "reasons": sorted(reasons),
-                "power_w_max": max((num(p[2]) or 0) for p in inside),
-                "samples": len(inside), "note": note}
+        reasons = frozenset(n for n, v in zip(names, p[3:7]) if v.lower().startswith("active"))
+        return num(p[0]), num(p[1]), num(p[2]), reasons
+
+    def _read_smi(self):
+        for line in self.proc.stdout:
+            s = self.parse_smi(line)
+            if s is not None:
+                self.samples.append((time.time(),) + s)
+
+    def stop(self):
+        self._halt.set()
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def count(self, t0, t1):
+        return sum(1 for s in list(self.samples) if t0 <= s[0] <= t1)
+
+    def summary(self, t0, t1, note="inside timed region"):
+        inside = [s for s in list(self.samples) if t0 <= s[0] <= t1]
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm = [s[1] for s in inside if s[1] is not None]
+        smax = [s[2] for s in inside if s[2] is not None]
+        power = [s[3] for s in inside if s[3] is not None]
+        reasons = set()
+        for s in inside:
+            reasons |= set(s[4])
+        out = {"sm_mhz": statistics.median(sm) if sm else None,
+               "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons),
+               "power_w_max": max(power) if power else None, "samples": len(inside),
+               "note": note}
+        if self.source:
+            out["source"] = self.source
+        return out
 
 
 # ------------------------------------------------------------ native arm
+
+def kv_tokens_parallel(synthetic, w, b, n, pool):
+    """synthetic.kv_tokens(w, b, 0, n), its 128-token chunks drawn in parallel
+    (each chunk has its own seeded generator, so the values are the same)."""
+    k = np.empty((w.H, n, w.D), np.float16)
+    v = np.empty_like(k)
+
+    def one(c):
+        m = min(synthetic.CHUNK, n - c * synthetic.CHUNK)
+        kc, vc = synthetic.kv_chunk(w, b, c, m)
+        k[:, c * synthetic.CHUNK:c * synthetic.CHUNK + m] = kc
+        v[:, c * synthetic.CHUNK:c * synthetic.CHUNK + m] = vc
+    list(pool.map(one, range(-(-n // synthetic.CHUNK))))
+    return k, v
+
+
+def fast_prefill(torch, qs, synthetic, cache, w):
+    """Bring ``cache`` to the workload's starting state (its n_groups and
+    fill per sequence) in a few public calls: qs_prefill of each sequence's
+    quantized tokens (which leaves the last 2G of them in the buffer), two
+    masked flushes that quantize those, one append of the buffer tokens and a
+    rollback that drops the padding and commits the rest.  The groups are the
+    consecutive G-token chunks of the stream either way, so the state equals
+    the one appending the whole context token by token would leave."""
+    dev = cache.state.device
+    B, H, D, G = w.B, w.H, w.D, w.G
+    tq = np.array(w.quantized, np.int64)
+    f = np.array(w.fill, np.int64)
+    assert np.all(tq % G == 0) and np.all((f >= 0) & (f <= 2 * G))
+    qs.qs_state_reset(cache)
+    with ThreadPoolExecutor(max_workers=max(1, min(32, os.cpu_count() or 1))) as pool:
+        tmax = int(tq.max(initial=0))
+        if tmax:
+            kd = torch.zeros((B, H, tmax, D), dtype=torch.float16, device=dev)
+            vd = torch.zeros_like(kd)
+            for b in range(B):
+                if tq[b]:
+                    k, v = kv_tokens_parallel(synthetic, w, b, int(tq[b]), pool)
+                    kd[b, :, :tq[b]].copy_(torch.from_numpy(k))
+                    vd[b, :, :tq[b]].copy_(torch.from_numpy(v))
+            qs.qs_prefill(cache, kd, vd, torch.from_numpy(tq.astype(np.int32)).to(dev))
+            del kd, vd
+            for k_ in range(2):
+                mask = torch.from_numpy((tq >= G * (k_ + 1)).astype(np.uint8)).to(dev)
+                qs.qs_quantize_flush(cache, mask)
+        fmax = int(f.max(initial=0))
+        if fmax:
+            kb = np.zeros((B, H, fmax, D), np.float16)
+            vb = np.zeros_like(kb)
+            for b in range(B):
+                if f[b]:
+                    kb[b, :, :f[b]], vb[b, :, :f[b]] = synthetic.kv_tokens(w, b, int(tq[b]),
+                                                                          int(f[b]))
+            qs.qs_buffer_append(cache, torch.from_numpy(kb).to(dev), torch.from_numpy(vb).to(dev))
+            qs.qs_buffer_rollback(cache, torch.from_numpy((fmax - f).astype(np.int32)).to(dev))
+    st = cache.state.cpu().numpy()
+    assert np.array_equal(st[:, 0], tq // G) and np.array_equal(st[:, 1], f), st[:, :5]
+    assert np.all(qs.qs_get_errors(cache) == 0)
+
 
 class Round:
     """Device state and inputs of the benchmark step on one GPU."""
 
     def __init__(self, torch, w, seed, upper_bits=4):
-        from hierarchical_quantized_kv_gb300 import driver, qs, synthetic
+        from hierarchical_quantized_kv_gb300 import qs, synthetic
         self.torch, self.qs, self.w = torch, qs, w
         dev = torch.device("cuda")
         B, H, D = w.B, w.H, w.D
         self.cache = qs.Cache(B, H, max(w.n_groups) + 2, upper_bits=upper_bits)
-        driver.prefill(self.cache, w)
+        fast_prefill(torch, qs, synthetic, self.cache, w)
         torch.cuda.synchronize()
         self.state0 = self.cache.state.clone()
         rng = np.random.default_rng([seed, 77])
@@ -233,25 +415,19 @@ class Round:
         self.drop_draft = torch.full((B,), GAMMA, dtype=torch.int32, device=dev)
         self.drops = [torch.from_numpy(GAMMA - synthetic.accepted_counts(w, s)).to(dev) for s in range(16)]
         self.scale = 1.0 / np.sqrt(D)
-        # state after the step's flush: one more group, half the buffer
-        ng0, f0 = int(self.state0[0, 0]), int(self.state0[0, 1])
-        self.ng1, self.f1 = ng0 + 1, f0 - w.G
-        BH = B * H
-        self.bytes = {
-            "flush": FLUSH_BYTES_PER_HEAD * BH,
-            "draft": [attn_bytes(self.ng1, self.f1 + i + 1, 1, True, BH) for i in range(GAMMA)],
-            "verify": attn_bytes(self.ng1, self.f1 + GAMMA + 1, GAMMA + 1, False, BH),
-            "append": append_bytes(GAMMA, BH) + append_bytes(GAMMA + 1, BH),
-        }
-        self.step_bytes = (self.bytes["flush"] + sum(self.bytes["draft"]) + self.bytes["verify"]
-                           + self.bytes["append"])
+        st = self.state0.cpu().numpy()
+        self.plan = round_plan(st[:, 0], st[:, 1], H, upper_bits=upper_bits)
+        # state after the step's flush (per sequence)
+        self.ng1, self.f1 = self.plan["ng1"], self.plan["f1"]
+        self.bytes = self.plan["bytes"]
+        self.step_bytes = self.plan["step"]
         # need_flush, flush, GAMMA x (append, draft), rollback, append, verify, rollback
         self.launches_per_step = 2 + GAMMA * 2 + 1 + 1 + 1 + 1
 
-    def step(self, s, host=None, ev=None):
+    def step(self, s, host=None, ev=None, external=False):
         """One speculative round.  ev: a list that receives (kind, start, end)
         CUDA events recorded around each attention call (as graph nodes when
-        the step is captured)."""
+        the step is captured with external=True)."""
         qs, c = self.qs, self.cache
         torch = self.torch
         if ev is not None:
@@ -260,7 +436,9 @@ class Round:
         def timed(kind, fn):
             if ev is None:
                 return fn()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            mk = (lambda: torch.cuda.Event(enable_timing=True, external=True)) if external else \
+                (lambda: torch.cuda.Event(enable_timing=True))
+            e0, e1 = mk(), mk()
             e0.record()
             fn()
             e1.record()
@@ -283,10 +461,13 @@ class Round:
         if host is not None:
             host.d2h(self)
 
-    # states for single-call timing
+    # states for single-call timing: per-sequence groups and fill
     def set_state(self, ng, fill):
+        torch = self.torch
         st = self.state0.clone()
-        st[:, 0], st[:, 1], st[:, 2] = ng, fill, 0
+        st[:, 0] = torch.as_tensor(np.asarray(ng), dtype=torch.int32, device=st.device)
+        st[:, 1] = torch.as_tensor(np.asarray(fill), dtype=torch.int32, device=st.device)
+        st[:, 2] = 0
         self.cache.state.copy_(st)
 
 
@@ -343,6 +524,106 @@ def time_calls(torch, fn, setup, iters, l2_scratch):
     return statistics.mean(ts[1:]) if len(ts) > 1 else ts[0]
 
 
+def external_events_supported(torch):
+    try:
+        torch.cuda.Event(enable_timing=True, external=True)
+        return True
+    except TypeError:
+        return False
+
+
+def in_step_launch_times(torch, r, n_rep):
+    """Device time of each attention call inside the step: the steps are
+    captured with CUDA events as graph nodes around each attention call and
+    replayed n_rep times (eager steps with events where torch cannot record
+    events into a graph).  Returns ({kind: [us, ...]}, how)."""
+    launch = {"draft": [], "verify": []}
+    if external_events_supported(torch):
+        recs, graphs = [], []
+        for s in range(len(r.drops)):
+            rec = []
+            graphs.append(capture(torch, lambda s=s, rec=rec: r.step(s, ev=rec, external=True)))
+            recs.append(rec)
+        for i in range(n_rep):
+            k = i % len(graphs)
+            graphs[k].replay()
+            torch.cuda.synchronize()
+            if i >= 2:
+                for kind, e0, e1 in recs[k]:
+                    launch[kind].append(e0.elapsed_time(e1) * 1e3)
+        how = ("CUDA events captured as graph nodes around each attention call, %d graph-replayed "
+               "steps after the timed region" % (n_rep - 2))
+    else:
+        recs = []
+        for s in range(n_rep):
+            rec = []
+            r.step(s, ev=rec)
+            recs.append(rec)
+        torch.cuda.synchronize()
+        for rec in recs[2:]:
+            for kind, e0, e1 in rec:
+                launch[kind].append(e0.elapsed_time(e1) * 1e3)
+        how = "CUDA events around each attention call in %d eager steps" % (n_rep - 2)
+    r.cache.state.copy_(r.state0)
+    return launch, how
+
+
+def replay_us(torch, graphs, n):
+    """Mean device time per replay of the step graphs, n replays in a row."""
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for s in range(n):
+        graphs[s % len(graphs)].replay()
+    b.record()
+    b.synchronize()
+    return a.elapsed_time(b) / n * 1e3
+
+
+def config_round(torch, qs, synthetic, name, peak, n_rep=40, n_replay=100):
+    """The speculative round on another workload: the attention calls'
+    durations inside the round (CUDA events) with their algorithmic bytes,
+    GB/s and fraction of the HBM peak, and the round's own time by graph
+    replay.  Bytes per sequence from its own counters."""
+    w = synthetic.CONFIGS[name]()
+    t_setup = time.perf_counter()
+    r = Round(torch, w, seed=0)
+    setup_s = time.perf_counter() - t_setup
+    for s in range(3):
+        r.step(s)
+    torch.cuda.synchronize()
+    launch, how = in_step_launch_times(torch, r, n_rep)
+    graphs = [capture(torch, lambda s=s: r.step(s)) for s in range(len(r.drops))]
+    replay_us(torch, graphs, 10)
+    round_us = replay_us(torch, graphs, n_replay)
+    errs = qs.qs_get_errors(r.cache)
+    assert np.all(errs == 0), errs
+    d_us, v_us = float(np.mean(launch["draft"])), float(np.mean(launch["verify"]))
+    d_b = float(np.mean(r.bytes["draft"]))
+    v_b = r.bytes["verify"]
+    ctx = np.array(w.context)
+    out = {
+        "workload": w.name, "B": w.B, "H": w.H,
+        "context": int(ctx[0]) if len(set(ctx)) == 1 else
+        {"min": int(ctx.min()), "max": int(ctx.max()), "mean": round(float(ctx.mean()), 1)},
+        "fill": int(w.fill[0]) if len(set(w.fill)) == 1 else
+        {"min": int(min(w.fill)), "max": int(max(w.fill))},
+        "flushing_sequences": int(r.plan["mask"].sum()),
+        "draft_us": round(d_us, 2), "draft_bytes": int(d_b), "draft_gbs": round(d_b / d_us / 1e3, 1),
+        "verify_us": round(v_us, 2), "verify_bytes": int(v_b),
+        "verify_gbs": round(v_b / v_us / 1e3, 1),
+        "round_us": round(round_us, 2), "round_bytes": int(r.step_bytes),
+        "round_gbs": round(r.step_bytes / round_us / 1e3, 1),
+        "launch_timing": how, "setup_s": round(setup_s, 1)}
+    if d_b > 2 * 129e6:  # working set larger than L2: an HBM roofline figure
+        out["draft_frac"] = round(d_b / d_us / 1e3 / peak, 4)
+        out["verify_frac"] = round(v_b / v_us / 1e3 / peak, 4)
+    else:
+        out["note"] = "working set fits in L2; no HBM roofline figure"
+    del graphs, r
+    torch.cuda.empty_cache()
+    return out
+
+
 def two_bit_calls(torch, qs, synthetic, w, l2, it):
     """The two-bit draft layout (upper_bits 2: the draft reads the top two
     bits of each code) on the benchmark workload: per-call draft and 5-query
@@ -354,7 +635,8 @@ def two_bit_calls(torch, qs, synthetic, w, l2, it):
             ("verify", qs.QS_VERIFY_INT8, r.qv, r.ov, r.lse, GAMMA + 1, r.f1 + GAMMA + 1)):
         us = time_calls(torch, lambda: qs.qs_attn_decode(r.cache, mode, q, r.scale, out, lse, r.ws),
                         lambda: r.set_state(r.ng1, fill), it, l2)
-        nb = attn_bytes(r.ng1, fill, n_q, mode == qs.QS_DRAFT_UPPER4, w.B * w.H, 1, 2)
+        nb = sum(attn_bytes(int(n), int(f), n_q, mode == qs.QS_DRAFT_UPPER4, w.H, 1, 2)
+                 for n, f in zip(r.ng1, fill))
         res[name + "_us"] = round(us, 2)
         res[name + "_gbs"] = round(nb / us / 1e3, 1)
     assert np.all(qs.qs_get_errors(r.cache) == 0)
@@ -419,8 +701,9 @@ def native(args):
         graphs[s % len(graphs)].replay()
     torch.cuda.synchronize()
 
-    sampler = ClockSampler(local)
-    time.sleep(0.3)
+    reader = nvml_reader(torch, local)
+    sampler = ClockSampler(reader=reader) if reader is not None else ClockSampler(smi_index=local)
+    time.sleep(0.3 if reader is None else 0.02)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -436,9 +719,24 @@ def native(args):
     t1 = time.time()
     if world > 1:
         dist.barrier()
-    sampler.stop()
     ms = rank_max(dist, world, ev0.elapsed_time(ev1) / args.steps, "cuda")
-    clocks = sampler.summary(t0, t1)
+    note = "inside timed region"
+    t_end = t1
+    if sampler.count(t0, t1) < 2:
+        # a region shorter than two sampling periods: the same step loop runs
+        # on (untimed) until two samples have been taken since it started
+        note = ("timed region (%.1f ms) shorter than two sampling periods; samples from its start "
+                "through the same graph replays continued right after it" % ((t1 - t0) * 1e3))
+        deadline = time.time() + 2.0
+        s = args.steps
+        while sampler.count(t0, time.time()) < 2 and time.time() < deadline:
+            for _ in range(20):
+                graphs[s % len(graphs)].replay()
+                s += 1
+            torch.cuda.synchronize()
+        t_end = time.time()
+    sampler.stop()
+    clocks = sampler.summary(t0, t_end, note)
 
     # per-call timing with L2 flushed (draft, verify, flush)
     l2 = torch.ones(64 << 20, dtype=torch.float32, device="cuda")  # 256 MB
@@ -464,12 +762,14 @@ def native(args):
         pc = qs.Cache(1, w.H, r.cache.cap)
         prefill_us = time_calls(torch, lambda: qs.qs_prefill(pc, kp, vp, lens),
                                 lambda: qs.qs_state_reset(pc), it, l2)
-        assert torch.equal(pc.state[0, :4].cpu(), r.state0[0, :4].cpu())
+        st_p = pc.state[0, :2].cpu().numpy()
+        ng_p = -(-(T - 2 * w.G) // w.G) if T > 2 * w.G else 0
+        assert st_p[0] == ng_p and st_p[1] == T - ng_p * w.G, st_p
         prefill_gbs = prefill_bytes(T, w.H) / prefill_us / 1e3
         del kp, vp, pc
-    gqa = gqa_calls(torch, qs, synthetic, l2, it) if w.name == synthetic.llama_32k().name else None
-    two_bit = (two_bit_calls(torch, qs, synthetic, w, l2, it)
-               if w.name == synthetic.llama_32k().name else None)
+    main_32k = w.name == synthetic.llama_32k().name
+    gqa = gqa_calls(torch, qs, synthetic, l2, it) if main_32k else None
+    two_bit = two_bit_calls(torch, qs, synthetic, w, l2, it) if main_32k else None
     # speculative acceptance for the round (synthetic probabilities over a
     # 32,000-token vocabulary): accept/reject, the emitted token, n_drop
     V = 32000
@@ -482,47 +782,55 @@ def native(args):
     sa = [torch.empty(w.B, dtype=torch.int32, device="cuda") for _ in range(3)]
     spec_us = time_calls(torch, lambda: qs.qs_spec_accept(pp, qq, dr, uu, ee, *sa), lambda: None, it,
                          l2)
+    del l2
     draft_b, verify_b = r.bytes["draft"][0], r.bytes["verify"]
     draft_gbs, verify_gbs = draft_b / draft_us / 1e3, verify_b / verify_us / 1e3
-    # The roofline's launch durations: a second timed region right after the
-    # main one, the same steps launched eagerly (no graph) with CUDA events on
-    # the launch stream around each attention call; the host stays ahead of
-    # the device, so each pair of events brackets that kernel alone.
-    launch = {"draft": [], "verify": []}
-    n_ev = max(8, min(args.steps // 8, 200))
-    recs = []
-    for s in range(n_ev):
-        rec = []
-        r.step(s, ev=rec)
-        recs.append(rec)
-    torch.cuda.synchronize()
-    for rec in recs[2:]:  # the first steps warm the eager path up
-        for kind, e0, e1 in rec:
-            launch[kind].append(e0.elapsed_time(e1) * 1e3)
+    # The roofline's launch durations: the attention calls inside the step
+    launch, launch_how = in_step_launch_times(torch, r, max(12, min(args.steps, 60)))
     draft_launch_us = float(np.mean(launch["draft"]))
     verify_launch_us = float(np.mean(launch["verify"]))
-    r.cache.state.copy_(r.state0)
+    draft_b_mean = float(np.mean(r.bytes["draft"]))
     # dominant kernel by device time within a step
-    dominant = ("draft", draft_b / draft_launch_us / 1e3, draft_launch_us, GAMMA * draft_launch_us) \
+    dominant = ("draft", draft_b_mean / draft_launch_us / 1e3, draft_launch_us) \
         if GAMMA * draft_launch_us >= verify_launch_us else \
-        ("verify", verify_b / verify_launch_us / 1e3, verify_launch_us, verify_launch_us)
+        ("verify", verify_b / verify_launch_us / 1e3, verify_launch_us)
 
     # end to end through host buffers: each step copies its inputs from pinned
-    # host memory, runs, copies its outputs back, and the host waits for them
+    # host memory, runs, copies its outputs back, and the host waits for them.
+    # e2e: the step's calls made through the C ABI from Python every step (no
+    # graph); e2e_graph: the same step replayed from a CUDA graph.
     host = HostIO(torch, r)
+    e_steps = max(1, min(args.steps, 500))
+    for s in range(3):
+        r.step(s, host)
+        torch.cuda.current_stream().synchronize()
+    te0 = time.perf_counter()
+    for s in range(e_steps):
+        r.step(s, host)
+        torch.cuda.current_stream().synchronize()  # the host reads the step's result
+    e2e_ms = rank_max(dist, world, (time.perf_counter() - te0) * 1e3 / e_steps, "cuda")
     egraphs = [capture(torch, lambda s=s: r.step(s, host)) for s in range(len(r.drops))]
     for s in range(3):
         egraphs[s % len(egraphs)].replay()
         torch.cuda.current_stream().synchronize()
-    e_steps = max(1, min(args.steps, 500))
     te0 = time.perf_counter()
     for s in range(e_steps):
         egraphs[s % len(egraphs)].replay()
-        torch.cuda.current_stream().synchronize()  # the host reads the step's result
-    e2e_ms = rank_max(dist, world, (time.perf_counter() - te0) * 1e3 / e_steps, "cuda")
+        torch.cuda.current_stream().synchronize()
+    e2e_graph_ms = rank_max(dist, world, (time.perf_counter() - te0) * 1e3 / e_steps, "cuda")
+    del egraphs, graphs
 
     errs = qs.qs_get_errors(r.cache)
     assert np.all(errs == 0), errs
+    step_bytes, flushing = r.step_bytes, int(r.plan["mask"].sum())
+    ng_att = int(np.max(r.ng1))
+    del r
+    torch.cuda.empty_cache()
+    configs = {}
+    if not args.no_configs and rank == 0 and world == 1:
+        for name in ("tiny", "128k", "batched32k", "ragged"):
+            if name != args.config:
+                configs[name] = config_round(torch, qs, synthetic, name, peak)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w, budget_s=args.cpu_budget)
@@ -530,7 +838,7 @@ def native(args):
         dist.destroy_process_group()
     if rank != 0:
         return
-    gbs = aggregate_gbs(r.step_bytes, world, ms)
+    gbs = aggregate_gbs(step_bytes, world, ms)
     line = {
         "metric": METRIC, "value": round(gbs, 1), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
@@ -539,9 +847,10 @@ def native(args):
         "config": {"workload": w.name + " speculative round (gamma=4: flush, 4x(append 1 + draft 1q), "
                                "rollback 4, append 5, verify 5q, rollback 4-a)",
                    "B": w.B, "H": w.H, "D": w.D, "G": w.G, "context": w.context[0],
-                   "quantized_groups_at_attention": r.ng1, "bytes_per_step": r.step_bytes,
+                   "quantized_groups_at_attention": ng_att,
+                   "bytes_per_step": step_bytes, "flushing_sequences": flushing,
                    "l2": "step: inputs larger than L2 (%.0f MB of planes per step); per-call numbers: "
-                         "L2 evicted before each call by a 256 MB read" % (r.step_bytes / 1e6),
+                         "L2 evicted before each call by a 256 MB read" % (step_bytes / 1e6),
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "draft_in_step_us": round(draft_launch_us, 2), "verify_in_step_us": round(verify_launch_us, 2),
         "draft_us": round(draft_us, 2), "draft_gbs": round(draft_gbs, 1),
@@ -554,16 +863,21 @@ def native(args):
         "two_bit_draft": two_bit,
         "roofline": {"bound": "hbm", "kernel": "qs_attn_decode %s (split_kernel: split-KV attention + LSE merge, one launch)" % dominant[0],
                      "launch_us": round(dominant[2], 2),
-                     "launch_timing": "CUDA events around each call in %d eagerly launched steps "
-                                      "after the timed region (mean of %d calls)"
-                                      % (n_ev - 2, len(launch[dominant[0]])),
+                     "launch_timing": launch_how + " (mean of %d calls)" % len(launch[dominant[0]]),
                      "achieved": round(dominant[1], 1), "peak": peak,
                      "peak_kind": "%s hbm_gbs (copy, burst)" % peak_kind, "unit": "GB/s",
                      "frac": round(dominant[1] / peak, 4), "traffic": stored_traffic(dominant[0])},
-        "e2e": {"value": round(aggregate_gbs(r.step_bytes, world, e2e_ms), 1), "unit": "GB/s",
+        "e2e": {"value": round(aggregate_gbs(step_bytes, world, e2e_ms), 1), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": host.h2d_bytes,
-                "d2h_bytes_per_step": host.d2h_bytes},
-        "gpu_launches": r.launches_per_step * args.steps,
+                "d2h_bytes_per_step": host.d2h_bytes,
+                "how": "every step: one pinned H2D copy of the step's inputs, the step's %d calls "
+                       "through the C ABI (ctypes, no graph), one D2H copy of its outputs, a host "
+                       "wait" % 14},
+        "e2e_graph": {"value": round(aggregate_gbs(step_bytes, world, e2e_graph_ms), 1),
+                      "unit": "GB/s", "ms_per_step": round(e2e_graph_ms, 4),
+                      "how": "the same step, copies included, replayed from a CUDA graph"},
+        "configs": configs,
+        "gpu_launches": 14 * args.steps,
         "launch": "CUDA graph replay of each step (one graph per distinct step)",
         "clocks": clocks,
     }
@@ -615,16 +929,18 @@ def sample_heads(w):
     return list(range(min(w.H, oracle.num_threads())))
 
 
+def sample_step_bytes(w, n_heads):
+    """Algorithmic bytes of one step on the oracle sample: sequence 0's
+    counters, n_heads of its heads (the flush counted only if it is due)."""
+    return round_plan([w.n_groups[0]], [w.fill[0]], n_heads)["step"]
+
+
 def cpu_baseline(w, budget_s=15.0):
     heads = sample_heads(w)
     oc = cpu_sample(w, heads)
     rng = np.random.default_rng(5)
     BH = len(heads)
-    ng1, f1 = w.n_groups[0] + 1, w.fill[0] - w.G
-    step_bytes = (FLUSH_BYTES_PER_HEAD * BH
-                  + sum(attn_bytes(ng1, f1 + i + 1, 1, True, BH) for i in range(GAMMA))
-                  + attn_bytes(ng1, f1 + GAMMA + 1, GAMMA + 1, False, BH)
-                  + append_bytes(GAMMA, BH) + append_bytes(GAMMA + 1, BH))
+    step_bytes = sample_step_bytes(w, BH)
     n, t0 = 0, time.perf_counter()
     while True:
         cpu_step(oc, w, n, rng)
@@ -653,11 +969,7 @@ def reference(args):
     oc = cpu_sample(w, heads)
     rng = np.random.default_rng(5)
     BH = len(heads)
-    ng1, f1 = w.n_groups[0] + 1, w.fill[0] - w.G
-    step_bytes = (FLUSH_BYTES_PER_HEAD * BH
-                  + sum(attn_bytes(ng1, f1 + i + 1, 1, True, BH) for i in range(GAMMA))
-                  + attn_bytes(ng1, f1 + GAMMA + 1, GAMMA + 1, False, BH)
-                  + append_bytes(GAMMA, BH) + append_bytes(GAMMA + 1, BH))
+    step_bytes = sample_step_bytes(w, BH)
     for s in range(args.warmup):
         cpu_step(oc, w, s, rng)
     t0 = time.perf_counter()
@@ -754,6 +1066,8 @@ def main():
     ap.add_argument("--call-iters", type=int, default=30)
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the rounds on the other workloads")
     ap.add_argument("--profile", choices=["draft", "verify", "flush", "prefill", "step", "gqa_draft",
                                           "gqa_verify"])
     ap.add_argument("--profile-calls", type=int, default=3)

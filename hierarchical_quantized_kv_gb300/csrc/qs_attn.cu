@@ -103,6 +103,8 @@ struct Params {
   int ncg;    // column groups of eight rows, ceil(R / 8): warp w serves group w % ncg
   int P;      // split-kernel grid size (number of contiguous unit ranges)
   float sl2;  // softmax_scale * log2(e)
+  uint64_t wait_ns;  // limit on each pipeline wait (kWaitLimitNs outside tests)
+  int no_issue;      // test entry only: issue no copy, so that every wait runs out
 };
 
 struct Tables {
@@ -420,6 +422,20 @@ __device__ __forceinline__ void issue_unit(const qs_cache &c, const Tables &T, c
   }
 }
 
+// Device-scope fence between a CTA's partials and its arrival on a segment
+// counter (release), and between the arrival that completes a segment and
+// the reads of the other CTAs' partials (acquire).
+#ifndef QS_FENCE_AR
+#define QS_FENCE_AR 0
+#endif
+__device__ __forceinline__ void fence_gpu() {
+#if QS_FENCE_AR
+  asm volatile("fence.acq_rel.gpu;" ::: "memory");
+#else
+  __threadfence();
+#endif
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -457,42 +473,37 @@ __device__ __forceinline__ float4 ld_part4(const float *p) {
   return v;
 }
 
-// CTA-wide: lanes hold four channels each; the nw warps take jpr rows at
-// once (the smallest divisor of nw >= R, or nw in rounds) and split the
-// partials into nw / jpr phases.  Each thread loads its partials
-// four at a time, all four in flight before the first is used; the phases
-// then meet in `red` (384 x 6 floats of shared memory): the largest m first,
-// then one independent rescale per phase.  Row j's partials start at
-// srcA + (j / 8) * cgA (and srcB + (j / 8) * cgB): warp partials hold only
-// the rows of their warp's column group.  Not inlined: it runs at the end of
-// the kernel from a cold instruction cache, where one small copy matters more
-// than the call.
-__device__ __noinline__ void merge_partials(const float *srcA, int cgA, int kstrideA, int nA,
-                                            const float *srcB, int cgB, int kstrideB, int ns,
-                                            int R, const MergeOut &mo, float *red, int nw) {
-  constexpr int kBatch = 4;
-  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  int jpr = nw;  // rows at once: the smallest divisor of nw that is >= min(R, nw)
-  for (int d = 1; d < nw; ++d)
-    if (nw % d == 0 && d >= min(R, nw)) {
-      jpr = d;
-      break;
-    }
-  const int ph = nw / jpr, phase = w / jpr;
+// Row-parallel: row j of the R rows is merged by one warp, whose lanes hold
+// four channels each; with more rows than warps a warp takes rows
+// blockDim / 32 apart.  Each lane loads a batch of partials (m, l and its four
+// channels of O) at once, all in flight before the first is used, and folds
+// them into a running (M, L, O) with one rescale per batch: no shared-memory
+// scratch and no barrier, so warps without a row return at once.  Row j's
+// partials start at srcA + (j / 8) * cgA (and srcB + (j / 8) * cgB): warp
+// partials hold only the rows of their warp's column group.  dst may be
+// partial 0 of the sources: each lane writes only what it read, after the
+// warp's reads.  Not inlined: it runs once or twice per launch, at the end,
+// where every instruction is fetched cold, so one small shared copy matters
+// more than the call.
+__device__ __noinline__ void merge_rows(const float *srcA, int cgA, int kstrideA, int nA,
+                                        const float *srcB, int cgB, int kstrideB, int ns, int R,
+                                        const MergeOut &mo) {
+  constexpr int kBatch = 8;
+  const int lane = threadIdx.x & 31;
   const int mo_off = R * kD;
 #pragma unroll 1
-  for (int j = w % jpr; j - w % jpr < R; j += jpr) {  // rounds of jpr rows
-  const float *a0 = srcA + (j >> 3) * cgA, *b0 = srcB + (j >> 3) * cgB;
-  float M = -INFINITY, L = 0.f;
-  float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (j < R) {
+  for (int idx = threadIdx.x; idx < R * 32; idx += blockDim.x) {
+    const int j = idx >> 5;
+    const float *a0 = srcA + (j >> 3) * cgA, *b0 = srcB + (j >> 3) * cgB;
+    float M = -INFINITY, L = 0.f;
+    float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 1
-    for (int kb = phase; kb < ns; kb += kBatch * ph) {
+    for (int kb = 0; kb < ns; kb += kBatch) {
       float ms[kBatch], ls[kBatch];
       float4 os[kBatch];
 #pragma unroll
       for (int u = 0; u < kBatch; ++u) {
-        const int k = kb + u * ph;
+        const int k = kb + u;
         ms[u] = -INFINITY;
         ls[u] = 0.f;
         os[u] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -528,35 +539,7 @@ __device__ __noinline__ void merge_partials(const float *srcA, int cgA, int kstr
       }
       M = mn;
     }
-  }
-  if (ph > 1) {  // the phases (warps jpr apart) meet in shared memory
-    float *mine = red + 6 * threadIdx.x;
-    mine[0] = M; mine[1] = L; mine[2] = A.x; mine[3] = A.y; mine[4] = A.z; mine[5] = A.w;
-    __syncthreads();
-    if (phase == 0 && j < R) {
-      float mx = M;
-      for (int q = 1; q < ph; ++q) mx = fmaxf(mx, red[6 * (threadIdx.x + 32 * jpr * q)]);
-      if (mx != -INFINITY) {
-        const float f0 = (M == -INFINITY) ? 0.f : fast_exp2(M - mx);
-        L *= f0;
-        A.x *= f0; A.y *= f0; A.z *= f0; A.w *= f0;
-        for (int q = 1; q < ph; ++q) {
-          const float *o = red + 6 * (threadIdx.x + 32 * jpr * q);
-          const float f = (o[0] == -INFINITY) ? 0.f : fast_exp2(o[0] - mx);
-          L = fmaf(f, o[1], L);
-          A.x = fmaf(f, o[2], A.x);
-          A.y = fmaf(f, o[3], A.y);
-          A.z = fmaf(f, o[4], A.z);
-          A.w = fmaf(f, o[5], A.w);
-        }
-        M = mx;
-      }
-    }
-    __syncthreads();  // red is free again; every read of the sources is done
-  } else {
-    __syncwarp();  // the warp's reads of query j are done before dst is written
-  }
-  if (phase == 0 && j < R) {
+    __syncwarp();  // every lane's reads of row j are done before dst is written
     if (mo.final) {
       const float Ld = L > 0.f ? L : 1.f;  // L > 0 whenever a token is visible
       uint2 h;
@@ -574,12 +557,11 @@ __device__ __noinline__ void merge_partials(const float *srcA, int cgA, int kstr
       }
     }
   }
-  }  // rounds
 }
 
 // One warp's partial of a piece (unnormalized, log2 domain; m = -inf if the
 // warp saw no visible token; O as accumulated times oscale, plus the value
-// bias) in the layout merge_partials reads: rows
+// bias) in the layout merge_rows reads: rows
 // [8 cg, 8 cg + 8) of R, O at row * 128 + d, m at R * 128 + row, l at
 // R * 128 + 24 + row; dst is in global or shared memory.
 __device__ __forceinline__ void write_partial(const Softmax &sm, float oscale, float *dst, int R,
@@ -617,12 +599,12 @@ __device__ __forceinline__ void write_empty(float *dst, int R, int cg, int lane)
   }
 }
 
-// Wait (bounded) until a stage's copy of unit i has been issued.
-__device__ __forceinline__ bool wait_issued(volatile int *issued, int i) {
+// Wait (at most limit_ns) until a stage's copy of unit i has been issued.
+__device__ __forceinline__ bool wait_issued(volatile int *issued, int i, uint64_t limit_ns) {
   if (*issued == i) return true;
   const uint64_t t0 = globaltimer_ns();
   while (*issued != i)
-    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
   return true;
 }
 
@@ -715,7 +697,7 @@ __global__ void __launch_bounds__(NW * 32, 1) split_kernel(const Params prm) {
     int last = 0;
     if (lane == 0) last = atomicAdd(&s_left_first, 1) == NW - 1;
     if (!__shfl_sync(0xffffffffu, last, 0)) return;
-    __threadfence();
+    fence_gpu();
     const long long seg = (long long)first.b * c.H + first.h;
     const int plo = cta_of(first.s0, U, prm.P);  // the segment ends in this range: p_hi = p
     if (lane == 0 && atomicAdd(&c.arrive[seg], 1) == p - plo) {
@@ -734,7 +716,7 @@ __global__ void __launch_bounds__(NW * 32, 1) split_kernel(const Params prm) {
   }
 
   // units i and i + S share stage i % S; warp 0 issues the first S
-  if (w == 0) {
+  if (w == 0 && !prm.no_issue) {
     Seg a;
     for (int k = 0; k < S && k < n; ++k) {
       a.seek(x0 + k, T, c.B);
@@ -791,8 +773,8 @@ __global__ void __launch_bounds__(NW * 32, 1) split_kernel(const Params prm) {
     const int stage = i % S;
     // the stage must hold unit i's copy (not the unit S before it) before its
     // barrier parity means anything
-    bool ok = wait_issued(issued + stage, i);
-    if (ok) ok = mbar_wait(full0 + 8 * stage, (uint32_t)((i / S) & 1));
+    bool ok = wait_issued(issued + stage, i, prm.wait_ns);
+    if (ok) ok = mbar_wait(full0 + 8 * stage, (uint32_t)((i / S) & 1), prm.wait_ns);
     ok = __all_sync(0xffffffffu, ok);  // the tensor-core code below needs the whole warp
     if (!ok) {
       if (lane == 0) {
@@ -1139,17 +1121,27 @@ __global__ void __launch_bounds__(NW * 32, 1) split_kernel(const Params prm) {
   __syncthreads();
   // no copy may still be landing in the stage memory reused below: after a
   // timeout, wait for each stage's last copy (otherwise every issued copy
-  // has been waited for by the warps that claimed its halves)
-  if (w == 0 && s_abort) {
-    const unsigned long long deadline = globaltimer_ns() + kWaitLimitNs;
-    for (int s = lane; s < S; s += 32) {
-      const int j = issued[s];
-      if (j >= 0)
-        while (!mbar_try_wait(full0 + 8 * s, (uint32_t)((j / S) & 1)) && globaltimer_ns() < deadline) {
-        }
+  // has been waited for by the warps that claimed its halves).  If that wait
+  // runs out too, s_abort = 2: a copy may still land in the stages, so the
+  // CTA writes nothing more into them (its partials and merges are skipped;
+  // the arrivals below still return the counters to zero).
+  if (s_abort) {  // uniform: read after the barrier above
+    if (w == 0) {
+      const unsigned long long deadline = globaltimer_ns() + prm.wait_ns;
+      bool drained = true;
+      for (int s = lane; s < S; s += 32) {
+        const int j = issued[s];
+        if (j >= 0)
+          while (!mbar_try_wait(full0 + 8 * s, (uint32_t)((j / S) & 1)))
+            if (globaltimer_ns() >= deadline) {
+              drained = false;
+              break;
+            }
+      }
+      if (!__all_sync(0xffffffffu, drained) && lane == 0) s_abort = 2;
     }
+    __syncthreads();
   }
-  __syncthreads();
 
   // ---- log-sum-exp merge.  Per piece of this CTA's range (but a shared
   // first piece, see above): merge the NW warp partials (the last piece's
@@ -1160,19 +1152,22 @@ __global__ void __launch_bounds__(NW * 32, 1) split_kernel(const Params prm) {
   // resets the counter.  Only the first and the last piece of a range can be
   // shared.
   const bool aborted = s_abort != 0;
-  float *red = reinterpret_cast<float *>(smem);                 // stage memory, free now
-  float *last_part = reinterpret_cast<float *>(smem + 16384);  // NW partials
-  if (cur_ord == ord_last) write_partial(sm, Centre<MODE, UB>::kScale, last_part + w * stride, R, cg, lane, PK);
-  else write_empty(last_part + w * stride, R, cg, lane);
+  float *last_part = reinterpret_cast<float *>(smem);  // NW partials, in stage memory (free now)
+  if (s_abort != 2) {
+    if (cur_ord == ord_last)
+      write_partial(sm, Centre<MODE, UB>::kScale, last_part + w * stride, R, cg, lane, PK);
+    else
+      write_empty(last_part + w * stride, R, cg, lane);
+  }
   __syncthreads();
   if (s_first_fin && !aborted) {
-    __threadfence();  // the other CTAs' partials are visible from here on
+    fence_gpu();  // the other CTAs' partials are visible from here on
     const long long seg = (long long)first.b * c.H + first.h;
     const int plo = cta_of(first.s0, U, prm.P);
     const MergeOut fo{true, prm.out + (size_t)seg * R * kD,
                       prm.lse ? prm.lse + (size_t)seg * R : nullptr, nullptr};
-    merge_partials(prm.ws + (size_t)(ord_first + plo) * NW * stride, 0, NW * stride, p - plo,
-                   slot(ord_first, 0), stride, ncg * stride, p - plo + NW / ncg, R, fo, red, NW);
+    merge_rows(prm.ws + (size_t)(ord_first + plo) * NW * stride, 0, NW * stride, p - plo,
+               slot(ord_first, 0), stride, ncg * stride, p - plo + NW / ncg, R, fo);
   }
   int n_arr = 0;
   {
@@ -1186,8 +1181,8 @@ __global__ void __launch_bounds__(NW * 32, 1) split_kernel(const Params prm) {
       const MergeOut mo{plo == phi, prm.out + (size_t)seg * R * kD,
                         prm.lse ? prm.lse + (size_t)seg * R : nullptr, slot(pc.ord, 0)};
       if (!aborted)
-        merge_partials(pc.ord == ord_last ? last_part : slot(pc.ord, 0), stride, ncg * stride,
-                       NW / ncg, nullptr, 0, 0, NW / ncg, R, mo, red, NW);
+        merge_rows(pc.ord == ord_last ? last_part : slot(pc.ord, 0), stride, ncg * stride,
+                   NW / ncg, nullptr, 0, 0, NW / ncg, R, mo);
       if (plo != phi) {
         if (threadIdx.x == 0) {
           s_seg[n_arr] = (int)seg;
@@ -1203,11 +1198,11 @@ __global__ void __launch_bounds__(NW * 32, 1) split_kernel(const Params prm) {
   __syncthreads();  // this CTA's partials are written (made visible by the fence below)
   if (threadIdx.x < n_arr) {
     int *ctr = c.arrive + s_seg[threadIdx.x];
-    __threadfence();
+    fence_gpu();
     const int last = atomicAdd(ctr, 1) == s_need[threadIdx.x] - 1;
     if (last) {
       atomicExch(ctr, 0);  // every other arrival is in: ready for the next call
-      __threadfence();     // the other CTAs' partials are visible from here on
+      fence_gpu();     // the other CTAs' partials are visible from here on
     }
     s_last[threadIdx.x] = last;
   }
@@ -1227,8 +1222,8 @@ __global__ void __launch_bounds__(NW * 32, 1) split_kernel(const Params prm) {
     const float *cta0 = prm.ws + ((size_t)(s_ord[a] + plo) * NW) * stride;
     const float *raw0 = prm.ws + ((size_t)(s_ord[a] + phi) * NW) * stride;
     const int nA = raw ? phi - plo : phi - plo + 1;
-    merge_partials(cta0, 0, NW * stride, nA, raw0, stride, ncg * stride,
-                   nA + (raw ? NW / ncg : 0), R, mo, red, NW);
+    merge_rows(cta0, 0, NW * stride, nA, raw0, stride, ncg * stride,
+               nA + (raw ? NW / ncg : 0), R, mo);
   }
 }
 
@@ -1326,9 +1321,14 @@ qs_status qs_attn_workspace_size(const qs_cache *c, int32_t n_q, size_t *bytes) 
   return qs_attn_workspace_size_gqa(c, n_q, 1, bytes);
 }
 
-qs_status qs_attn_decode_gqa(const qs_cache *c, qs_mode mode, const uint16_t *q, int32_t n_q,
-                             int32_t group, float softmax_scale, uint16_t *out, float *lse,
-                             void *workspace, size_t workspace_bytes, qs_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Validation, launch configuration and launch shared by the entry points.
+qs_status decode(const qs_cache *c, qs_mode mode, const uint16_t *q, int32_t n_q, int32_t group,
+                 float softmax_scale, uint16_t *out, float *lse, void *workspace,
+                 size_t workspace_bytes, uint64_t wait_ns, int no_issue, qs_stream_t stream) {
   qs_status s = check_cache(c);
   if (s != QS_OK) return s;
   if (!q || !out || n_q < 1 || n_q > kMaxQ || group < 1 || group * n_q > kMaxR) return QS_ERR_ARG;
@@ -1344,6 +1344,8 @@ qs_status qs_attn_decode_gqa(const qs_cache *c, qs_mode mode, const uint16_t *q,
   prm.R = group * n_q;
   prm.ncg = (prm.R + 7) / 8;
   prm.sl2 = softmax_scale * 1.4426950408889634f;
+  prm.wait_ns = wait_ns;
+  prm.no_issue = no_issue;
   const bool packed = (mode == QS_DRAFT_UPPER4 && prm.R <= 4);
   if ((s = grid_size(mode, packed, c->upper_bits, prm.ncg, prm.P)) != QS_OK) return s;
   if (!workspace || !aligned16(workspace) ||
@@ -1355,11 +1357,39 @@ qs_status qs_attn_decode_gqa(const qs_cache *c, qs_mode mode, const uint16_t *q,
                             : launch_ub<4>(mode, packed, prm, st);
 }
 
+}  // namespace
+
+extern "C" {
+
+qs_status qs_attn_decode_gqa(const qs_cache *c, qs_mode mode, const uint16_t *q, int32_t n_q,
+                             int32_t group, float softmax_scale, uint16_t *out, float *lse,
+                             void *workspace, size_t workspace_bytes, qs_stream_t stream) {
+  return decode(c, mode, q, n_q, group, softmax_scale, out, lse, workspace, workspace_bytes,
+                kWaitLimitNs, 0, stream);
+}
+
 qs_status qs_attn_decode(const qs_cache *c, qs_mode mode, const uint16_t *q, int32_t n_q,
                          float softmax_scale, uint16_t *out, float *lse, void *workspace,
                          size_t workspace_bytes, qs_stream_t stream) {
   return qs_attn_decode_gqa(c, mode, q, n_q, 1, softmax_scale, out, lse, workspace,
                             workspace_bytes, stream);
+}
+
+// Test entry, not declared in include/qs.h: qs_attn_decode_gqa with every
+// pipeline wait limited to wait_ns (1 us .. 100 ms) and no copy ever issued,
+// so the first wait of every warp runs out.  It exercises the failure path
+// of the kernel without a fault: the sequences get QS_DEV_TIMEOUT, the
+// kernel returns within a few multiples of wait_ns, no output is written, and
+// the arrival counters end at zero, so the next ordinary call on the cache is
+// valid.
+qs_status qs_test_attn_decode_timeout(const qs_cache *c, qs_mode mode, const uint16_t *q,
+                                      int32_t n_q, int32_t group, float softmax_scale,
+                                      uint16_t *out, float *lse, void *workspace,
+                                      size_t workspace_bytes, uint64_t wait_ns,
+                                      qs_stream_t stream) {
+  if (wait_ns < 1000ull || wait_ns > 100000000ull) return QS_ERR_ARG;
+  return decode(c, mode, q, n_q, group, softmax_scale, out, lse, workspace, workspace_bytes,
+                wait_ns, 1, stream);
 }
 
 }  // extern "C"

@@ -66,6 +66,8 @@ _SIGS = {
                            _P, _P, _P, ctypes.c_size_t, _P],
     "qs_prefill": [ctypes.POINTER(QsCacheStruct), _P, _P, _I32, _P, _P],
     "qs_spec_accept": [_P, _P, _P, _P, _P, _I32, _I32, _I32, _P, _P, _P, _P],
+    "qs_attn_decode_static_ws": [ctypes.POINTER(QsCacheStruct), ctypes.c_int, _P, _I32,
+                                 ctypes.c_float, _P, _P, _P],
 }
 
 
@@ -230,6 +232,20 @@ def qs_attn_decode_gqa(cache, mode, q, group, softmax_scale, out, lse=None, work
     _check("qs_attn_decode_gqa", lib().qs_attn_decode_gqa(
         cache._ref, int(mode), _ptr(q), n_q, int(group), float(softmax_scale), _ptr(out), _ptr(lse),
         _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def qs_attn_decode_static_ws(cache, mode, q, softmax_scale, out, lse=None, stream=None):
+    """qs_attn_decode with its scratch in the library's fixed device array
+    (for callers that cannot allocate device memory); q, out, lse as for
+    qs_attn_decode.  Returns the status instead of raising on
+    QS_ERR_TOO_LARGE, so a caller can fall back to the allocating call."""
+    n_q = q.shape[2]
+    status = lib().qs_attn_decode_static_ws(cache._ref, int(mode), _ptr(q), n_q,
+                                            float(softmax_scale), _ptr(out), _ptr(lse),
+                                            _stream(stream))
+    if status != QS_ERR_TOO_LARGE:
+        _check("qs_attn_decode_static_ws", status)
+    return status
 
 
 def qs_get_errors(cache, stream=None):

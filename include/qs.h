@@ -165,12 +165,16 @@ typedef struct {
 
 /* Byte size of every cache array for the given dimensions.  Pure host
  * function.  Errors: QS_ERR_ARG (null out, non-positive sizes),
- * QS_ERR_UNSUPPORTED (D or G != 128). */
+ * QS_ERR_UNSUPPORTED (D or G != 128).  The sizes follow the layout above;
+ * the pages fix the planes' contents (Pith review page, "What carries the
+ * argument": C_U and C_L per group with a shared scale and zero-point; the
+ * double buffer of two halves of G tokens), not a memory layout. */
 qs_status qs_cache_bytes(int32_t B, int32_t H, int32_t D, int32_t G, int32_t cap_groups,
                          qs_cache_bytes_t *out);
 
 /* Zero every sequence's counters (empty cache) and the attention arrival
- * counters.  Asynchronous memsets. */
+ * counters.  Asynchronous memsets.  No counterpart on the pages: it is this
+ * library's initialisation of its device-resident bookkeeping. */
 qs_status qs_state_reset(const qs_cache *c, qs_stream_t stream);
 
 /* Append n_new tokens per sequence to the fp16 buffer as pending tokens.
@@ -190,7 +194,13 @@ qs_status qs_buffer_append(const qs_cache *c, const uint16_t *k_new, const uint1
 qs_status qs_buffer_rollback(const qs_cache *c, const int32_t *d_n_drop, qs_stream_t stream);
 
 /* d_mask[b] = 1 if appending n_next more tokens would exceed 2G, else 0.
- * d_mask: uint8 [B] device array.  Feed it to qs_quantize_flush. */
+ * d_mask: uint8 [B] device array, written by the call (caller-owned).
+ * Feed it to qs_quantize_flush before the append.  Host errors: QS_ERR_ARG
+ * (null mask, negative n_next).  Source: Pith review page, "What
+ * carries the argument": a buffer half is quantized once every G decoding
+ * steps.  The pages do not say at which point of a round; this library
+ * flushes right before an append that would overflow the 2G buffer, when the
+ * oldest half is fully committed as long as n_next <= G / 2. */
 qs_status qs_need_flush(const qs_cache *c, int32_t n_next, uint8_t *d_mask, qs_stream_t stream);
 
 /* Quantize-on-flush.  For every sequence with d_mask[b] != 0 (all when
@@ -257,7 +267,9 @@ qs_status qs_spec_accept(const float *p, const float *q, const int32_t *draft, c
                          int32_t *token, int32_t *n_drop, qs_stream_t stream);
 
 /* Bytes of device workspace qs_attn_decode needs for n_q queries (1..8) on
- * the current device.  Pure host function (reads device attributes). */
+ * the current device.  Pure host function (reads device attributes).  The
+ * workspace holds the split-KV partials of Flash Decoding (Pith review page,
+ * Appendix E); its size is this implementation's, not the pages'. */
 qs_status qs_attn_workspace_size(const qs_cache *c, int32_t n_q, size_t *bytes);
 
 /* Split-KV decode attention over the quantized groups and the fp16 buffer.
@@ -315,8 +327,11 @@ qs_status qs_attn_decode_gqa(const qs_cache *c, qs_mode mode, const uint16_t *q,
  *  - a problem whose qs_attn_workspace_size exceeds QS_STATIC_WS_BYTES returns
  *    QS_ERR_TOO_LARGE before launching anything;
  *  - the first call on a device looks up the array's device address (with
- *    that device current) and caches it; make that first call before any
- *    stream capture;
+ *    that device current) and caches it together with the identity of the
+ *    current CUDA context; make that first call before any stream capture.
+ *    A call under another context of the same device (after cudaDeviceReset,
+ *    or a context made current through the driver API) looks the address up
+ *    again, so make its first call before capture too;
  *  - every call on a device uses the same array: calls that overlap on the
  *    GPU (other streams, other threads) race and corrupt each other's
  *    results; order them on one stream.  The array needs no clearing: every
@@ -326,7 +341,8 @@ qs_status qs_attn_decode_static_ws(const qs_cache *c, qs_mode mode, const uint16
                                    qs_stream_t stream);
 
 /* Copy every sequence's error word to h_err (int32 [B], host memory) and
- * clear them on the device.  Synchronizes the stream. */
+ * clear them on the device.  Synchronizes the stream.  No counterpart on the
+ * pages: it reports the device-side precondition failures of the calls above. */
 qs_status qs_get_errors(const qs_cache *c, int32_t *h_err, qs_stream_t stream);
 
 /* Human-readable name of a status code (static string). */

@@ -90,3 +90,60 @@ def test_32k_round_bytes():
            + bench.attn_bytes(ng1, f1 + bench.GAMMA + 1, bench.GAMMA + 1, False, H)
            + bench.append_bytes(bench.GAMMA, H) + bench.append_bytes(bench.GAMMA + 1, H))
     assert got == total
+
+
+def _seq_draft(ng, fill, H):
+    return H * (ng * G * 136 + fill * 2 * ROW + 2 * ROW)
+
+
+def _seq_verify(ng, fill, H, n_q=5):
+    return H * (ng * G * 264 + fill * 2 * ROW + n_q * 2 * ROW)
+
+
+def test_round_plan_counts_each_sequence_from_its_own_counters():
+    """A batch whose sequences differ: only those whose buffer cannot take
+    the five target tokens (fill + 5 > 2G) flush, and each sequence's drafts
+    and verify read its own groups and buffered tokens."""
+    H = 2
+    ng0, f0 = [10, 3, 0, 7], [256, 40, 251, 252]
+    p = bench.round_plan(ng0, f0, H)
+    assert list(p["mask"]) == [1, 0, 0, 1]
+    assert list(p["ng1"]) == [11, 3, 0, 8] and list(p["f1"]) == [128, 40, 251, 124]
+    assert p["bytes"]["flush"] == 2 * H * (2 * G * ROW + G * (4 * (D // 2) + META_PER_TOKEN))
+    for i in range(4):
+        assert p["bytes"]["draft"][i] == sum(_seq_draft(n, f + i + 1, H)
+                                             for n, f in zip(p["ng1"], p["f1"]))
+    assert p["bytes"]["verify"] == sum(_seq_verify(n, f + 5, H) for n, f in zip(p["ng1"], p["f1"]))
+    assert p["bytes"]["append"] == 4 * H * 9 * (2 * ROW + 2 * ROW)  # 4 sequences, 9 tokens
+    assert p["step"] == (p["bytes"]["flush"] + sum(p["bytes"]["draft"]) + p["bytes"]["verify"]
+                         + p["bytes"]["append"])
+
+
+def test_ragged_and_batched_rounds():
+    """The ragged workload (16 sequences, contexts 4k..64k, fill 1..256) and
+    the batched one (8 x 32k): bytes summed over sequences from their own
+    counters, flushes only where due."""
+    from hierarchical_quantized_kv_gb300 import synthetic
+    for w in (synthetic.ragged(), synthetic.batched_32k()):
+        p = bench.round_plan(w.n_groups, w.fill, w.H)
+        due = [f + 5 > 2 * G for f in w.fill]
+        assert list(p["mask"]) == [int(x) for x in due]
+        ng1 = [n + d for n, d in zip(w.n_groups, due)]
+        f1 = [f - G * d for f, d in zip(w.fill, due)]
+        want_draft = sum(_seq_draft(n, f + 1, w.H) for n, f in zip(ng1, f1))
+        assert p["bytes"]["draft"][0] == want_draft
+        assert p["bytes"]["verify"] == sum(_seq_verify(n, f + 5, w.H) for n, f in zip(ng1, f1))
+        assert p["bytes"]["flush"] == sum(due) * w.H * bench.FLUSH_BYTES_PER_HEAD
+    w = synthetic.ragged()
+    assert 0 < sum(f + 5 > 2 * G for f in w.fill) < w.B   # some flush, some do not
+    # the 32k round seen through the plan: the bench line's 858,292,224 bytes
+    w = synthetic.llama_32k()
+    assert bench.round_plan(w.n_groups, w.fill, w.H)["step"] == 858_292_224
+
+
+def test_oracle_sample_bytes():
+    """The CPU baseline's sample: sequence 0's counters on the sampled heads."""
+    from hierarchical_quantized_kv_gb300 import synthetic
+    w = synthetic.llama_32k()
+    assert bench.sample_step_bytes(w, 32) == 858_292_224
+    assert bench.sample_step_bytes(w, 16) * 2 == 858_292_224

@@ -9,8 +9,6 @@ test calls it through the C ABI, twice in a row, and checks each result
 against qs_attn_decode on the same inputs, within the parity tolerance of the
 other tests.  This file is named to be collected last.
 """
-import ctypes
-
 import numpy as np
 import pytest
 
@@ -31,15 +29,8 @@ def torch():
 
 
 def _static_call(torch, cache, mode, q, scale, out, lse):
-    L = qs.lib()
-    f = L.qs_attn_decode_static_ws
-    f.argtypes = [ctypes.POINTER(qs.QsCacheStruct), ctypes.c_int, ctypes.c_void_p, ctypes.c_int32,
-                  ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
-    f.restype = ctypes.c_int
-    return f(cache._ref, mode, ctypes.c_void_p(q.data_ptr()), q.shape[2], ctypes.c_float(scale),
-             ctypes.c_void_p(out.data_ptr()),
-             None if lse is None else ctypes.c_void_p(lse.data_ptr()),
-             ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    # through the C ABI (ctypes marshalling in the binding); returns the status
+    return qs.qs_attn_decode_static_ws(cache, mode, q, scale, out, lse)
 
 
 def test_static_workspace_matches_allocating_call(torch):
