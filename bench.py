@@ -367,9 +367,14 @@ def fast_prefill(torch, qs, synthetic, cache, w):
 class Round:
     """Device state and inputs of the benchmark step on one GPU."""
 
-    def __init__(self, torch, w, seed, upper_bits=4):
+    def __init__(self, torch, w, seed, upper_bits=4, fused=True):
+        """fused: the flush decides its own mask (qs_quantize_flush_due) and
+        each attention call takes its appended tokens in the same launch
+        (qs_attn_decode_append); else qs_need_flush, qs_quantize_flush and
+        separate qs_buffer_append calls."""
         from hierarchical_quantized_kv_gb300 import qs, synthetic
         self.torch, self.qs, self.w = torch, qs, w
+        self.fused = fused
         dev = torch.device("cuda")
         B, H, D = w.B, w.H, w.D
         self.cache = qs.Cache(B, H, max(w.n_groups) + 2, upper_bits=upper_bits)
@@ -421,13 +426,16 @@ class Round:
         self.ng1, self.f1 = self.plan["ng1"], self.plan["f1"]
         self.bytes = self.plan["bytes"]
         self.step_bytes = self.plan["step"]
-        # need_flush, flush, GAMMA x (append, draft), rollback, append, verify, rollback
-        self.launches_per_step = 2 + GAMMA * 2 + 1 + 1 + 1 + 1
+        # (need_flush +) flush, GAMMA x (append +) draft, rollback, (append +) verify, rollback
+        self.launches_per_step = (1 if fused else 2) + GAMMA * (1 if fused else 2) + 1 + \
+            (1 if fused else 2) + 1
 
-    def step(self, s, host=None, ev=None, external=False):
+    def step(self, s, host=None, ev=None, external=False, extra=None):
         """One speculative round.  ev: a list that receives (kind, start, end)
         CUDA events recorded around each attention call (as graph nodes when
-        the step is captured with external=True)."""
+        the step is captured with external=True).  extra = "draft" or
+        "verify": one more such attention call (without an append) right
+        after each of that kind, for the marginal in-step time."""
         qs, c = self.qs, self.cache
         torch = self.torch
         if ev is not None:
@@ -446,16 +454,35 @@ class Round:
 
         if host is not None:
             host.h2d(self)
-        qs.qs_need_flush(c, GAMMA + 1, self.mask)
-        qs.qs_quantize_flush(c, self.mask)
+        if self.fused:  # the sequences that cannot take the gamma + 1 targets flush
+            qs.qs_quantize_flush_due(c, GAMMA + 1)
+        else:
+            qs.qs_need_flush(c, GAMMA + 1, self.mask)
+            qs.qs_quantize_flush(c, self.mask)
         for i in range(GAMMA):
-            qs.qs_buffer_append(c, self.kd[i], self.vd[i])
-            timed("draft", lambda i=i: qs.qs_attn_decode(c, qs.QS_DRAFT_UPPER4, self.qd[i], self.scale,
-                                                         self.od[i], None, self.ws))
+            if self.fused:  # append the draft token and attend in one launch
+                timed("draft", lambda i=i: qs.qs_attn_decode_append(
+                    c, qs.QS_DRAFT_UPPER4, self.kd[i], self.vd[i], self.qd[i], self.scale,
+                    self.od[i], None, self.ws))
+                if extra == "draft":
+                    qs.qs_attn_decode(c, qs.QS_DRAFT_UPPER4, self.qd[i], self.scale, self.od[i],
+                                      None, self.ws)
+            else:
+                qs.qs_buffer_append(c, self.kd[i], self.vd[i])
+                timed("draft", lambda i=i: qs.qs_attn_decode(c, qs.QS_DRAFT_UPPER4, self.qd[i],
+                                                             self.scale, self.od[i], None, self.ws))
         qs.qs_buffer_rollback(c, self.drop_draft)
-        qs.qs_buffer_append(c, self.kt, self.vt)
-        timed("verify", lambda: qs.qs_attn_decode(c, qs.QS_VERIFY_INT8, self.qv, self.scale, self.ov,
-                                                  self.lse, self.ws))
+        if self.fused:
+            timed("verify", lambda: qs.qs_attn_decode_append(
+                c, qs.QS_VERIFY_INT8, self.kt, self.vt, self.qv, self.scale, self.ov, self.lse,
+                self.ws))
+            if extra == "verify":
+                qs.qs_attn_decode(c, qs.QS_VERIFY_INT8, self.qv, self.scale, self.ov, self.lse,
+                                  self.ws)
+        else:
+            qs.qs_buffer_append(c, self.kt, self.vt)
+            timed("verify", lambda: qs.qs_attn_decode(c, qs.QS_VERIFY_INT8, self.qv, self.scale,
+                                                      self.ov, self.lse, self.ws))
         qs.qs_buffer_rollback(c, self.drops[s % len(self.drops)])
         c.state.copy_(self.state0)
         if host is not None:
@@ -566,6 +593,23 @@ def in_step_launch_times(torch, r, n_rep):
         how = "CUDA events around each attention call in %d eager steps" % (n_rep - 2)
     r.cache.state.copy_(r.state0)
     return launch, how
+
+
+def marginal_us(torch, r, kind, base_graphs, n, rounds=3):
+    """Marginal device time of one attention call of `kind` inside the step
+    (programmatic dependent launch overlap included): the step's graphs and
+    the same step with one more such call after each one, replayed n times
+    each, alternately; the least difference of the per-step times over the
+    rounds, per added call."""
+    extra = [capture(torch, lambda s=s: r.step(s, extra=kind)) for s in range(len(r.drops))]
+    per_step = GAMMA if kind == "draft" else 1
+    diffs = []
+    for _ in range(rounds):
+        a = replay_us(torch, base_graphs, n)
+        b = replay_us(torch, extra, n)
+        diffs.append((b - a) / per_step)
+    r.cache.state.copy_(r.state0)
+    return min(diffs)
 
 
 def replay_us(torch, graphs, n):
@@ -789,6 +833,10 @@ def native(args):
     launch, launch_how = in_step_launch_times(torch, r, max(12, min(args.steps, 60)))
     draft_launch_us = float(np.mean(launch["draft"]))
     verify_launch_us = float(np.mean(launch["verify"]))
+    draft_marg_us = verify_marg_us = None
+    if r.fused:
+        draft_marg_us = marginal_us(torch, r, "draft", graphs, max(100, args.steps))
+        verify_marg_us = marginal_us(torch, r, "verify", graphs, max(100, args.steps))
     draft_b_mean = float(np.mean(r.bytes["draft"]))
     # dominant kernel by device time within a step
     dominant = ("draft", draft_b_mean / draft_launch_us / 1e3, draft_launch_us) \
@@ -823,6 +871,7 @@ def native(args):
     errs = qs.qs_get_errors(r.cache)
     assert np.all(errs == 0), errs
     step_bytes, flushing = r.step_bytes, int(r.plan["mask"].sum())
+    launches = r.launches_per_step
     ng_att = int(np.max(r.ng1))
     del r
     torch.cuda.empty_cache()
@@ -853,6 +902,8 @@ def native(args):
                          "L2 evicted before each call by a 256 MB read" % (step_bytes / 1e6),
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "draft_in_step_us": round(draft_launch_us, 2), "verify_in_step_us": round(verify_launch_us, 2),
+        "draft_marginal_us": None if draft_marg_us is None else round(draft_marg_us, 2),
+        "verify_marginal_us": None if verify_marg_us is None else round(verify_marg_us, 2),
         "draft_us": round(draft_us, 2), "draft_gbs": round(draft_gbs, 1),
         "verify_us": round(verify_us, 2), "verify_gbs": round(verify_gbs, 1),
         "flush_us": round(flush_us, 2),
@@ -866,19 +917,30 @@ def native(args):
                      "launch_timing": launch_how + " (mean of %d calls)" % len(launch[dominant[0]]),
                      "achieved": round(dominant[1], 1), "peak": peak,
                      "peak_kind": "%s hbm_gbs (copy, burst)" % peak_kind, "unit": "GB/s",
-                     "frac": round(dominant[1] / peak, 4), "traffic": stored_traffic(dominant[0])},
+                     "frac": round(dominant[1] / peak, 4), "traffic": stored_traffic(dominant[0]),
+                     "marginal_us": None if draft_marg_us is None else
+                     round(draft_marg_us if dominant[0] == "draft" else verify_marg_us, 2),
+                     "marginal_frac": None if draft_marg_us is None else
+                     round((draft_b_mean if dominant[0] == "draft" else verify_b)
+                           / (draft_marg_us if dominant[0] == "draft" else verify_marg_us)
+                           / 1e3 / peak, 4),
+                     "marginal_timing": "the step's graphs against the same step with one more "
+                                        "such call after each, graph-replayed; difference per "
+                                        "added call (overlap of consecutive launches included)"},
         "e2e": {"value": round(aggregate_gbs(step_bytes, world, e2e_ms), 1), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": host.h2d_bytes,
                 "d2h_bytes_per_step": host.d2h_bytes,
                 "how": "every step: one pinned H2D copy of the step's inputs, the step's %d calls "
                        "through the C ABI (ctypes, no graph), one D2H copy of its outputs, a host "
-                       "wait" % 14},
+                       "wait" % launches},
         "e2e_graph": {"value": round(aggregate_gbs(step_bytes, world, e2e_graph_ms), 1),
                       "unit": "GB/s", "ms_per_step": round(e2e_graph_ms, 4),
                       "how": "the same step, copies included, replayed from a CUDA graph"},
         "configs": configs,
-        "gpu_launches": 14 * args.steps,
-        "launch": "CUDA graph replay of each step (one graph per distinct step)",
+        "gpu_launches": launches * args.steps,
+        "launch": "CUDA graph replay of each step (one graph per distinct step); the flush "
+                  "decides its own mask and each attention call appends its tokens in the same "
+                  "launch (qs_quantize_flush_due, qs_attn_decode_append)",
         "clocks": clocks,
     }
     if cpu is not None:

@@ -12,6 +12,10 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libqs.so")
+# the checked build (-DQS_CHECKED=1): device-side bounds checks that count
+# failures instead of trapping; used by the tests, never by the product path
+BUILD_CHECKED = os.path.join(HERE, "_build_checked")
+LIB_CHECKED = os.path.join(HERE, "libqs_checked.so")
 SOURCES = ["qs_buffer.cu", "qs_quantize.cu", "qs_attn.cu", "qs_attn_static.cu", "qs_spec.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC = os.environ.get("NVCC", "nvcc")
@@ -26,17 +30,21 @@ def _stale(target, deps):
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(verbose=False, force=False):
-    os.makedirs(BUILD, exist_ok=True)
+def build(verbose=False, force=False, checked=False):
+    """Compile every translation unit for sm_103a and link libqs.so (with
+    checked=True: the bounds-checked variant, libqs_checked.so)."""
+    build_dir, lib = (BUILD_CHECKED, LIB_CHECKED) if checked else (BUILD, LIB)
+    extra = ["-DQS_CHECKED=1"] if checked else []
+    os.makedirs(build_dir, exist_ok=True)
     headers = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cuh")]
     headers.append(os.path.join(os.path.dirname(HERE), "include", "qs.h"))
     objs, jobs = [], []
     for s in SOURCES:
         src = os.path.join(CSRC, s)
-        obj = os.path.join(BUILD, s.replace(".cu", ".o"))
+        obj = os.path.join(build_dir, s.replace(".cu", ".o"))
         objs.append(obj)
         if force or _stale(obj, [src] + headers):
-            cmd = [NVCC] + ARCH + FLAGS + (["-Xptxas", "-v"] if verbose else []) + \
+            cmd = [NVCC] + ARCH + FLAGS + extra + (["-Xptxas", "-v"] if verbose else []) + \
                 ["-c", src, "-o", obj]
             jobs.append(cmd)
 
@@ -50,15 +58,15 @@ def build(verbose=False, force=False):
                 sys.stderr.write(r.stderr)
             if r.returncode != 0:
                 raise RuntimeError("nvcc failed: %s\n%s%s" % (" ".join(cmd), r.stdout, r.stderr))
-    if force or jobs or _stale(LIB, objs):
-        tmp = LIB + ".tmp%d" % os.getpid()
+    if force or jobs or _stale(lib, objs):
+        tmp = lib + ".tmp%d" % os.getpid()
         cmd = [NVCC] + ARCH + ["-shared", "-o", tmp] + objs + ["-lcudart"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError("link failed: %s\n%s%s" % (" ".join(cmd), r.stdout, r.stderr))
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(verbose="-v" in sys.argv, force="-f" in sys.argv))
+    print(build(verbose="-v" in sys.argv, force="-f" in sys.argv, checked="--checked" in sys.argv))

@@ -85,8 +85,8 @@ struct Layout {
   static constexpr int kZeroOff = align16(kIssOff + 4 * Cfg<MODE>::kStages);     // zero row (ldmatrix)
   static constexpr int kTabOff = kZeroOff + 32;
   // per-sequence tables: n_groups, fill, half_base, segment length, base
-  // unit, first segment ordinal
-  static constexpr int kSmemBytes = kTabOff + 6 * kMaxB * 4;
+  // unit, first segment ordinal, fill before a fused append
+  static constexpr int kSmemBytes = kTabOff + 7 * kMaxB * 4;
   static_assert(kStageBytes % 16 == 0 && kBarOff % 16 == 0 && kZeroOff % 16 == 0,
                 "bulk copies and ldmatrix rows need 16-byte aligned shared memory");
 };
@@ -105,24 +105,33 @@ struct Params {
   float sl2;  // softmax_scale * log2(e)
   uint64_t wait_ns;  // limit on each pipeline wait (kWaitLimitNs outside tests)
   int no_issue;      // test entry only: issue no copy, so that every wait runs out
+  // append fused in front of the attention (n_new > 0): fp16 [B][H][n_new][D]
+  // tokens that enter the buffer before the queries attend
+  const uint16_t *k_new, *v_new;
+  int n_new;
+  size_t ws_floats;  // workspace size (the checked build bounds its indexing by it)
 };
 
 struct Tables {
   int *ng, *fill, *hb, *len, *base;  // base in units, len in units per head
   int *ord0;  // ordinal of (b, head 0) among the segments that have units
+  int *fold;  // buffered tokens before a fused append (fill - n_new, or fill)
 };
 
 __device__ __forceinline__ Tables tables_at(uint8_t *smem, int off) {
   int *t = reinterpret_cast<int *>(smem + off);
-  return Tables{t, t + kMaxB, t + 2 * kMaxB, t + 3 * kMaxB, t + 4 * kMaxB, t + 5 * kMaxB};
+  return Tables{t, t + kMaxB, t + 2 * kMaxB, t + 3 * kMaxB, t + 4 * kMaxB, t + 5 * kMaxB,
+                t + 6 * kMaxB};
 }
 
 // Warp-cooperative: read counters, segment lengths (units per head), the
 // exclusive prefix of units (x H) and the ordinal of each sequence's first
 // segment (segments of sequences without units are skipped) into the tables.
-// Returns the total number of units.
+// With a fused append of n_new tokens, a sequence whose buffer can take them
+// attends over fill + n_new tokens (the others over fill: their append fails,
+// as a separate append would).  Returns the total number of units.
 template <int TT>
-__device__ long long build_tables(const qs_cache &c, int n_q, Tables T, int lane) {
+__device__ long long build_tables(const qs_cache &c, int n_q, int n_new, Tables T, int lane) {
   const int per = (c.B + 31) / 32;
   const int b0 = lane * per;
   int local = 0, local_ne = 0;
@@ -132,9 +141,12 @@ __device__ long long build_tables(const qs_cache &c, int n_q, Tables T, int lane
       const int32_t *st = c.state + (size_t)b * QS_STATE_WORDS;
       // clamped so that no counter value can address outside the arrays
       const int ng = min(max(st[QS_ST_N_GROUPS], 0), c.cap_groups);
-      const int fill = min(max(st[QS_ST_FILL], 0), kRing);
+      const int fill_raw = st[QS_ST_FILL];
+      const int fold = min(max(fill_raw, 0), kRing);
+      const int fill = (n_new > 0 && fill_raw >= 0 && fill_raw + n_new <= kRing) ? fold + n_new : fold;
       T.ng[b] = ng;
       T.fill[b] = fill;
+      T.fold[b] = fold;
       T.hb[b] = st[QS_ST_HALF_BASE] & 1;
       const int len = (n_q <= fill) ? ng + (fill + TT - 1) / TT : 0;
       T.len[b] = len;
@@ -289,16 +301,19 @@ __device__ __forceinline__ uint32_t upper_from2(uint32_t u, uint32_t m, int sh) 
 }
 
 __device__ __forceinline__ uint32_t lds32(uint32_t a) {
+  if (!chk(smem_in(a, 4), 1)) return 0;
   uint32_t v;
   asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(a));
   return v;
 }
 __device__ __forceinline__ uint2 lds64(uint32_t a) {
+  if (!chk(smem_in(a, 8), 1)) return make_uint2(0, 0);
   uint2 v;
   asm volatile("ld.shared.v2.b32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
   return v;
 }
 __device__ __forceinline__ uint4 lds128(uint32_t a) {
+  if (!chk(smem_in(a, 16), 1)) return make_uint4(0, 0, 0, 0);
   uint4 v;
   asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
@@ -385,16 +400,29 @@ __device__ __forceinline__ void load_q_pairs(const uint16_t *qrow, bool valid, i
 // A two-bit draft copies only the C_U2 half (4 KB) of each upper plane into
 // the stage's upper slots; verify copies both halves (the slots' layout is
 // then C_U2 | M2 instead of C_U).
+__device__ __forceinline__ uint8_t *prm_smem_base() {
+  extern __shared__ __align__(128) uint8_t qs_dyn_smem[];
+  return qs_dyn_smem;
+}
+
+// With a fused append, buffer rows at or past the old fill come straight
+// from the appended tokens (the ring gets them in the same launch, not read
+// back here).
 template <int MODE, int UB>
-__device__ __forceinline__ void issue_unit(const qs_cache &c, const Tables &T, const Seg &cu,
+__device__ __forceinline__ void issue_unit(const Params &prm, const Tables &T, const Seg &cu,
                                            uint32_t dst, uint32_t bar, int lane) {
+  const qs_cache &c = prm.c;
   using C = Cfg<MODE>;
   constexpr int TT = C::kTailTok;
   const size_t bh = (size_t)cu.b * c.H + cu.h;
   const int ng = T.ng[cu.b];
   if (cu.u < ng) {
     if (lane == 0) {
-      const size_t grp = bh * c.cap_groups + cu.u;
+      size_t grp = bh * c.cap_groups + cu.u;
+      // checked build: a copy out of bounds reads group 0 (and lands in the
+      // stage's start) instead, so its barrier still completes
+      if (!chk(in_range(grp, 1, (size_t)c.B * c.H * c.cap_groups), 3)) grp = 0;
+      if (!chk(smem_in(dst, C::kGroupBytes), 2)) dst = smem_addr(prm_smem_base());
       const uint64_t pol = l2_evict_first_policy();  // planes are read once per call
       constexpr int kUp = (MODE == QS_DRAFT_UPPER4 && UB == 2) ? 4096 : 8192;
       mbar_arrive_expect_tx(bar, C::kGroupBytes - 2 * (8192 - kUp));
@@ -412,12 +440,27 @@ __device__ __forceinline__ void issue_unit(const qs_cache &c, const Tables &T, c
     if (lane == 0) mbar_arrive_expect_tx(bar, rows * 2 * kD * 2);
     __syncwarp();
     const int slot0 = T.hb[cu.b] * kG + i0;  // chunks never straddle the ring end
+    const int fold = T.fold[cu.b];
     for (int rr = lane; rr < 2 * rows; rr += 32) {
       const bool isv = rr >= rows;
       const int row = isv ? rr - rows : rr;
-      const int slot = (slot0 + row) & (kRing - 1);
-      const uint16_t *src = (isv ? c.buf_v : c.buf_k) + (bh * kRing + slot) * kD;
-      bulk_g2s(dst + (isv ? TT * kTailRow : 0) + row * kTailRow, src, kD * 2, bar);
+      const uint16_t *src;
+      if (i0 + row < fold) {
+        const int slot = (slot0 + row) & (kRing - 1);
+        src = (isv ? c.buf_v : c.buf_k) + (bh * kRing + slot) * kD;
+      } else {
+        src = (isv ? prm.v_new : prm.k_new) + (bh * prm.n_new + (i0 + row - fold)) * kD;
+      }
+      uint32_t d = dst + (isv ? TT * kTailRow : 0) + row * kTailRow;
+      if (!chk(smem_in(d, kD * 2), 2)) d = smem_addr(prm_smem_base());
+      if (QS_CHECKED) {
+        const size_t ring_rows = (size_t)c.B * c.H * kRing, new_rows = (size_t)c.B * c.H * prm.n_new;
+        const bool ok = i0 + row < fold
+                            ? in_range((size_t)(src - (isv ? c.buf_v : c.buf_k)) / kD, 1, ring_rows)
+                            : in_range((size_t)(src - (isv ? prm.v_new : prm.k_new)) / kD, 1, new_rows);
+        if (!chk(ok, 4)) src = isv ? c.buf_v : c.buf_k;
+      }
+      bulk_g2s(d, src, kD * 2, bar);
     }
   }
 }
@@ -425,6 +468,9 @@ __device__ __forceinline__ void issue_unit(const qs_cache &c, const Tables &T, c
 // Device-scope fence between a CTA's partials and its arrival on a segment
 // counter (release), and between the arrival that completes a segment and
 // the reads of the other CTAs' partials (acquire).
+#ifndef QS_MERGE_KS
+#define QS_MERGE_KS 1  // > 1: merges split each row's partials over up to this many lanes
+#endif
 #ifndef QS_FENCE_AR
 #define QS_FENCE_AR 0
 #endif
@@ -485,6 +531,101 @@ __device__ __forceinline__ float4 ld_part4(const float *p) {
 // warp's reads.  Not inlined: it runs once or twice per launch, at the end,
 // where every instruction is fetched cold, so one small shared copy matters
 // more than the call.
+#if QS_MERGE_KS > 1
+__device__ __noinline__ void merge_rows(const float *srcA, int cgA, int kstrideA, int nA,
+                                        const float *srcB, int cgB, int kstrideB, int ns, int R,
+                                        const MergeOut &mo) {
+  // items (row j, four channels c4), the partials of an item split over ks
+  // adjacent lanes that combine by shuffles at the end
+  constexpr int kBatch = 4;
+  const int items = R * 32;
+  int ks = 1;
+  while (ks < QS_MERGE_KS && items * ks * 2 <= (int)blockDim.x) ks *= 2;
+  const int mo_off = R * kD;
+#pragma unroll 1
+  for (int base = 0; base < items * ks; base += blockDim.x) {
+    const int t = base + threadIdx.x;
+    const bool valid = t < items * ks;
+    const int item = t / ks, kq = t & (ks - 1);
+    const int j = valid ? item >> 5 : 0, c4 = item & 31;
+    const float *a0 = srcA + (j >> 3) * cgA, *b0 = srcB + (j >> 3) * cgB;
+    float M = -INFINITY, L = 0.f;
+    float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 1
+    for (int kb = kq; valid && kb < ns; kb += ks * kBatch) {
+      float ms[kBatch], ls[kBatch];
+      float4 os[kBatch];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int k = kb + u * ks;
+        ms[u] = -INFINITY;
+        ls[u] = 0.f;
+        os[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (k < ns) {
+          const float *sk = k < nA ? a0 + k * kstrideA : b0 + (k - nA) * kstrideB;
+          ms[u] = ld_part(sk + mo_off + j);
+          ls[u] = ld_part(sk + mo_off + kMaxR + j);
+          os[u] = ld_part4(sk + j * kD + 4 * c4);
+        }
+      }
+      float mn = M;
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) mn = fmaxf(mn, ms[u]);
+      if (mn == -INFINITY) continue;
+      const float a = (M == -INFINITY) ? 0.f : fast_exp2(M - mn);
+      L *= a;
+      A.x *= a; A.y *= a; A.z *= a; A.w *= a;
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const bool use = ms[u] > -INFINITY;  // an empty partial's l and O stay out
+        const float f = use ? fast_exp2(ms[u] - mn) : 0.f;
+        L = fmaf(f, use ? ls[u] : 0.f, L);
+        A.x = fmaf(f, use ? os[u].x : 0.f, A.x);
+        A.y = fmaf(f, use ? os[u].y : 0.f, A.y);
+        A.z = fmaf(f, use ? os[u].z : 0.f, A.z);
+        A.w = fmaf(f, use ? os[u].w : 0.f, A.w);
+      }
+      M = mn;
+    }
+#pragma unroll 1
+    for (int o = 1; o < ks; o <<= 1) {
+      const float M2 = __shfl_xor_sync(0xffffffffu, M, o), L2 = __shfl_xor_sync(0xffffffffu, L, o);
+      float4 A2;
+      A2.x = __shfl_xor_sync(0xffffffffu, A.x, o);
+      A2.y = __shfl_xor_sync(0xffffffffu, A.y, o);
+      A2.z = __shfl_xor_sync(0xffffffffu, A.z, o);
+      A2.w = __shfl_xor_sync(0xffffffffu, A.w, o);
+      const float mn = fmaxf(M, M2);
+      if (mn != -INFINITY) {
+        const float a = M == -INFINITY ? 0.f : fast_exp2(M - mn);
+        const float a2 = M2 == -INFINITY ? 0.f : fast_exp2(M2 - mn);
+        L = L * a + L2 * a2;
+        A.x = A.x * a + A2.x * a2;
+        A.y = A.y * a + A2.y * a2;
+        A.z = A.z * a + A2.z * a2;
+        A.w = A.w * a + A2.w * a2;
+        M = mn;
+      }
+    }
+    if (valid && kq == 0) {
+      if (mo.final) {
+        const float Ld = L > 0.f ? L : 1.f;
+        uint2 h;
+        h.x = pack_half2(A.x / Ld, A.y / Ld);
+        h.y = pack_half2(A.z / Ld, A.w / Ld);
+        *reinterpret_cast<uint2 *>(mo.out + j * kD + 4 * c4) = h;
+        if (mo.lse && c4 == 0) mo.lse[j] = (M + log2f(L)) * 0.69314718055994531f;
+      } else {
+        reinterpret_cast<float4 *>(mo.dst + j * kD)[c4] = A;
+        if (c4 == 0) {
+          mo.dst[mo_off + j] = M;
+          mo.dst[mo_off + kMaxR + j] = L;
+        }
+      }
+    }
+  }
+}
+#else
 __device__ __noinline__ void merge_rows(const float *srcA, int cgA, int kstrideA, int nA,
                                         const float *srcB, int cgB, int kstrideB, int ns, int R,
                                         const MergeOut &mo) {
@@ -558,6 +699,7 @@ __device__ __noinline__ void merge_rows(const float *srcA, int cgA, int kstrideA
     }
   }
 }
+#endif
 
 // One warp's partial of a piece (unnormalized, log2 domain; m = -inf if the
 // warp saw no visible token; O as accumulated times oscale, plus the value
@@ -650,7 +792,7 @@ __global__ void __launch_bounds__(NW * 32, 1) split_kernel(const Params prm) {
   pdl_trigger();
   pdl_wait();  // counters, cache and queries are written by earlier kernels
   if (w == 0) {
-    const long long tot = build_tables<TT>(c, prm.n_q, T, lane);
+    const long long tot = build_tables<TT>(c, prm.n_q, prm.n_new, T, lane);
     if (lane == 0) s_total = tot;
   }
   __syncthreads();
@@ -658,6 +800,41 @@ __global__ void __launch_bounds__(NW * 32, 1) split_kernel(const Params prm) {
   const int p = blockIdx.x;
   const int R = prm.R, ncg = prm.ncg, cg = w % ncg;  // this warp's column group
   const int stride = R * kD + 2 * kMaxR;             // floats per partial
+
+  if (prm.n_new > 0 && w == NW - 1) {
+    // The fused append, by a warp that issues no first copy.  Every CTA has
+    // read the counters above; the CTA whose ticket comes last commits the
+    // appended counters (no CTA of this launch reads them again).  The new
+    // tokens enter the ring slots past the old fill, which no CTA of this
+    // launch reads (its copies of those rows come from k_new / v_new).
+    if (lane == 0 && atomicAdd(&c.state[QS_ST_TICKET], 1) == (int)gridDim.x - 1) {
+      for (int b = 0; b < c.B; ++b) {
+        int32_t *st = c.state + (size_t)b * QS_STATE_WORDS;
+        if (T.fill[b] != T.fold[b]) {
+          st[QS_ST_FILL] = T.fill[b];
+          st[QS_ST_PENDING] += prm.n_new;
+        } else {
+          st[QS_ST_ERR] |= QS_DEV_OVERFLOW;  // as a separate append would: no-op
+        }
+      }
+      c.state[QS_ST_TICKET] = 0;
+    }
+    constexpr int kRowVec = kD * 2 / 16;  // uint4 per fp16 row
+    for (int j = p; j < c.B * c.H; j += gridDim.x) {
+      const int b = j / c.H;
+      if (T.fill[b] == T.fold[b]) continue;  // this sequence's append failed
+      const int slot0 = T.hb[b] * kG + T.fold[b];
+      const uint4 *sk = reinterpret_cast<const uint4 *>(prm.k_new) + (size_t)j * prm.n_new * kRowVec;
+      const uint4 *sv = reinterpret_cast<const uint4 *>(prm.v_new) + (size_t)j * prm.n_new * kRowVec;
+      uint4 *bk = reinterpret_cast<uint4 *>(c.buf_k) + (size_t)j * kRing * kRowVec;
+      uint4 *bv = reinterpret_cast<uint4 *>(c.buf_v) + (size_t)j * kRing * kRowVec;
+      for (int e = lane; e < prm.n_new * kRowVec; e += 32) {
+        const int slot = (slot0 + e / kRowVec) & (kRing - 1);
+        bk[slot * kRowVec + e % kRowVec] = sk[e];
+        bv[slot * kRowVec + e % kRowVec] = sv[e];
+      }
+    }
+  }
 
   // sequences with n_q > fill see no token: zero outputs, lse = -inf, error
   for (int b = p; b < c.B; b += prm.P) {
@@ -678,7 +855,15 @@ __global__ void __launch_bounds__(NW * 32, 1) split_kernel(const Params prm) {
   lastseg.seek(x1 - 1, T, c.B);
   const int ord_first = first.ord, ord_last = lastseg.ord;
   // partial slot of warp ww for the piece of segment ordinal o
-  auto slot = [&](int o, int ww) { return prm.ws + ((size_t)(o + p) * NW + ww) * stride; };
+  auto slot = [&](int o, int ww) {
+    const size_t off = ((size_t)(o + p) * NW + ww) * stride;
+    // checked build: a partial out of the workspace is written to slot 0
+    return prm.ws + (chk(in_range(off, stride, prm.ws_floats), 7) ? off : 0);
+  };
+  // checked build: [q, q + n) inside the workspace (the merges' reads)
+  auto ws_ok = [&](const float *q, size_t n) {
+    return chk(in_range((size_t)(q - prm.ws), n, prm.ws_floats), 8);
+  };
   // A segment split across CTAs p_lo..p_hi is finished by whichever CTA
   // arrives last on its counter.  CTAs p_lo..p_hi-1 hold it as their last
   // piece and arrive with one merged CTA partial at the end.  CTA p_hi holds
@@ -721,7 +906,7 @@ __global__ void __launch_bounds__(NW * 32, 1) split_kernel(const Params prm) {
     for (int k = 0; k < S && k < n; ++k) {
       a.seek(x0 + k, T, c.B);
       if (lane == 0) issued[k] = k;
-      issue_unit<MODE, UB>(c, T, a, sbase + k * L::kStageBytes, full0 + 8 * k, lane);
+      issue_unit<MODE, UB>(prm, T, a, sbase + k * L::kStageBytes, full0 + 8 * k, lane);
     }
   }
 
@@ -765,7 +950,9 @@ __global__ void __launch_bounds__(NW * 32, 1) split_kernel(const Params prm) {
       cur_ord = cur.ord;
       const size_t bh = (size_t)cur.b * c.H + cur.h;
       const int qi = PK ? (r >> 1) : 8 * cg + r;  // the query row in B column r
-      load_q_pairs(prm.q + (bh * R + qi) * kD, qi < R, cq, qp0, qp1);
+      const bool q_ok =  // (rows qi >= R are not read)
+          qi >= R || chk(in_range((bh * R + qi) * kD, kD, (size_t)c.B * c.H * R * kD), 9);
+      load_q_pairs(prm.q + (q_ok ? (bh * R + qi) * kD : 0), qi < R, cq, qp0, qp1);
       sm.reset();
       fill = T.fill[cur.b];
       ng = T.ng[cur.b];
@@ -916,10 +1103,15 @@ __global__ void __launch_bounds__(NW * 32, 1) split_kernel(const Params prm) {
 #pragma unroll
         for (int qq = 0; qq < 2; ++qq) {
           const int moff = kOffMeta + 2 * (32 * (2 * hw + qq) + 4 * r);
+#if QS_CHECKED
+          const uint2 svw = lds64(st + moff + QS_META_V_SCALE * 256);
+          const uint2 zvw = lds64(st + moff + QS_META_V_ZERO * 256);
+#else
           const uint2 svw =
               *reinterpret_cast<const uint2 *>(smem + (st - sbase) + moff + QS_META_V_SCALE * 256);
           const uint2 zvw =
               *reinterpret_cast<const uint2 *>(smem + (st - sbase) + moff + QS_META_V_ZERO * 256);
+#endif
           const float2 sv01 = __half22float2(u32_as_h2(svw.x)), sv23 = __half22float2(u32_as_h2(svw.y));
           const float2 zv01 = __half22float2(u32_as_h2(zvw.x)), zv23 = __half22float2(u32_as_h2(zvw.y));
           const float svs[4] = {sv01.x, sv01.y, sv23.x, sv23.y};
@@ -1075,7 +1267,8 @@ __global__ void __launch_bounds__(NW * 32, 1) split_kernel(const Params prm) {
               const int mi = lane >> 3;
               const int tok = mr0 + 16 * tl + (lane & 7) + (mi >> 1) * 8;
               const int ch = 16 * md + (mi & 1) * 8;
-              const uint32_t addr = tok < rows ? vbase + tok * kTailRow + ch * 2 : zero_row;
+              uint32_t addr = tok < rows ? vbase + tok * kTailRow + ch * 2 : zero_row;
+              if (!chk(smem_in(addr, 16), 6)) addr = zero_row;
               uint32_t f0, f1, f2, f3;
               ldmatrix_x4_trans(addr, f0, f1, f2, f3);
               mma16816(d, f0, f1, f2, f3, bq0[tl], bq1[tl]);
@@ -1103,7 +1296,7 @@ __global__ void __launch_bounds__(NW * 32, 1) split_kernel(const Params prm) {
         fence_proxy_async_smem();
         if (lane == 0) issued[stage] = i + S;
         __syncwarp();
-        issue_unit<MODE, UB>(c, T, ahead, sbase + stage * L::kStageBytes, full0 + 8 * stage, lane);
+        issue_unit<MODE, UB>(prm, T, ahead, sbase + stage * L::kStageBytes, full0 + 8 * stage, lane);
       }
     }
   }
@@ -1153,6 +1346,7 @@ __global__ void __launch_bounds__(NW * 32, 1) split_kernel(const Params prm) {
   // shared.
   const bool aborted = s_abort != 0;
   float *last_part = reinterpret_cast<float *>(smem);  // NW partials, in stage memory (free now)
+  chk(smem_in(smem_addr(last_part), (uint32_t)(NW * stride * 4)), 11);
   if (s_abort != 2) {
     if (cur_ord == ord_last)
       write_partial(sm, Centre<MODE, UB>::kScale, last_part + w * stride, R, cg, lane, PK);
@@ -1166,6 +1360,8 @@ __global__ void __launch_bounds__(NW * 32, 1) split_kernel(const Params prm) {
     const int plo = cta_of(first.s0, U, prm.P);
     const MergeOut fo{true, prm.out + (size_t)seg * R * kD,
                       prm.lse ? prm.lse + (size_t)seg * R : nullptr, nullptr};
+    if (ws_ok(prm.ws + (size_t)(ord_first + plo) * NW * stride, (size_t)(p - plo) * NW * stride) &&
+        ws_ok(slot(ord_first, 0), (size_t)NW * stride) && chk(seg < (long long)c.B * c.H, 10))
     merge_rows(prm.ws + (size_t)(ord_first + plo) * NW * stride, 0, NW * stride, p - plo,
                slot(ord_first, 0), stride, ncg * stride, p - plo + NW / ncg, R, fo);
   }
@@ -1180,7 +1376,8 @@ __global__ void __launch_bounds__(NW * 32, 1) split_kernel(const Params prm) {
       const int plo = cta_of(S0, U, prm.P), phi = cta_of(E0 - 1, U, prm.P);
       const MergeOut mo{plo == phi, prm.out + (size_t)seg * R * kD,
                         prm.lse ? prm.lse + (size_t)seg * R : nullptr, slot(pc.ord, 0)};
-      if (!aborted)
+      if (!aborted && chk(seg < (long long)c.B * c.H, 10) &&
+          (pc.ord == ord_last || ws_ok(slot(pc.ord, 0), (size_t)NW * stride)))
         merge_rows(pc.ord == ord_last ? last_part : slot(pc.ord, 0), stride, ncg * stride,
                    NW / ncg, nullptr, 0, 0, NW / ncg, R, mo);
       if (plo != phi) {
@@ -1222,6 +1419,8 @@ __global__ void __launch_bounds__(NW * 32, 1) split_kernel(const Params prm) {
     const float *cta0 = prm.ws + ((size_t)(s_ord[a] + plo) * NW) * stride;
     const float *raw0 = prm.ws + ((size_t)(s_ord[a] + phi) * NW) * stride;
     const int nA = raw ? phi - plo : phi - plo + 1;
+    if (ws_ok(cta0, (size_t)nA * NW * stride) && (!raw || ws_ok(raw0, (size_t)NW * stride)) &&
+        chk(seg < (long long)c.B * c.H, 10))
     merge_rows(cta0, 0, NW * stride, nA, raw0, stride, ncg * stride,
                nA + (raw ? NW / ncg : 0), R, mo);
   }
@@ -1328,7 +1527,8 @@ namespace {
 // Validation, launch configuration and launch shared by the entry points.
 qs_status decode(const qs_cache *c, qs_mode mode, const uint16_t *q, int32_t n_q, int32_t group,
                  float softmax_scale, uint16_t *out, float *lse, void *workspace,
-                 size_t workspace_bytes, uint64_t wait_ns, int no_issue, qs_stream_t stream) {
+                 size_t workspace_bytes, uint64_t wait_ns, int no_issue, const uint16_t *k_new,
+                 const uint16_t *v_new, int32_t n_new, qs_stream_t stream) {
   qs_status s = check_cache(c);
   if (s != QS_OK) return s;
   if (!q || !out || n_q < 1 || n_q > kMaxQ || group < 1 || group * n_q > kMaxR) return QS_ERR_ARG;
@@ -1346,6 +1546,10 @@ qs_status decode(const qs_cache *c, qs_mode mode, const uint16_t *q, int32_t n_q
   prm.sl2 = softmax_scale * 1.4426950408889634f;
   prm.wait_ns = wait_ns;
   prm.no_issue = no_issue;
+  prm.k_new = k_new;
+  prm.v_new = v_new;
+  prm.n_new = n_new;
+  prm.ws_floats = workspace_bytes / sizeof(float);
   const bool packed = (mode == QS_DRAFT_UPPER4 && prm.R <= 4);
   if ((s = grid_size(mode, packed, c->upper_bits, prm.ncg, prm.P)) != QS_OK) return s;
   if (!workspace || !aligned16(workspace) ||
@@ -1365,7 +1569,18 @@ qs_status qs_attn_decode_gqa(const qs_cache *c, qs_mode mode, const uint16_t *q,
                              int32_t group, float softmax_scale, uint16_t *out, float *lse,
                              void *workspace, size_t workspace_bytes, qs_stream_t stream) {
   return decode(c, mode, q, n_q, group, softmax_scale, out, lse, workspace, workspace_bytes,
-                kWaitLimitNs, 0, stream);
+                kWaitLimitNs, 0, nullptr, nullptr, 0, stream);
+}
+
+qs_status qs_attn_decode_append(const qs_cache *c, qs_mode mode, const uint16_t *k_new,
+                                const uint16_t *v_new, int32_t n_new, const uint16_t *q,
+                                int32_t n_q, int32_t group, float softmax_scale, uint16_t *out,
+                                float *lse, void *workspace, size_t workspace_bytes,
+                                qs_stream_t stream) {
+  if (!k_new || !v_new || n_new < 1 || n_new > kRing) return QS_ERR_ARG;
+  if (!aligned16(k_new) || !aligned16(v_new)) return QS_ERR_ALIGN;
+  return decode(c, mode, q, n_q, group, softmax_scale, out, lse, workspace, workspace_bytes,
+                kWaitLimitNs, 0, k_new, v_new, n_new, stream);
 }
 
 qs_status qs_attn_decode(const qs_cache *c, qs_mode mode, const uint16_t *q, int32_t n_q,
@@ -1389,7 +1604,31 @@ qs_status qs_test_attn_decode_timeout(const qs_cache *c, qs_mode mode, const uin
                                       qs_stream_t stream) {
   if (wait_ns < 1000ull || wait_ns > 100000000ull) return QS_ERR_ARG;
   return decode(c, mode, q, n_q, group, softmax_scale, out, lse, workspace, workspace_bytes,
-                wait_ns, 1, stream);
+                wait_ns, 1, nullptr, nullptr, 0, stream);
 }
 
 }  // extern "C"
+
+#if QS_CHECKED
+extern "C" int qs_checked_failures_quantize(unsigned long long *out2, int reset);
+
+// Checked build only (-DQS_CHECKED=1): the number of failed bounds checks of
+// the attention and quantization kernels since the last reset, and the tag of
+// the first (1 shared-memory load, 2 copy destination, 3 group index, 4 buffer
+// row, 6 ldmatrix row, 7 partial slot, 8 merge source, 9 query row, 10 output
+// head, 11 tail partials, 20 flush group, 21 metadata position, 22 prefill
+// group rows, 23 prefill buffer rows).  reset != 0 zeroes the counts.
+// Returns 0, or 1 if a CUDA call failed.
+extern "C" int qs_checked_failures(unsigned long long *count, unsigned int *first_tag, int reset) {
+  unsigned long long a[2], q[2];
+  if (cudaMemcpyFromSymbol(a, g_check_fail, sizeof(a)) != cudaSuccess) return 1;
+  if (qs_checked_failures_quantize(q, reset)) return 1;
+  if (reset) {
+    const unsigned long long z[2] = {0, 0};
+    if (cudaMemcpyToSymbol(g_check_fail, z, sizeof(z)) != cudaSuccess) return 1;
+  }
+  *count = a[0] + q[0];
+  *first_tag = (unsigned int)(a[0] ? a[1] : q[1]);
+  return 0;
+}
+#endif

@@ -82,6 +82,37 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
+// ---- checked build (-DQS_CHECKED=1): the kernels check the bounds of their
+// shared-memory and global indexing on the device.  A failing access is
+// skipped (a load reads zero) and counted with a tag naming it, never
+// trapped; the checked library exports qs_checked_failures to read the
+// counts.  The ordinary build compiles every check away.
+#ifndef QS_CHECKED
+#define QS_CHECKED 0
+#endif
+#if QS_CHECKED
+static __device__ unsigned long long g_check_fail[2];  // count, first failing tag (per file)
+__device__ __forceinline__ bool chk(bool ok, uint32_t tag) {
+  if (!ok && atomicAdd(&g_check_fail[0], 1ull) == 0ull) g_check_fail[1] = tag;
+  return ok;
+}
+// [a, a + n) inside this CTA's dynamic shared memory (shared-window address)
+__device__ __forceinline__ bool smem_in(uint32_t a, uint32_t n) {
+  extern __shared__ __align__(128) uint8_t qs_dyn_smem[];
+  uint32_t dyn;
+  asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn));
+  const uint32_t lo = static_cast<uint32_t>(__cvta_generic_to_shared(qs_dyn_smem));
+  return a >= lo && a + n <= lo + dyn;
+}
+#else
+__device__ __forceinline__ constexpr bool chk(bool, uint32_t) { return true; }
+__device__ __forceinline__ constexpr bool smem_in(uint32_t, uint32_t) { return true; }
+#endif
+// [i, i + n) inside an array of len elements
+__device__ __forceinline__ bool in_range(size_t i, size_t n, size_t len) {
+  return i <= len && n <= len - i;
+}
+
 // Upper bound on any single pipeline wait; a healthy call takes well under a
 // millisecond, so running out means a broken pipeline: record and bail out.
 constexpr uint64_t kWaitLimitNs = 4000000000ull;

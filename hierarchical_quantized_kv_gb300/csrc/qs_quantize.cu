@@ -115,6 +115,9 @@ __device__ void quantize_part(FlushSmem<QW> &S, const __half *gk, const __half *
                               const qs_cache &c, size_t grp, int part, int tid) {
   constexpr int kQWarps = QW, kQThreads = 32 * QW;
   const int warp = tid >> 5, lane = tid & 31;
+  // checked build: a group index out of the arrays writes nothing (the same
+  // for every thread of the CTA)
+  if (!chk(in_range(grp, 1, (size_t)c.B * c.H * c.cap_groups), 20)) return;
   // 1. loads: the key column slice (64 B of each of 128 rows), 32 value rows
   for (int e = tid; e < kG * 4; e += kQThreads) {  // 4 x 16 B per key row
     const int t = e >> 2, q = e & 3;
@@ -228,7 +231,8 @@ __device__ void quantize_part(FlushSmem<QW> &S, const __half *gk, const __half *
   // 7. metadata: key scale / zero of the channel slice, value scale / zero of the quarter
   if (tid < kSlice) {
     uint16_t *m = c.meta + grp * 4 * 128;
-    const int kp = kmeta_pos(part * kSlice + tid), vp = vmeta_pos(part * kSlice + tid);
+    int kp = kmeta_pos(part * kSlice + tid), vp = vmeta_pos(part * kSlice + tid);
+    if (!chk(kp >= 0 && kp < 128 && vp >= 0 && vp < 128, 21)) kp = vp = 0;
     m[QS_META_K_SCALE * 128 + kp] = S.ks[tid];
     m[QS_META_K_ZERO * 128 + kp] = S.kz[tid];
     m[QS_META_V_SCALE * 128 + vp] = S.vs[tid];
@@ -238,8 +242,11 @@ __device__ void quantize_part(FlushSmem<QW> &S, const __half *gk, const __half *
 
 }  // namespace
 
+// n_next >= 0: flush the sequences whose buffer cannot take n_next more
+// tokens (qs_need_flush's rule; mask unused); else the masked ones (all
+// without a mask).
 __global__ void __launch_bounds__(32 * kFlushWarps)
-    flush_kernel(qs_cache c, const uint8_t *__restrict__ mask) {
+    flush_kernel(qs_cache c, const uint8_t *__restrict__ mask, int n_next) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   FlushSmem<kFlushWarps> &S = *reinterpret_cast<FlushSmem<kFlushWarps> *>(smem_raw);
   const int part = blockIdx.x, h = blockIdx.y, b = blockIdx.z, tid = threadIdx.x;
@@ -247,8 +254,8 @@ __global__ void __launch_bounds__(32 * kFlushWarps)
   pdl_wait();
   int32_t *st = c.state + (size_t)b * QS_STATE_WORDS;
   if (tid == 0) {
-    int act = mask ? (mask[b] != 0) : 1;
     const int fill = st[QS_ST_FILL], pending = st[QS_ST_PENDING], ng = st[QS_ST_N_GROUPS];
+    int act = n_next >= 0 ? (fill + n_next > kRing) : (mask ? (mask[b] != 0) : 1);
     const bool lead = (h == 0 && part == 0);
     if (act && fill - pending < kG) {
       if (lead) atomicOr(&st[QS_ST_ERR], QS_DEV_FLUSH_UNCOMMITTED);
@@ -323,7 +330,8 @@ __global__ void __launch_bounds__(32 * kPrefillWarps) prefill_kernel(qs_cache c,
   const uint16_t *kp = k + bh * T * kD, *vp = v + bh * T * kD;
   if (x < 4 * gmax) {
     const int g = x >> 2, part = x & 3;
-    if (g < ng)
+    // checked build: the group's prompt rows inside the prompt array
+    if (g < ng && chk(in_range(((size_t)g + 1) * kG, 0, (size_t)T), 22))
       quantize_part(S, reinterpret_cast<const __half *>(kp) + (size_t)g * kG * kD,
                     reinterpret_cast<const __half *>(vp) + (size_t)g * kG * kD, c,
                     bh * c.cap_groups + g, part, tid);
@@ -334,10 +342,11 @@ __global__ void __launch_bounds__(32 * kPrefillWarps) prefill_kernel(qs_cache c,
     const uint4 *vs = reinterpret_cast<const uint4 *>(vp + (size_t)ng * kG * kD);
     uint4 *kd = reinterpret_cast<uint4 *>(c.buf_k + bh * kRing * kD);
     uint4 *vd = reinterpret_cast<uint4 *>(c.buf_v + bh * kRing * kD);
-    for (int e = i0 * (kD / 8) + tid; e < i1 * (kD / 8); e += 32 * kPrefillWarps) {
-      kd[e] = ks[e];
-      vd[e] = vs[e];
-    }
+    if (chk(i1 <= kRing && (size_t)ng * kG + i1 <= (size_t)T, 23))
+      for (int e = i0 * (kD / 8) + tid; e < i1 * (kD / 8); e += 32 * kPrefillWarps) {
+        kd[e] = ks[e];
+        vd[e] = vs[e];
+      }
   }
   __syncthreads();
   if (tid == 0) {
@@ -394,5 +403,27 @@ extern "C" qs_status qs_quantize_flush(const qs_cache *c, const uint8_t *d_mask,
   const int smem = (int)sizeof(FlushSmem<kFlushWarps>);
   if ((s = set_smem_once((const void *)flush_kernel, smem, &g_flush_ready)) != QS_OK) return s;
   return launch_pdl(flush_kernel, dim3(kParts, c->H, c->B), dim3(32 * kFlushWarps), smem,
-                    (cudaStream_t)stream, *c, d_mask);
+                    (cudaStream_t)stream, *c, d_mask, -1);
 }
+
+extern "C" qs_status qs_quantize_flush_due(const qs_cache *c, int32_t n_next, qs_stream_t stream) {
+  qs_status s = check_cache(c);
+  if (s != QS_OK) return s;
+  if (n_next < 0 || n_next > kRing) return QS_ERR_ARG;
+  const int smem = (int)sizeof(FlushSmem<kFlushWarps>);
+  if ((s = set_smem_once((const void *)flush_kernel, smem, &g_flush_ready)) != QS_OK) return s;
+  return launch_pdl(flush_kernel, dim3(kParts, c->H, c->B), dim3(32 * kFlushWarps), smem,
+                    (cudaStream_t)stream, *c, static_cast<const uint8_t *>(nullptr), (int)n_next);
+}
+
+#if QS_CHECKED
+// Checked build only: this file's failure count and first failing tag.
+extern "C" int qs_checked_failures_quantize(unsigned long long *out2, int reset) {
+  if (cudaMemcpyFromSymbol(out2, g_check_fail, sizeof(g_check_fail)) != cudaSuccess) return 1;
+  if (reset) {
+    const unsigned long long z[2] = {0, 0};
+    if (cudaMemcpyToSymbol(g_check_fail, z, sizeof(z)) != cudaSuccess) return 1;
+  }
+  return 0;
+}
+#endif

@@ -56,6 +56,7 @@ _SIGS = {
     "qs_buffer_rollback": [ctypes.POINTER(QsCacheStruct), _P, _P],
     "qs_need_flush": [ctypes.POINTER(QsCacheStruct), _I32, _P, _P],
     "qs_quantize_flush": [ctypes.POINTER(QsCacheStruct), _P, _P],
+    "qs_quantize_flush_due": [ctypes.POINTER(QsCacheStruct), _I32, _P],
     "qs_attn_workspace_size": [ctypes.POINTER(QsCacheStruct), _I32, ctypes.POINTER(ctypes.c_size_t)],
     "qs_attn_decode": [ctypes.POINTER(QsCacheStruct), ctypes.c_int, _P, _I32, ctypes.c_float, _P,
                        _P, _P, ctypes.c_size_t, _P],
@@ -68,6 +69,8 @@ _SIGS = {
     "qs_spec_accept": [_P, _P, _P, _P, _P, _I32, _I32, _I32, _P, _P, _P, _P],
     "qs_attn_decode_static_ws": [ctypes.POINTER(QsCacheStruct), ctypes.c_int, _P, _I32,
                                  ctypes.c_float, _P, _P, _P],
+    "qs_attn_decode_append": [ctypes.POINTER(QsCacheStruct), ctypes.c_int, _P, _P, _I32, _P, _I32,
+                              _I32, ctypes.c_float, _P, _P, _P, ctypes.c_size_t, _P],
 }
 
 
@@ -182,6 +185,12 @@ def qs_quantize_flush(cache, mask=None, stream=None):
     _check("qs_quantize_flush", lib().qs_quantize_flush(cache._ref, _ptr(mask), _stream(stream)))
 
 
+def qs_quantize_flush_due(cache, n_next, stream=None):
+    """Flush every sequence whose buffer cannot take n_next more tokens."""
+    _check("qs_quantize_flush_due", lib().qs_quantize_flush_due(cache._ref, int(n_next),
+                                                                _stream(stream)))
+
+
 def qs_prefill(cache, k, v, lens, stream=None):
     """k, v: fp16 [B, H, T, D] contiguous device tensors; lens: int32 [B]
     device tensor of prompt lengths."""
@@ -246,6 +255,18 @@ def qs_attn_decode_static_ws(cache, mode, q, softmax_scale, out, lse=None, strea
     if status != QS_ERR_TOO_LARGE:
         _check("qs_attn_decode_static_ws", status)
     return status
+
+
+def qs_attn_decode_append(cache, mode, k_new, v_new, q, softmax_scale, out, lse=None,
+                          workspace=None, group=1, stream=None):
+    """qs_buffer_append(k_new, v_new) then qs_attn_decode(_gqa), one launch.
+    k_new, v_new: fp16 [B, H, n_new, D]; q, out: fp16 [B, H*group, n_q, D]."""
+    assert k_new.is_contiguous() and v_new.is_contiguous() and k_new.shape == v_new.shape
+    n_q = q.shape[2]
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("qs_attn_decode_append", lib().qs_attn_decode_append(
+        cache._ref, int(mode), _ptr(k_new), _ptr(v_new), k_new.shape[2], _ptr(q), n_q, int(group),
+        float(softmax_scale), _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes, _stream(stream)))
 
 
 def qs_get_errors(cache, stream=None):

@@ -213,6 +213,14 @@ qs_status qs_need_flush(const qs_cache *c, int32_t n_next, uint8_t *d_mask, qs_s
  * Appendix D; "QuantSpec Guide", "Periodic Group Quantization". */
 qs_status qs_quantize_flush(const qs_cache *c, const uint8_t *d_mask, qs_stream_t stream);
 
+/* qs_need_flush(n_next) followed by qs_quantize_flush with that mask, in one
+ * launch and without the mask array: every sequence whose buffer cannot take
+ * n_next more tokens (fill + n_next > 2G) quantizes its oldest half, with the
+ * same preconditions, results and error bits as qs_quantize_flush.  Host
+ * errors: QS_ERR_ARG (n_next outside 0..2G).  Source: as qs_need_flush and
+ * qs_quantize_flush. */
+qs_status qs_quantize_flush_due(const qs_cache *c, int32_t n_next, qs_stream_t stream);
+
 /* Bulk prefill: fill empty caches from a prompt in one call.  k, v: fp16
  * [B][H][T][D] device arrays (token t of head h of sequence b at
  * [b][h][t]); d_len: int32 [B] device array, the prompt length of each
@@ -310,6 +318,28 @@ qs_status qs_attn_workspace_size_gqa(const qs_cache *c, int32_t n_q, int32_t gro
 qs_status qs_attn_decode_gqa(const qs_cache *c, qs_mode mode, const uint16_t *q, int32_t n_q,
                              int32_t group, float softmax_scale, uint16_t *out, float *lse,
                              void *workspace, size_t workspace_bytes, qs_stream_t stream);
+
+/* qs_buffer_append followed by qs_attn_decode_gqa, in one launch: n_new
+ * tokens k_new, v_new (fp16 [B][H][n_new][D] device arrays, 16-byte aligned,
+ * 1 <= n_new <= 2G; H counts KV heads) enter each sequence's buffer as pending
+ * tokens, then the queries attend over the buffer including them -- the
+ * speculative round's "append a draft token, then draft" and "append the
+ * gamma + 1 target tokens, then verify" without a launch in between.  The
+ * results, the buffer, the counters and the error words equal those of the
+ * two separate calls: a sequence whose buffer cannot take the tokens gets
+ * QS_DEV_OVERFLOW and attends over its buffer as it was.  The attention reads
+ * the new rows from k_new / v_new while the same launch writes them into the
+ * ring, so k_new and v_new must stay unchanged until the call completes.
+ * Arguments, workspace and errors otherwise as qs_attn_decode_gqa (group = 1
+ * is qs_attn_decode), plus QS_ERR_ARG for null k_new / v_new or n_new outside
+ * 1..2G.  Sources: Pith review page, "What carries the argument" (new tokens
+ * enter the double full-precision buffer; both passes attend over it);
+ * "QuantSpec Guide", "The Self-Speculative Verification Loop". */
+qs_status qs_attn_decode_append(const qs_cache *c, qs_mode mode, const uint16_t *k_new,
+                                const uint16_t *v_new, int32_t n_new, const uint16_t *q,
+                                int32_t n_q, int32_t group, float softmax_scale, uint16_t *out,
+                                float *lse, void *workspace, size_t workspace_bytes,
+                                qs_stream_t stream);
 
 /* Size of the fixed scratch array behind qs_attn_decode_static_ws. */
 #define QS_STATIC_WS_BYTES (8u << 20)
