@@ -465,12 +465,16 @@ __device__ __forceinline__ void issue_unit(const Params &prm, const Tables &T, c
   }
 }
 
+// Each merge splits a row's partials over up to QS_MERGE_KS adjacent lanes
+// (1: one lane per row and four channels).  Measured on the 32k step: 8
+// against 1, 215.0 against 215.9 us per step, isolated draft 45.7 against 47.5.
+#ifndef QS_MERGE_KS
+#define QS_MERGE_KS 8
+#endif
+
 // Device-scope fence between a CTA's partials and its arrival on a segment
 // counter (release), and between the arrival that completes a segment and
 // the reads of the other CTAs' partials (acquire).
-#ifndef QS_MERGE_KS
-#define QS_MERGE_KS 1  // > 1: merges split each row's partials over up to this many lanes
-#endif
 #ifndef QS_FENCE_AR
 #define QS_FENCE_AR 0
 #endif
@@ -519,18 +523,20 @@ __device__ __forceinline__ float4 ld_part4(const float *p) {
   return v;
 }
 
-// Row-parallel: row j of the R rows is merged by one warp, whose lanes hold
-// four channels each; with more rows than warps a warp takes rows
-// blockDim / 32 apart.  Each lane loads a batch of partials (m, l and its four
-// channels of O) at once, all in flight before the first is used, and folds
-// them into a running (M, L, O) with one rescale per batch: no shared-memory
-// scratch and no barrier, so warps without a row return at once.  Row j's
+// Row-parallel merge of ns partials.  An item is (row j, four channels): with
+// QS_MERGE_KS > 1 and few rows, the partials of an item are split over ks
+// adjacent lanes (as many as the CTA's threads allow, at most QS_MERGE_KS),
+// which combine their (M, L, O) by shuffles at the end; with QS_MERGE_KS = 1
+// one warp takes a row, its lanes four channels each.  Each lane loads a
+// batch of partials (m, l and its four channels of O) at once, all in flight
+// before the first is used, and folds them into a running (M, L, O) with one
+// rescale per batch: no shared-memory scratch and no barrier.  Row j's
 // partials start at srcA + (j / 8) * cgA (and srcB + (j / 8) * cgB): warp
-// partials hold only the rows of their warp's column group.  dst may be
-// partial 0 of the sources: each lane writes only what it read, after the
-// warp's reads.  Not inlined: it runs once or twice per launch, at the end,
-// where every instruction is fetched cold, so one small shared copy matters
-// more than the call.
+// partials hold only the rows of their warp's column group.  dst never
+// overlaps the sources (a CTA partial is made only of a range's last piece,
+// whose warp partials are in shared memory).  Not inlined: it runs once or
+// twice per launch, at the end, where every instruction is fetched cold, so
+// one small shared copy matters more than the call.
 #if QS_MERGE_KS > 1
 __device__ __noinline__ void merge_rows(const float *srcA, int cgA, int kstrideA, int nA,
                                         const float *srcB, int cgB, int kstrideB, int ns, int R,
@@ -894,7 +900,8 @@ __global__ void __launch_bounds__(NW * 32, 1) split_kernel(const Params prm) {
   };
 
   // the warps reach the range's last segment mid-range: start its queries
-  // towards L1 now (two 128-byte lines per row)
+  // towards L1 now (two 128-byte lines per row; a copy in shared memory was
+  // measured no faster)
   if (ord_last != ord_first && threadIdx.x < 2 * R) {
     const size_t bh = (size_t)lastseg.b * c.H + lastseg.h;
     prefetch_l1(prm.q + (bh * R) * kD + threadIdx.x * 64);
