@@ -54,7 +54,11 @@ constexpr int kWarps = 2 * kPairs;
 // five-query tile does not spill (32k: 63 against 71 µs per call; 128k:
 // 175 against 192).  Three column groups keep twelve warps (four per group).
 constexpr int kVerifyWarps = 8;
-constexpr int kTailRow = 272;  // padded fp16 row stride (bytes) of buffer tiles
+// fp16 row stride (bytes) of a buffer tile in shared memory.  Rows padded
+// by 16 bytes are read without bank conflicts but take one copy per row;
+// unpadded rows arrive in one copy per plane.
+template <bool PAD>
+constexpr int tail_row() { return PAD ? 272 : 256; }
 constexpr int kOffKU = 0, kOffVU = 8192, kOffMeta = 16384, kOffKL = 17408, kOffVL = 25600;
 
 template <int MODE>
@@ -76,7 +80,7 @@ constexpr int align16(int x) { return (x + 15) & ~15; }
 
 template <int MODE>
 struct Layout {
-  static constexpr int kTailBytes = Cfg<MODE>::kTailTok * kTailRow * 2;
+  static constexpr int kTailBytes = Cfg<MODE>::kTailTok * tail_row<true>() * 2;
   static constexpr int kStageBytes =
       Cfg<MODE>::kGroupBytes > kTailBytes ? Cfg<MODE>::kGroupBytes : kTailBytes;
   static constexpr int kBarOff = Cfg<MODE>::kStages * kStageBytes;               // full barriers
@@ -408,12 +412,13 @@ __device__ __forceinline__ uint8_t *prm_smem_base() {
 // With a fused append, buffer rows at or past the old fill come straight
 // from the appended tokens (the ring gets them in the same launch, not read
 // back here).
-template <int MODE, int UB>
+template <int MODE, int UB, bool PAD>
 __device__ __forceinline__ void issue_unit(const Params &prm, const Tables &T, const Seg &cu,
                                            uint32_t dst, uint32_t bar, int lane) {
   const qs_cache &c = prm.c;
   using C = Cfg<MODE>;
   constexpr int TT = C::kTailTok;
+  static_assert(kG % TT == 0 && kRing % TT == 0, "a buffer chunk must not straddle the ring end");
   const size_t bh = (size_t)cu.b * c.H + cu.h;
   const int ng = T.ng[cu.b];
   if (cu.u < ng) {
@@ -435,31 +440,48 @@ __device__ __forceinline__ void issue_unit(const Params &prm, const Tables &T, c
       }
     }
   } else {
+    // A buffer chunk: rows fp16 rows of K, then of V.  The rows before the
+    // old fill are consecutive ring slots (a chunk starts at a multiple of
+    // its size from the half base, so it wraps to the ring's start whole or
+    // not at all); rows from the appended tokens follow.
+    constexpr int kRow = tail_row<PAD>();
     const int i0 = (cu.u - ng) * TT;
     const int rows = min(TT, T.fill[cu.b] - i0);
-    if (lane == 0) mbar_arrive_expect_tx(bar, rows * 2 * kD * 2);
-    __syncwarp();
-    const int slot0 = T.hb[cu.b] * kG + i0;  // chunks never straddle the ring end
     const int fold = T.fold[cu.b];
-    for (int rr = lane; rr < 2 * rows; rr += 32) {
-      const bool isv = rr >= rows;
-      const int row = isv ? rr - rows : rr;
+    const int slot0 = (T.hb[cu.b] * kG + i0) & (kRing - 1);
+    // unpadded: one bulk copy each for the K and V ring rows (the copy
+    // engine spends about as long on a 256-byte copy as on an 8 KB one);
+    // padded: one copy per row
+    const int n_bulk = PAD ? 0 : max(0, min(rows, fold - i0));
+    if (lane == 0) {
+      mbar_arrive_expect_tx(bar, rows * 2 * kD * 2);
+      if (n_bulk > 0) {
+        size_t r0 = bh * kRing + slot0;
+        // checked build: rows out of the ring read row 0 instead
+        if (!chk(in_range(r0, n_bulk, (size_t)c.B * c.H * kRing), 4)) r0 = 0;
+        uint32_t dk = dst, dv = dst + TT * kRow;
+        if (!chk(smem_in(dv, n_bulk * kRow), 2)) dk = dv = smem_addr(prm_smem_base());
+        bulk_g2s(dk, c.buf_k + r0 * kD, n_bulk * kRow, bar);
+        bulk_g2s(dv, c.buf_v + r0 * kD, n_bulk * kRow, bar);
+      }
+    }
+    __syncwarp();
+    const int n_rest = rows - n_bulk;
+    for (int rr = lane; rr < 2 * n_rest; rr += 32) {
+      const bool isv = rr >= n_rest;
+      const int row = n_bulk + (isv ? rr - n_rest : rr);
       const uint16_t *src;
       if (i0 + row < fold) {
-        const int slot = (slot0 + row) & (kRing - 1);
-        src = (isv ? c.buf_v : c.buf_k) + (bh * kRing + slot) * kD;
+        size_t ri = bh * kRing + slot0 + row;
+        if (!chk(in_range(ri, 1, (size_t)c.B * c.H * kRing), 4)) ri = 0;
+        src = (isv ? c.buf_v : c.buf_k) + ri * kD;
       } else {
-        src = (isv ? prm.v_new : prm.k_new) + (bh * prm.n_new + (i0 + row - fold)) * kD;
+        size_t rn = bh * prm.n_new + (i0 + row - fold);
+        if (!chk(in_range(rn, 1, (size_t)c.B * c.H * prm.n_new), 4)) rn = 0;
+        src = (isv ? prm.v_new : prm.k_new) + rn * kD;
       }
-      uint32_t d = dst + (isv ? TT * kTailRow : 0) + row * kTailRow;
+      uint32_t d = dst + (isv ? TT * kRow : 0) + row * kRow;
       if (!chk(smem_in(d, kD * 2), 2)) d = smem_addr(prm_smem_base());
-      if (QS_CHECKED) {
-        const size_t ring_rows = (size_t)c.B * c.H * kRing, new_rows = (size_t)c.B * c.H * prm.n_new;
-        const bool ok = i0 + row < fold
-                            ? in_range((size_t)(src - (isv ? c.buf_v : c.buf_k)) / kD, 1, ring_rows)
-                            : in_range((size_t)(src - (isv ? prm.v_new : prm.k_new)) / kD, 1, new_rows);
-        if (!chk(ok, 4)) src = isv ? c.buf_v : c.buf_k;
-      }
       bulk_g2s(d, src, kD * 2, bar);
     }
   }
@@ -768,6 +790,10 @@ __global__ void __launch_bounds__(NW * 32, 1) split_kernel(const Params prm) {
   using L = Layout<MODE>;
   constexpr int TT = C::kTailTok, S = C::kStages;
   constexpr int kTailTiles = TT / 32;  // 16-token tiles of a buffer chunk per warp
+  // buffer tiles padded where several column groups read each tile (the
+  // 12-warp multi-row variants); unpadded, one copy per plane, elsewhere
+  constexpr bool kPadTail = !PK && NW == 12;
+  constexpr int kRow = tail_row<kPadTail>();
   extern __shared__ __align__(128) uint8_t smem[];
   const qs_cache &c = prm.c;
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -913,7 +939,7 @@ __global__ void __launch_bounds__(NW * 32, 1) split_kernel(const Params prm) {
     for (int k = 0; k < S && k < n; ++k) {
       a.seek(x0 + k, T, c.B);
       if (lane == 0) issued[k] = k;
-      issue_unit<MODE, UB>(prm, T, a, sbase + k * L::kStageBytes, full0 + 8 * k, lane);
+      issue_unit<MODE, UB, kPadTail>(prm, T, a, sbase + k * L::kStageBytes, full0 + 8 * k, lane);
     }
   }
 
@@ -1230,8 +1256,8 @@ __global__ void __launch_bounds__(NW * 32, 1) split_kernel(const Params prm) {
 #pragma unroll
             for (int i4 = 0; i4 < 4; ++i4) {
               const int ra = mr + r, rb = mr + r + 8;
-              const uint4 x = ra < rows ? lds128(st + ra * kTailRow + 64 * cq + 16 * i4) : make_uint4(0, 0, 0, 0);
-              const uint4 y = rb < rows ? lds128(st + rb * kTailRow + 64 * cq + 16 * i4) : make_uint4(0, 0, 0, 0);
+              const uint4 x = ra < rows ? lds128(st + ra * kRow + 64 * cq + 16 * i4) : make_uint4(0, 0, 0, 0);
+              const uint4 y = rb < rows ? lds128(st + rb * kRow + 64 * cq + 16 * i4) : make_uint4(0, 0, 0, 0);
               w0[4 * i4] = x.x; w0[4 * i4 + 1] = x.y; w0[4 * i4 + 2] = x.z; w0[4 * i4 + 3] = x.w;
               w1[4 * i4] = y.x; w1[4 * i4 + 1] = y.y; w1[4 * i4 + 2] = y.z; w1[4 * i4 + 3] = y.w;
             }
@@ -1265,7 +1291,7 @@ __global__ void __launch_bounds__(NW * 32, 1) split_kernel(const Params prm) {
             bq0[tl] = movmatrix_trans(pack_half2(pv[0], pv[1]));
             bq1[tl] = movmatrix_trans(pack_half2(pv[2], pv[3]));
           }
-          const uint32_t vbase = st + TT * kTailRow;
+          const uint32_t vbase = st + TT * kRow;
 #pragma unroll
           for (int md = 0; md < 8; ++md) {
             float d[4] = {0.f, 0.f, 0.f, 0.f};
@@ -1274,7 +1300,7 @@ __global__ void __launch_bounds__(NW * 32, 1) split_kernel(const Params prm) {
               const int mi = lane >> 3;
               const int tok = mr0 + 16 * tl + (lane & 7) + (mi >> 1) * 8;
               const int ch = 16 * md + (mi & 1) * 8;
-              uint32_t addr = tok < rows ? vbase + tok * kTailRow + ch * 2 : zero_row;
+              uint32_t addr = tok < rows ? vbase + tok * kRow + ch * 2 : zero_row;
               if (!chk(smem_in(addr, 16), 6)) addr = zero_row;
               uint32_t f0, f1, f2, f3;
               ldmatrix_x4_trans(addr, f0, f1, f2, f3);
@@ -1303,7 +1329,7 @@ __global__ void __launch_bounds__(NW * 32, 1) split_kernel(const Params prm) {
         fence_proxy_async_smem();
         if (lane == 0) issued[stage] = i + S;
         __syncwarp();
-        issue_unit<MODE, UB>(prm, T, ahead, sbase + stage * L::kStageBytes, full0 + 8 * stage, lane);
+        issue_unit<MODE, UB, kPadTail>(prm, T, ahead, sbase + stage * L::kStageBytes, full0 + 8 * stage, lane);
       }
     }
   }
