@@ -87,7 +87,8 @@ struct Layout {
   static constexpr int kCntOff = align16(kBarOff + 8 * Cfg<MODE>::kStages);      // release counters
   static constexpr int kIssOff = align16(kCntOff + 4 * Cfg<MODE>::kStages);      // unit per stage
   static constexpr int kZeroOff = align16(kIssOff + 4 * Cfg<MODE>::kStages);     // zero row (ldmatrix)
-  static constexpr int kTabOff = kZeroOff + 32;
+  static constexpr int kMrgOff = kZeroOff + 32;  // barrier of the finishing merge's copies
+  static constexpr int kTabOff = kMrgOff + 16;
   // per-sequence tables: n_groups, fill, half_base, segment length, base
   // unit, first segment ordinal, fill before a fused append
   static constexpr int kSmemBytes = kTabOff + 7 * kMaxB * 4;
@@ -512,6 +513,12 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Global memory written through ordinary stores (and acquired) is read next
+// by bulk copies.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // ------------------------------------------------------- log-sum-exp merge
 // Merge of ns partials of one (sequence, head): partial k < nA starts at
 // srcA + k * kstrideA floats, partial k >= nA at srcB + (k - nA) * kstrideB.
@@ -559,16 +566,32 @@ __device__ __forceinline__ float4 ld_part4(const float *p) {
 // whose warp partials are in shared memory).  Not inlined: it runs once or
 // twice per launch, at the end, where every instruction is fetched cold, so
 // one small shared copy matters more than the call.
+// Partials per batch of one lane's loads, and the lanes ks that share an
+// item (row j, four channels) of R * 32 items: as many as the CTA's threads
+// allow, at most QS_MERGE_KS.
+constexpr int kMergeBatch = QS_MERGE_KS > 1 ? 4 : 8;
+__device__ __forceinline__ int merge_split(int R) {
+  int ks = 1;
+  while (ks < QS_MERGE_KS && R * 32 * ks * 2 <= (int)blockDim.x) ks *= 2;
+  return ks;
+}
+// Dependent rounds of loads a merge of ns partials takes: passes over the
+// items times batches per lane.
+__device__ __forceinline__ int merge_rounds(int R, int ns) {
+  const int ks = merge_split(R);
+  return (R * 32 * ks + (int)blockDim.x - 1) / (int)blockDim.x *
+         ((ns + ks * kMergeBatch - 1) / (ks * kMergeBatch));
+}
+
 #if QS_MERGE_KS > 1
 __device__ __noinline__ void merge_rows(const float *srcA, int cgA, int kstrideA, int nA,
                                         const float *srcB, int cgB, int kstrideB, int ns, int R,
                                         const MergeOut &mo) {
   // items (row j, four channels c4), the partials of an item split over ks
   // adjacent lanes that combine by shuffles at the end
-  constexpr int kBatch = 4;
+  constexpr int kBatch = kMergeBatch;
   const int items = R * 32;
-  int ks = 1;
-  while (ks < QS_MERGE_KS && items * ks * 2 <= (int)blockDim.x) ks *= 2;
+  const int ks = merge_split(R);
   const int mo_off = R * kD;
 #pragma unroll 1
   for (int base = 0; base < items * ks; base += blockDim.x) {
@@ -657,7 +680,7 @@ __device__ __noinline__ void merge_rows(const float *srcA, int cgA, int kstrideA
 __device__ __noinline__ void merge_rows(const float *srcA, int cgA, int kstrideA, int nA,
                                         const float *srcB, int cgB, int kstrideB, int ns, int R,
                                         const MergeOut &mo) {
-  constexpr int kBatch = 8;
+  constexpr int kBatch = kMergeBatch;
   const int lane = threadIdx.x & 31;
   const int mo_off = R * kD;
 #pragma unroll 1
@@ -801,6 +824,7 @@ __global__ void __launch_bounds__(NW * 32, 1) split_kernel(const Params prm) {
   const int r = lane >> 2, cq = lane & 3;
   const uint32_t sbase = smem_addr(smem);
   const uint32_t full0 = sbase + L::kBarOff, zero_row = sbase + L::kZeroOff;
+  const uint32_t mrg_bar = sbase + L::kMrgOff;
   int *cnt = reinterpret_cast<int *>(smem + L::kCntOff);            // releases per stage
   volatile int *issued = reinterpret_cast<int *>(smem + L::kIssOff);  // unit copied into a stage
   Tables T = tables_at(smem, L::kTabOff);
@@ -814,6 +838,7 @@ __global__ void __launch_bounds__(NW * 32, 1) split_kernel(const Params prm) {
       cnt[s] = 0;
       issued[s] = -1;
     }
+    if (MODE == QS_VERIFY_INT8) mbar_init(mrg_bar, 1);
     fence_mbar_init();
     s_next[0] = s_next[1] = s_next[2] = 0;
     s_abort = 0;
@@ -1437,6 +1462,7 @@ __global__ void __launch_bounds__(NW * 32, 1) split_kernel(const Params prm) {
     s_last[threadIdx.x] = last;
   }
   __syncthreads();
+  int n_mrg = 0;  // phases of the merge barrier used
   for (int a = 0; a < n_arr; ++a) {
     if (!s_last[a] || aborted) continue;
     const long long seg = s_seg[a];
@@ -1452,10 +1478,41 @@ __global__ void __launch_bounds__(NW * 32, 1) split_kernel(const Params prm) {
     const float *cta0 = prm.ws + ((size_t)(s_ord[a] + plo) * NW) * stride;
     const float *raw0 = prm.ws + ((size_t)(s_ord[a] + phi) * NW) * stride;
     const int nA = raw ? phi - plo : phi - plo + 1;
-    if (ws_ok(cta0, (size_t)nA * NW * stride) && (!raw || ws_ok(raw0, (size_t)NW * stride)) &&
-        chk(seg < (long long)c.B * c.H, 10))
-    merge_rows(cta0, 0, NW * stride, nA, raw0, stride, ncg * stride,
-               nA + (raw ? NW / ncg : 0), R, mo);
+    if (!(ws_ok(cta0, (size_t)nA * NW * stride) && (!raw || ws_ok(raw0, (size_t)NW * stride)) &&
+          chk(seg < (long long)c.B * c.H, 10)))
+      continue;
+    // Verify: where a merge straight from L2 would wait on six or more round
+    // trips (many rows and partials per lane), the segment's partials are
+    // first gathered into the stage memory (free now) by one bulk copy each.
+    // Measured: the 20-row grouped-query verify (ten rounds) 58.6 -> 56.4 us;
+    // the 5-row verify's four rounds gained nothing.  The drafts' merges
+    // take one to three rounds; compiled into them (even when not taken) the
+    // gathering cost 1-1.5 us per draft call.
+    const float *srcA = cta0, *srcB = raw0;
+    int kA = NW * stride;
+    const int ns = nA + (raw ? NW / ncg : 0);
+    const uint32_t n_st = (uint32_t)(nA + (raw ? NW : 0)) * stride * 4;
+    if (MODE == QS_VERIFY_INT8 && merge_rounds(R, ns) >= 6 && n_st <= (uint32_t)L::kBarOff) {
+      __syncthreads();  // the previous merge's reads of the stage memory are done
+      if (threadIdx.x == 0) {
+        fence_proxy_async_global();
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(mrg_bar, n_st);
+        for (int k = 0; k < nA; ++k)
+          bulk_g2s(sbase + k * stride * 4, cta0 + (size_t)k * NW * stride, stride * 4, mrg_bar);
+        if (raw) bulk_g2s(sbase + nA * stride * 4, raw0, NW * stride * 4, mrg_bar);
+      }
+      const bool ok = __syncthreads_and(mbar_wait(mrg_bar, (uint32_t)(n_mrg & 1), prm.wait_ns));
+      ++n_mrg;
+      if (!ok) {
+        if (threadIdx.x == 0) atomicOr(&c.state[(size_t)b * QS_STATE_WORDS + QS_ST_ERR], QS_DEV_TIMEOUT);
+        continue;
+      }
+      srcA = reinterpret_cast<const float *>(smem);
+      srcB = srcA + (size_t)nA * stride;
+      kA = stride;
+    }
+    merge_rows(srcA, 0, kA, nA, srcB, stride, ncg * stride, ns, R, mo);
   }
 }
 
