@@ -430,22 +430,25 @@ class Round:
         self.launches_per_step = (1 if fused else 2) + GAMMA * (1 if fused else 2) + 1 + \
             (1 if fused else 2) + 1
 
-    def step(self, s, host=None, ev=None, external=False, extra=None):
+    def step(self, s, host=None, ev=None, external=False, extra=None, seq=False):
         """One speculative round.  ev: a list that receives (kind, start, end)
         CUDA events recorded around each attention call (as graph nodes when
-        the step is captured with external=True).  extra = "draft" or
-        "verify": one more such attention call (without an append) right
-        after each of that kind, for the marginal in-step time."""
+        the step is captured with external=True); with seq=True one pair of
+        events around the run of gamma draft calls instead (kind
+        "draft_seq": consecutive launches keep their overlap).  extra =
+        "draft" or "verify": one more such attention call (without an append)
+        right after each of that kind, for the marginal in-step time."""
         qs, c = self.qs, self.cache
         torch = self.torch
         if ev is not None:
             ev.clear()
 
+        mk = (lambda: torch.cuda.Event(enable_timing=True, external=True)) if external else \
+            (lambda: torch.cuda.Event(enable_timing=True))
+
         def timed(kind, fn):
-            if ev is None:
+            if ev is None or (seq and kind == "draft"):
                 return fn()
-            mk = (lambda: torch.cuda.Event(enable_timing=True, external=True)) if external else \
-                (lambda: torch.cuda.Event(enable_timing=True))
             e0, e1 = mk(), mk()
             e0.record()
             fn()
@@ -459,6 +462,9 @@ class Round:
         else:
             qs.qs_need_flush(c, GAMMA + 1, self.mask)
             qs.qs_quantize_flush(c, self.mask)
+        if ev is not None and seq:
+            s0, s1 = mk(), mk()
+            s0.record()
         for i in range(GAMMA):
             if self.fused:  # append the draft token and attend in one launch
                 timed("draft", lambda i=i: qs.qs_attn_decode_append(
@@ -471,6 +477,9 @@ class Round:
                 qs.qs_buffer_append(c, self.kd[i], self.vd[i])
                 timed("draft", lambda i=i: qs.qs_attn_decode(c, qs.QS_DRAFT_UPPER4, self.qd[i],
                                                              self.scale, self.od[i], None, self.ws))
+        if ev is not None and seq:
+            s1.record()
+            ev.append(("draft_seq", s0, s1))
         qs.qs_buffer_rollback(c, self.drop_draft)
         if self.fused:
             timed("verify", lambda: qs.qs_attn_decode_append(
@@ -560,37 +569,49 @@ def external_events_supported(torch):
 
 
 def in_step_launch_times(torch, r, n_rep):
-    """Device time of each attention call inside the step: the steps are
-    captured with CUDA events as graph nodes around each attention call and
-    replayed n_rep times (eager steps with events where torch cannot record
-    events into a graph).  Returns ({kind: [us, ...]}, how)."""
-    launch = {"draft": [], "verify": []}
+    """Device time of the attention calls inside the step: the steps are
+    captured with CUDA events as graph nodes and replayed n_rep times (eager
+    steps with events where torch cannot record events into a graph).
+    "draft" and "verify": events around each call.  An event node between
+    two launches ends the overlap of the later launch's start with the
+    earlier one's end (programmatic dependent launch), so each such figure
+    carries a launch latency the timed step does not.  "draft_seq": events
+    around the step's run of gamma consecutive draft calls, divided by gamma
+    (the launches inside the run keep their overlap, as in the timed step).
+    Returns ({kind: [us, ...]}, how)."""
+    launch = {"draft": [], "verify": [], "draft_seq": []}
+    n_steps = min(4, len(r.drops))  # distinct steps (rollback counts) captured
+    n_rep = max(n_rep, 6 * n_steps)
     if external_events_supported(torch):
         recs, graphs = [], []
-        for s in range(len(r.drops)):
-            rec = []
-            graphs.append(capture(torch, lambda s=s, rec=rec: r.step(s, ev=rec, external=True)))
-            recs.append(rec)
+        for seq in (False, True):
+            for s in range(n_steps):
+                rec = []
+                graphs.append(capture(torch, lambda s=s, rec=rec, seq=seq:
+                                      r.step(s, ev=rec, external=True, seq=seq)))
+                recs.append(rec)
         for i in range(n_rep):
             k = i % len(graphs)
             graphs[k].replay()
             torch.cuda.synchronize()
-            if i >= 2:
+            if i >= len(graphs):
                 for kind, e0, e1 in recs[k]:
-                    launch[kind].append(e0.elapsed_time(e1) * 1e3)
-        how = ("CUDA events captured as graph nodes around each attention call, %d graph-replayed "
-               "steps after the timed region" % (n_rep - 2))
+                    t = e0.elapsed_time(e1) * 1e3
+                    launch[kind].append(t / GAMMA if kind == "draft_seq" else t)
+        how = ("CUDA events captured as graph nodes, %d graph-replayed steps after the timed region"
+               % (n_rep - len(graphs)))
     else:
         recs = []
         for s in range(n_rep):
             rec = []
-            r.step(s, ev=rec)
+            r.step(s, ev=rec, seq=bool(s & 1))
             recs.append(rec)
         torch.cuda.synchronize()
         for rec in recs[2:]:
             for kind, e0, e1 in rec:
-                launch[kind].append(e0.elapsed_time(e1) * 1e3)
-        how = "CUDA events around each attention call in %d eager steps" % (n_rep - 2)
+                t = e0.elapsed_time(e1) * 1e3
+                launch[kind].append(t / GAMMA if kind == "draft_seq" else t)
+        how = "CUDA events in %d eager steps" % (n_rep - 2)
     r.cache.state.copy_(r.state0)
     return launch, how
 
@@ -641,7 +662,8 @@ def config_round(torch, qs, synthetic, name, peak, n_rep=40, n_replay=100):
     round_us = replay_us(torch, graphs, n_replay)
     errs = qs.qs_get_errors(r.cache)
     assert np.all(errs == 0), errs
-    d_us, v_us = float(np.mean(launch["draft"])), float(np.mean(launch["verify"]))
+    d_us, v_us = float(np.mean(launch["draft_seq"])), float(np.mean(launch["verify"]))
+    d_call_us = float(np.mean(launch["draft"]))
     d_b = float(np.mean(r.bytes["draft"]))
     v_b = r.bytes["verify"]
     ctx = np.array(w.context)
@@ -653,11 +675,14 @@ def config_round(torch, qs, synthetic, name, peak, n_rep=40, n_replay=100):
         {"min": int(min(w.fill)), "max": int(max(w.fill))},
         "flushing_sequences": int(r.plan["mask"].sum()),
         "draft_us": round(d_us, 2), "draft_bytes": int(d_b), "draft_gbs": round(d_b / d_us / 1e3, 1),
+        "draft_us_events_per_call": round(d_call_us, 2),
         "verify_us": round(v_us, 2), "verify_bytes": int(v_b),
         "verify_gbs": round(v_b / v_us / 1e3, 1),
         "round_us": round(round_us, 2), "round_bytes": int(r.step_bytes),
         "round_gbs": round(r.step_bytes / round_us / 1e3, 1),
-        "launch_timing": how, "setup_s": round(setup_s, 1)}
+        "launch_timing": how + "; draft: events around the run of %d draft calls, per call; "
+                               "verify: events around the call" % GAMMA,
+        "setup_s": round(setup_s, 1)}
     if d_b > 2 * 129e6:  # working set larger than L2: an HBM roofline figure
         out["draft_frac"] = round(d_b / d_us / 1e3 / peak, 4)
         out["verify_frac"] = round(v_b / v_us / 1e3 / peak, 4)
@@ -831,7 +856,8 @@ def native(args):
     draft_gbs, verify_gbs = draft_b / draft_us / 1e3, verify_b / verify_us / 1e3
     # The roofline's launch durations: the attention calls inside the step
     launch, launch_how = in_step_launch_times(torch, r, max(12, min(args.steps, 60)))
-    draft_launch_us = float(np.mean(launch["draft"]))
+    draft_launch_us = float(np.mean(launch["draft_seq"]))
+    draft_call_us = float(np.mean(launch["draft"]))
     verify_launch_us = float(np.mean(launch["verify"]))
     draft_marg_us = verify_marg_us = None
     if r.fused:
@@ -902,6 +928,7 @@ def native(args):
                          "L2 evicted before each call by a 256 MB read" % (step_bytes / 1e6),
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "draft_in_step_us": round(draft_launch_us, 2), "verify_in_step_us": round(verify_launch_us, 2),
+        "draft_in_step_events_per_call_us": round(draft_call_us, 2),
         "draft_marginal_us": None if draft_marg_us is None else round(draft_marg_us, 2),
         "verify_marginal_us": None if verify_marg_us is None else round(verify_marg_us, 2),
         "draft_us": round(draft_us, 2), "draft_gbs": round(draft_gbs, 1),
@@ -914,7 +941,12 @@ def native(args):
         "two_bit_draft": two_bit,
         "roofline": {"bound": "hbm", "kernel": "qs_attn_decode %s (split_kernel: split-KV attention + LSE merge, one launch)" % dominant[0],
                      "launch_us": round(dominant[2], 2),
-                     "launch_timing": launch_how + " (mean of %d calls)" % len(launch[dominant[0]]),
+                     "launch_timing": launch_how + (
+                         "; events around the step's run of %d consecutive draft launches, per "
+                         "launch (mean of %d runs); events around each single call instead: %.2f us"
+                         % (GAMMA, len(launch["draft_seq"]), draft_call_us)
+                         if dominant[0] == "draft" else
+                         " (mean of %d calls)" % len(launch["verify"])),
                      "achieved": round(dominant[1], 1), "peak": peak,
                      "peak_kind": "%s hbm_gbs (copy, burst)" % peak_kind, "unit": "GB/s",
                      "frac": round(dominant[1] / peak, 4), "traffic": stored_traffic(dominant[0]),
