@@ -184,7 +184,10 @@ __device__ long long build_tables(const qs_cache &c, int n_q, int n_new, Tables 
 // p >= U idle).  Either way every CTA between a segment's first and last
 // owner owns part of it.
 __device__ __forceinline__ long long range_lo(int p, long long U, int P) {
-  return U >= P ? (long long)p * U / P : (p < U ? p : U);
+  if (U < P) return p < U ? p : U;
+  if (U * P < (1ll << 32))  // 32-bit division (p <= P)
+    return (long long)((uint32_t)p * (uint32_t)U / (uint32_t)P);
+  return (long long)p * U / P;
 }
 // The CTA whose range holds unit x.
 __device__ __forceinline__ int cta_of(long long x, long long U, int P) {
@@ -509,6 +512,16 @@ __device__ __forceinline__ void fence_gpu() {
 #endif
 }
 
+// Arrival on a segment counter: a device-scope atomic add with acquire and
+// release semantics (the CTA's partial, ordered before it by a barrier, is
+// published; the partials of the CTAs that arrived before are visible after
+// it, to the whole CTA after a barrier).
+__device__ __forceinline__ int atom_add_acq_rel_gpu(int *p, int v) {
+  int old;
+  asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -830,6 +843,7 @@ __global__ void __launch_bounds__(NW * 32, 1) split_kernel(const Params prm) {
   Tables T = tables_at(smem, L::kTabOff);
   __shared__ long long s_total;
   __shared__ int s_abort, s_left_first, s_first_fin, s_seg[2], s_ord[2], s_need[2], s_last[2];
+  __shared__ int s_plo[2], s_raw[2];
   __shared__ int s_next[3];  // claim counter per column group
 
   if (threadIdx.x == 0) {
@@ -1443,6 +1457,10 @@ __global__ void __launch_bounds__(NW * 32, 1) split_kernel(const Params prm) {
           s_seg[n_arr] = (int)seg;
           s_ord[n_arr] = pc.ord;
           s_need[n_arr] = phi - plo + 1;
+          s_plo[n_arr] = plo;
+          // CTA p_hi left its NW warp partials if the segment was only the
+          // first piece of its range
+          s_raw[n_arr] = S0 < range_lo(phi, U, prm.P) && E0 < range_lo(phi + 1, U, prm.P);
         }
         ++n_arr;
       }
@@ -1453,28 +1471,22 @@ __global__ void __launch_bounds__(NW * 32, 1) split_kernel(const Params prm) {
   __syncthreads();  // this CTA's partials are written (made visible by the fence below)
   if (threadIdx.x < n_arr) {
     int *ctr = c.arrive + s_seg[threadIdx.x];
-    fence_gpu();
-    const int last = atomicAdd(ctr, 1) == s_need[threadIdx.x] - 1;
-    if (last) {
-      atomicExch(ctr, 0);  // every other arrival is in: ready for the next call
-      fence_gpu();     // the other CTAs' partials are visible from here on
-    }
+    const int last = atom_add_acq_rel_gpu(ctr, 1) == s_need[threadIdx.x] - 1;
+    if (last) atomicExch(ctr, 0);  // every other arrival is in: ready for the next call
     s_last[threadIdx.x] = last;
   }
   __syncthreads();
   int n_mrg = 0;  // phases of the merge barrier used
   for (int a = 0; a < n_arr; ++a) {
     if (!s_last[a] || aborted) continue;
-    const long long seg = s_seg[a];
-    const int b = (int)(seg / c.H), len = T.len[b];
-    const int S0 = T.base[b] + (int)(seg % c.H) * len, E0 = S0 + len;
-    const int plo = cta_of(S0, U, prm.P), phi = cta_of(E0 - 1, U, prm.P);
+    const int seg = s_seg[a], b = seg / c.H;
+    const int plo = s_plo[a], phi = plo + s_need[a] - 1;
     const MergeOut mo{true, prm.out + (size_t)seg * R * kD,
                       prm.lse ? prm.lse + (size_t)seg * R : nullptr, nullptr};
     // CTA pp's partial of this segment is in its warp slot 0, except that
     // CTA p_hi left its NW warp partials when the segment was only the
     // first piece of its range
-    const bool raw = S0 < range_lo(phi, U, prm.P) && E0 < range_lo(phi + 1, U, prm.P);
+    const bool raw = s_raw[a];
     const float *cta0 = prm.ws + ((size_t)(s_ord[a] + plo) * NW) * stride;
     const float *raw0 = prm.ws + ((size_t)(s_ord[a] + phi) * NW) * stride;
     const int nA = raw ? phi - plo : phi - plo + 1;
