@@ -521,6 +521,12 @@ __device__ __forceinline__ int atom_add_acq_rel_gpu(int *p, int v) {
   asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
   return old;
 }
+// The same at CTA scope (a count of the CTA's warps in shared memory).
+__device__ __forceinline__ int atom_add_acq_rel_cta(int *p, int v) {
+  int old;
+  asm volatile("atom.add.acq_rel.cta.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -945,23 +951,22 @@ __global__ void __launch_bounds__(NW * 32, 1) split_kernel(const Params prm) {
   const bool shared_first = ord_first != ord_last && first.s0 < x0;
   auto leave = [&](int o) {
     if (!shared_first || o != ord_first) return;
-    // This warp's partial is ordered before its count at CTA scope; the last
-    // warp's device-scope fence below is cumulative, so it publishes the
-    // partials of every warp whose count it has seen before the arrival.
+    // The lanes' partial stores are ordered before lane 0's count
+    // (__syncwarp); the count is an acquire-release atomic at CTA scope, so
+    // the warp that counts last has acquired every other warp's partial, and
+    // its device-scope acquire-release arrival (cumulative) publishes them all.
     __syncwarp();
-    __threadfence_block();
-    int last = 0;
-    if (lane == 0) last = atomicAdd(&s_left_first, 1) == NW - 1;
-    if (!__shfl_sync(0xffffffffu, last, 0)) return;
-    fence_gpu();
-    const long long seg = (long long)first.b * c.H + first.h;
-    const int plo = cta_of(first.s0, U, prm.P);  // the segment ends in this range: p_hi = p
-    if (lane == 0 && atomicAdd(&c.arrive[seg], 1) == p - plo) {
-      // rare: the CTAs before have all arrived; this CTA finishes the segment
-      // at its end
-      atomicExch(&c.arrive[seg], 0);  // every other arrival is in
-      s_first_fin = 1;
+    if (lane == 0 && atom_add_acq_rel_cta(&s_left_first, 1) == NW - 1) {
+      const int seg = first.b * c.H + first.h;
+      const int plo = cta_of(first.s0, U, prm.P);  // the segment ends in this range: p_hi = p
+      if (atom_add_acq_rel_gpu(&c.arrive[seg], 1) == p - plo) {
+        // rare: the CTAs before have all arrived; this CTA finishes the
+        // segment at its end
+        atomicExch(&c.arrive[seg], 0);  // every other arrival is in
+        s_first_fin = 1;
+      }
     }
+    __syncwarp();
   };
 
   // the warps reach the range's last segment mid-range: start its queries
