@@ -498,19 +498,10 @@ __device__ __forceinline__ void issue_unit(const Params &prm, const Tables &T, c
 #define QS_MERGE_KS 8
 #endif
 
-// Device-scope fence between a CTA's partials and its arrival on a segment
-// counter (release), and between the arrival that completes a segment and
-// the reads of the other CTAs' partials (acquire).
-#ifndef QS_FENCE_AR
-#define QS_FENCE_AR 0
-#endif
-__device__ __forceinline__ void fence_gpu() {
-#if QS_FENCE_AR
-  asm volatile("fence.acq_rel.gpu;" ::: "memory");
-#else
-  __threadfence();
-#endif
-}
+// Device-scope fence: in the rare case where a CTA finishes the segment of
+// its shared first piece, between the arrival (made mid-range by one lane)
+// and the whole CTA's reads of the other CTAs' partials.
+__device__ __forceinline__ void fence_gpu() { __threadfence(); }
 
 // Arrival on a segment counter: a device-scope atomic add with acquire and
 // release semantics (the CTA's partial, ordered before it by a barrier, is
