@@ -56,19 +56,45 @@ __device__ __forceinline__ void scale_zero(float mn, float mx, uint16_t &s_bits,
 // to 2^-24, so u' = fl((x - z) * rf) is within 2^-14 of fl((x - z) / s) for
 // every |u| < 256 (u <= 255 (1 + 2^-23) since s >= r / 255).  Both round to
 // the same integer unless u' lies within 2^-12 of a half-integer; there the
-// exact quotient decides (about one element in 2^11).
-// Called by whole warps (the vote): the exact quotient is computed only
-// when some lane of the warp is that close to a tie, and rounding, clamping
-// to [0, 255] and conversion are one saturating conversion.  A zero scale
-// gives code 0 (then rf is +inf and a is 0 or positive: the code is forced).
-__device__ __forceinline__ uint32_t code_of(float x, float zf, float sf, float rf) {
-  const float a = __fsub_rn(x, zf);
-  float ue = __fmul_rn(a, rf);
-  const bool near = fabsf(__fsub_rn(ue, rintf(ue))) > 0.5f - 0x1p-12f;
-  if (__any_sync(0xffffffffu, near) && near) ue = __fdiv_rn(a, sf);
-  uint32_t q;
-  asm("cvt.rni.sat.u8.f32 %0, %1;" : "=r"(q) : "f"(ue));
-  return sf == 0.0f ? 0u : q;
+// exact quotient decides (about one element in 2^11).  Four elements at a
+// time, with one warp vote: the exact quotient is computed only when some
+// lane of the warp has an element that close to a tie, and then only for
+// those elements.  Rounding, clamping to [0, 255] and conversion are one
+// saturating conversion.  A zero scale gives code 0 (then rf is +inf and a
+// is 0 or positive: the code is forced).  Called by whole warps.
+__device__ __forceinline__ void codes4(const float (&x)[4], const float (&zf)[4],
+                                       const float (&sf)[4], const float (&rf)[4],
+                                       uint32_t (&q)[4]) {
+  float a[4], ue[4];
+  bool near[4], any = false;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    a[i] = __fsub_rn(x[i], zf[i]);
+    ue[i] = __fmul_rn(a[i], rf[i]);
+    near[i] = fabsf(__fsub_rn(ue[i], rintf(ue[i]))) > 0.5f - 0x1p-12f;
+    any |= near[i];
+  }
+  if (__any_sync(0xffffffffu, any)) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      if (near[i]) ue[i] = __fdiv_rn(a[i], sf[i]);
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint32_t v;
+    asm("cvt.rni.sat.u8.f32 %0, %1;" : "=r"(v) : "f"(ue[i]));
+    q[i] = sf[i] == 0.0f ? 0u : v;
+  }
+}
+
+// Two 4-bit planes' bytes from four 8-bit codes per word: words a and b hold
+// codes 4k..4k+3 and 4k+4..4k+7 (channel pairs 2k, 2k+1, 2k+2, 2k+3); the
+// result's byte i holds pair i's two nibbles (the first code's in the low
+// nibble): upper nibbles (hi) or lower nibbles (lo) of the codes.
+__device__ __forceinline__ uint32_t pair_nibbles(uint32_t a, uint32_t b, bool hi) {
+  const uint32_t na = (hi ? a >> 4 : a) & 0x0F0F0F0Fu, nb = (hi ? b >> 4 : b) & 0x0F0F0F0Fu;
+  // byte 0 of (n | n >> 4): nibble of byte 0, then of byte 1; byte 2: of bytes 2, 3
+  return prmt(na | (na >> 4), nb | (nb >> 4), 0x6420);
 }
 
 // Token held by nibble position p of a 16-byte value row (quarter layout).
@@ -159,9 +185,9 @@ __device__ void quantize_part(FlushSmem<QW> &S, const __half *gk, const __half *
       S.vz[t] = zb;
     }
     const float rf = __frcp_rn(sf);
-    const uint32_t q0 = code_of(a.x, zf, sf, rf), q1 = code_of(a.y, zf, sf, rf);
-    const uint32_t q2 = code_of(bb.x, zf, sf, rf), q3 = code_of(bb.y, zf, sf, rf);
-    *reinterpret_cast<uint32_t *>(&S.vc[t][4 * lane]) = q0 | (q1 << 8) | (q2 << 16) | (q3 << 24);
+    uint32_t q[4];
+    codes4({a.x, a.y, bb.x, bb.y}, {zf, zf, zf, zf}, {sf, sf, sf, sf}, {rf, rf, rf, rf}, q);
+    *reinterpret_cast<uint32_t *>(&S.vc[t][4 * lane]) = q[0] | (q[1] << 8) | (q[2] << 16) | (q[3] << 24);
   }
   __syncthreads();
   if (tid < kSlice) {
@@ -187,22 +213,31 @@ __device__ void quantize_part(FlushSmem<QW> &S, const __half *gk, const __half *
     const float z0 = __half2float(__ushort_as_half(S.kz[2 * j]));
     const float z1 = __half2float(__ushort_as_half(S.kz[2 * j + 1]));
     const float r0 = __frcp_rn(s0), r1 = __frcp_rn(s1);
-    for (int t = t0; t < t0 + kTc; ++t) {
+    static_assert(kTc % 2 == 0, "two tokens per step");
+#pragma unroll
+    for (int t = t0; t < t0 + kTc; t += 2) {
       const float2 x = __half22float2(*reinterpret_cast<const __half2 *>(&S.k[t][2 * j]));
-      const uint32_t q0 = code_of(x.x, z0, s0, r0), q1 = code_of(x.y, z1, s1, r1);
-      *reinterpret_cast<uint16_t *>(&S.kc[t][2 * j]) = (uint16_t)(q0 | (q1 << 8));
+      const float2 y = __half22float2(*reinterpret_cast<const __half2 *>(&S.k[t + 1][2 * j]));
+      uint32_t q[4];
+      codes4({x.x, x.y, y.x, y.y}, {z0, z1, z0, z1}, {s0, s1, s0, s1}, {r0, r1, r0, r1}, q);
+      *reinterpret_cast<uint16_t *>(&S.kc[t][2 * j]) = (uint16_t)(q[0] | (q[1] << 8));
+      *reinterpret_cast<uint16_t *>(&S.kc[t + 1][2 * j]) = (uint16_t)(q[2] | (q[3] << 8));
     }
   }
   __syncthreads();
 
   if (tid < kG) {
     // 5. key planes: bytes [16p, 16p+16) of token row tid (channels 2i, 2i+1)
-    uint32_t wu[4] = {0, 0, 0, 0}, wl[4] = {0, 0, 0, 0};
+    // the row's 32 codes in two 16-byte loads; word m of a plane row holds
+    // channel pairs 4m..4m+3 (codes 8m..8m+7)
+    const uint4 ra = *reinterpret_cast<const uint4 *>(&S.kc[tid][0]);
+    const uint4 rb = *reinterpret_cast<const uint4 *>(&S.kc[tid][16]);
+    const uint32_t cw[8] = {ra.x, ra.y, ra.z, ra.w, rb.x, rb.y, rb.z, rb.w};
+    uint32_t wu[4], wl[4];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const uint32_t c0 = S.kc[tid][2 * i], c1 = S.kc[tid][2 * i + 1];
-      wu[i >> 2] |= ((c0 >> 4) | (c1 & 0xF0u)) << (8 * (i & 3));
-      wl[i >> 2] |= ((c0 & 15u) | ((c1 & 15u) << 4)) << (8 * (i & 3));
+    for (int m = 0; m < 4; ++m) {
+      wu[m] = pair_nibbles(cw[2 * m], cw[2 * m + 1], true);
+      wl[m] = pair_nibbles(cw[2 * m], cw[2 * m + 1], false);
     }
     if (c.upper_bits == 2)
       store_upper2(c.k_upper + grp * kG * (kD / 2), 16 * (4 * tid + part), wu);
