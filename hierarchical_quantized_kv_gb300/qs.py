@@ -101,10 +101,30 @@ def _check(fn, status):
         raise QsError(fn, status)
 
 
+_current_raw_stream = None
+
+
+def _current_stream_handle():
+    """cudaStream_t of torch's current stream on the current device.  Through
+    torch._C._cuda_getCurrentRawStream (the lookup torch's own generated code
+    makes: about 0.3 us a call, against 3 us for torch.cuda.current_stream()
+    on the Grace host) where this torch has it, else the public call."""
+    global _current_raw_stream
+    if _current_raw_stream is None:
+        import torch
+        raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+        dev = getattr(torch._C, "_cuda_getDevice", None)
+        if raw is not None and dev is not None:
+            torch.cuda.init()
+            _current_raw_stream = lambda: raw(dev())
+        else:
+            _current_raw_stream = lambda: torch.cuda.current_stream().cuda_stream
+    return _current_raw_stream()
+
+
 def _stream(stream):
     if stream is None:
-        import torch
-        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+        return ctypes.c_void_p(_current_stream_handle())
     if isinstance(stream, int):
         return ctypes.c_void_p(stream)
     return ctypes.c_void_p(stream.cuda_stream)
