@@ -503,16 +503,8 @@ __device__ __forceinline__ void issue_unit(const Params &prm, const Tables &T, c
 // and the whole CTA's reads of the other CTAs' partials.
 __device__ __forceinline__ void fence_gpu() { __threadfence(); }
 
-// Arrival on a segment counter: a device-scope atomic add with acquire and
-// release semantics (the CTA's partial, ordered before it by a barrier, is
-// published; the partials of the CTAs that arrived before are visible after
-// it, to the whole CTA after a barrier).
-__device__ __forceinline__ int atom_add_acq_rel_gpu(int *p, int v) {
-  int old;
-  asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-  return old;
-}
-// The same at CTA scope (a count of the CTA's warps in shared memory).
+// Atomic add with acquire and release semantics at CTA scope (a count of
+// the CTA's warps in shared memory).
 __device__ __forceinline__ int atom_add_acq_rel_cta(int *p, int v) {
   int old;
   asm volatile("atom.add.acq_rel.cta.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
@@ -875,7 +867,7 @@ __global__ void __launch_bounds__(NW * 32, 1) split_kernel(const Params prm) {
     // appended counters (no CTA of this launch reads them again).  The new
     // tokens enter the ring slots past the old fill, which no CTA of this
     // launch reads (its copies of those rows come from k_new / v_new).
-    if (lane == 0 && atomicAdd(&c.state[QS_ST_TICKET], 1) == (int)gridDim.x - 1) {
+    if (lane == 0 && atom_add_acq_rel_gpu(&c.state[QS_ST_TICKET], 1) == (int)gridDim.x - 1) {
       for (int b = 0; b < c.B; ++b) {
         int32_t *st = c.state + (size_t)b * QS_STATE_WORDS;
         if (T.fill[b] != T.fold[b]) {

@@ -46,15 +46,11 @@ __global__ void __launch_bounds__(256) append_kernel(qs_cache c, const uint4 *__
     bv[slot * kRowVec + col] = sv[e];
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    const int ticket = atomicAdd(&st[QS_ST_TICKET], 1);
-    if (ticket == c.H - 1) {  // every head has read the old counters
-      st[QS_ST_FILL] = fill + n_new;
-      st[QS_ST_PENDING] += n_new;
-      st[QS_ST_TICKET] = 0;
-      __threadfence();
-    }
+  // every head has read the old counters once the ticket reaches H - 1
+  if (threadIdx.x == 0 && atom_add_acq_rel_gpu(&st[QS_ST_TICKET], 1) == c.H - 1) {
+    st[QS_ST_FILL] = fill + n_new;
+    st[QS_ST_PENDING] += n_new;
+    st[QS_ST_TICKET] = 0;
   }
 }
 

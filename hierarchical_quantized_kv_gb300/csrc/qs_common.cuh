@@ -160,6 +160,17 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
   }
 }
 
+// Device-scope atomic add with acquire and release semantics: an arrival on
+// a counter that publishes what the arriving thread wrote or observed before
+// it (a barrier before it covers the whole CTA's writes), and after which the
+// writes of the threads that arrived earlier are visible (to the whole CTA
+// after a barrier).
+__device__ __forceinline__ int atom_add_acq_rel_gpu(int *p, int v) {
+  int old;
+  asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
 // Bulk async copy global -> shared (TMA engine, no tensor map), completion
 // counted in bytes on an mbarrier.  Addresses 16-byte aligned, size % 16 == 0.
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes,

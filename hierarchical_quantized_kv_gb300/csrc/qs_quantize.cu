@@ -312,16 +312,13 @@ __global__ void __launch_bounds__(32 * kFlushWarps)
 
   quantize_part(S, gk, gv, c, bh * c.cap_groups + g, part, tid);
   __syncthreads();
-  if (tid == 0) {
-    __threadfence();
-    const int ticket = atomicAdd(&st[QS_ST_TICKET], 1);
-    if (ticket == kParts * c.H - 1) {  // every CTA of the sequence has read the old counters
-      st[QS_ST_N_GROUPS] = g + 1;
-      st[QS_ST_HALF_BASE] = base ^ 1;
-      st[QS_ST_FILL] -= kG;
-      st[QS_ST_TICKET] = 0;
-      __threadfence();
-    }
+  // every CTA of the sequence has read the old counters once the ticket
+  // reaches kParts H - 1 (the planes are published by the kernel's end)
+  if (tid == 0 && atom_add_acq_rel_gpu(&st[QS_ST_TICKET], 1) == kParts * c.H - 1) {
+    st[QS_ST_N_GROUPS] = g + 1;
+    st[QS_ST_HALF_BASE] = base ^ 1;
+    st[QS_ST_FILL] -= kG;
+    st[QS_ST_TICKET] = 0;
   }
 }
 
@@ -384,17 +381,12 @@ __global__ void __launch_bounds__(32 * kPrefillWarps) prefill_kernel(qs_cache c,
       }
   }
   __syncthreads();
-  if (tid == 0) {
-    __threadfence();
-    const int ticket = atomicAdd(&st[QS_ST_TICKET], 1);
-    if (ticket == (int)gridDim.x * c.H - 1) {
-      st[QS_ST_N_GROUPS] = ng;
-      st[QS_ST_FILL] = fill;
-      st[QS_ST_PENDING] = 0;
-      st[QS_ST_HALF_BASE] = 0;
-      st[QS_ST_TICKET] = 0;
-      __threadfence();
-    }
+  if (tid == 0 && atom_add_acq_rel_gpu(&st[QS_ST_TICKET], 1) == (int)gridDim.x * c.H - 1) {
+    st[QS_ST_N_GROUPS] = ng;
+    st[QS_ST_FILL] = fill;
+    st[QS_ST_PENDING] = 0;
+    st[QS_ST_HALF_BASE] = 0;
+    st[QS_ST_TICKET] = 0;
   }
 }
 
