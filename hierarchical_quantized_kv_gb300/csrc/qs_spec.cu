@@ -99,16 +99,29 @@ __global__ void __cluster_dims__(kSpecCluster, 1, 1) __launch_bounds__(kSpecThre
   pdl_wait();
   const float *pb = p + (size_t)b * (gamma + 1) * V;
   const float *qb = q + (size_t)b * gamma * V;
-  if (tid == 0) {
-    int a = 0;
-    while (a < gamma) {
-      const int x = draft[(size_t)b * gamma + a];
-      if (x < 0 || x >= V) break;  // not a token: rejected
-      const float pa = pb[(size_t)a * V + x], qa = qb[(size_t)a * V + x];
-      if (!(__fmul_rn(u[(size_t)b * gamma + a], qa) < pa)) break;
-      ++a;
+  if (tid < 32) {
+    // The accepted count: draft token i is tested by lane i % 32 (its token,
+    // p, q and u loaded by all lanes at once, not one after another); the
+    // first rejection, the lowest set bit of the vote, ends the run.
+    int a = gamma;
+    for (int base = 0; base < gamma; base += 32) {
+      const int i = base + tid;
+      bool reject = false;
+      if (i < gamma) {
+        const int x = draft[(size_t)b * gamma + i];
+        reject = x < 0 || x >= V;  // not a token: rejected
+        if (!reject) {
+          const float pa = pb[(size_t)i * V + x], qa = qb[(size_t)i * V + x];
+          reject = !(__fmul_rn(u[(size_t)b * gamma + i], qa) < pa);
+        }
+      }
+      const unsigned rej = __ballot_sync(0xffffffffu, reject);
+      if (rej) {
+        a = base + __ffs(rej) - 1;
+        break;
+      }
     }
-    s_a = a;
+    if (tid == 0) s_a = a;
   }
   __syncthreads();
   const int a = s_a;
