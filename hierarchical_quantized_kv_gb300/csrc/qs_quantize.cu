@@ -25,6 +25,11 @@ constexpr int kSlice = kD / kParts;  // key channels / value tokens per CTA
 // every phase but the packing (flush 14 -> 11.5 µs); a prefill is many
 // waves, where eight warps keep more CTAs resident (379 against 426 µs).
 constexpr int kFlushWarps = 16, kPrefillWarps = 8;
+// Group quarters per quantizing CTA of a prefill, loads pipelined one ahead.
+#ifndef QS_PREFILL_QUARTERS
+#define QS_PREFILL_QUARTERS 8
+#endif
+constexpr int kPrefillQuarters = QS_PREFILL_QUARTERS;
 
 // One CTA owns key channels [32p, 32p+32) (one 16-byte column of every key
 // row) and value tokens [32p, 32p+32) (value quarter p).
@@ -132,35 +137,62 @@ __device__ __forceinline__ void store_upper2(uint8_t *base, size_t off, const ui
   *reinterpret_cast<uint2 *>(base + (size_t)kG * kD / 4 + off / 2) = m;
 }
 
-// One CTA's share of quantizing a group of G tokens whose fp16 key and value
-// rows (D channels each, row stride D) start at gk and gv: key channels
-// [32 part, 32 part + 32) and value tokens [32 part, 32 part + 32), written
-// as group `grp` (index into the [B][H][cap] group arrays).  32 QW threads.
-template <int QW>
-__device__ void quantize_part(FlushSmem<QW> &S, const __half *gk, const __half *gv,
-                              const qs_cache &c, size_t grp, int part, int tid) {
-  constexpr int kQWarps = QW, kQThreads = 32 * QW;
-  const int warp = tid >> 5, lane = tid & 31;
-  // checked build: a group index out of the arrays writes nothing (the same
-  // for every thread of the CTA)
-  if (!chk(in_range(grp, 1, (size_t)c.B * c.H * c.cap_groups), 20)) return;
-  // 1. loads: the key column slice (64 B of each of 128 rows), 32 value rows
+// Asynchronous 16-byte copy global -> shared through the load/store path
+// (cached in L2 only; addresses 16-byte aligned), its commit group, and the
+// wait until at most N of the thread's groups are still in flight.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// A CTA's share of a group is a quarter: key channels [32 part, 32 part +
+// 32) and value tokens [32 part, 32 part + 32).
+// 1. loads of a group quarter into kt / vt: the key column slice (64 B of
+// each of 128 rows) and 32 value rows; ASYNC: as cp.async copies, one commit
+// group (the caller waits for it before quantize_loaded).
+template <int QW, bool ASYNC>
+__device__ __forceinline__ void load_part(__half (*kt)[kSlice], __half (*vt)[kD], const __half *gk,
+                                          const __half *gv, int part, int tid) {
+  constexpr int kQThreads = 32 * QW;
   for (int e = tid; e < kG * 4; e += kQThreads) {  // 4 x 16 B per key row
     const int t = e >> 2, q = e & 3;
-    reinterpret_cast<uint4 *>(&S.k[t][0])[q] =
-        reinterpret_cast<const uint4 *>(gk + (size_t)t * kD + part * kSlice)[q];
+    const uint4 *src = reinterpret_cast<const uint4 *>(gk + (size_t)t * kD + part * kSlice) + q;
+    if (ASYNC)
+      cp_async16(smem_addr(&kt[t][0]) + 16 * q, src);
+    else
+      reinterpret_cast<uint4 *>(&kt[t][0])[q] = *src;
   }
-  for (int e = tid; e < kSlice * kD / 8; e += kQThreads)
-    reinterpret_cast<uint4 *>(&S.v[0][0])[e] =
-        reinterpret_cast<const uint4 *>(gv + (size_t)part * kSlice * kD)[e];
-  __syncthreads();
+  for (int e = tid; e < kSlice * kD / 8; e += kQThreads) {
+    const uint4 *src = reinterpret_cast<const uint4 *>(gv + (size_t)part * kSlice * kD) + e;
+    if (ASYNC)
+      cp_async16(smem_addr(&vt[0][0]) + 16 * e, src);
+    else
+      reinterpret_cast<uint4 *>(&vt[0][0])[e] = *src;
+  }
+  if (ASYNC) cp_async_commit();
+}
+
+// Phases 2-7 of a group quarter whose rows are in kt / vt (all loads landed
+// and visible to the CTA).
+template <int QW>
+__device__ void quantize_loaded(FlushSmem<QW> &S, const __half (*kt)[kSlice],
+                                const __half (*vt)[kD], const qs_cache &c, size_t grp, int part,
+                                int tid) {
+  constexpr int kQWarps = QW, kQThreads = 32 * QW;
+  const int warp = tid >> 5, lane = tid & 31;
 
   // 2. keys: min / max per channel, warp w over tokens kG/kQWarps w onwards
   {
     constexpr int kTw = kG / kQWarps;
     float mn = INFINITY, mx = -INFINITY;
     for (int t = kTw * warp; t < kTw * warp + kTw; ++t) {
-      const float x = __half2float(S.k[t][lane]);
+      const float x = __half2float(kt[t][lane]);
       mn = fminf(mn, x);
       mx = fmaxf(mx, x);
     }
@@ -169,7 +201,7 @@ __device__ void quantize_part(FlushSmem<QW> &S, const __half *gk, const __half *
   }
   // 3. values: one warp per token, min / max over the 128 channels, codes
   for (int t = warp; t < kSlice; t += kQWarps) {
-    const __half2 *row = reinterpret_cast<const __half2 *>(&S.v[t][4 * lane]);
+    const __half2 *row = reinterpret_cast<const __half2 *>(&vt[t][4 * lane]);
     const float2 a = __half22float2(row[0]), bb = __half22float2(row[1]);
     float mn = fminf(fminf(a.x, a.y), fminf(bb.x, bb.y));
     float mx = fmaxf(fmaxf(a.x, a.y), fmaxf(bb.x, bb.y));
@@ -216,8 +248,8 @@ __device__ void quantize_part(FlushSmem<QW> &S, const __half *gk, const __half *
     static_assert(kTc % 2 == 0, "two tokens per step");
 #pragma unroll
     for (int t = t0; t < t0 + kTc; t += 2) {
-      const float2 x = __half22float2(*reinterpret_cast<const __half2 *>(&S.k[t][2 * j]));
-      const float2 y = __half22float2(*reinterpret_cast<const __half2 *>(&S.k[t + 1][2 * j]));
+      const float2 x = __half22float2(*reinterpret_cast<const __half2 *>(&kt[t][2 * j]));
+      const float2 y = __half22float2(*reinterpret_cast<const __half2 *>(&kt[t + 1][2 * j]));
       uint32_t q[4];
       codes4({x.x, x.y, y.x, y.y}, {z0, z1, z0, z1}, {s0, s1, s0, s1}, {r0, r1, r0, r1}, q);
       *reinterpret_cast<uint16_t *>(&S.kc[t][2 * j]) = (uint16_t)(q[0] | (q[1] << 8));
@@ -275,6 +307,30 @@ __device__ void quantize_part(FlushSmem<QW> &S, const __half *gk, const __half *
   }
 }
 
+// One CTA's share of quantizing a group of G tokens whose fp16 key and value
+// rows (D channels each, row stride D) start at gk and gv: key channels
+// [32 part, 32 part + 32) and value tokens [32 part, 32 part + 32), written
+// as group `grp` (index into the [B][H][cap] group arrays).  32 QW threads.
+template <int QW>
+__device__ void quantize_part(FlushSmem<QW> &S, const __half *gk, const __half *gv,
+                              const qs_cache &c, size_t grp, int part, int tid) {
+  // checked build: a group index out of the arrays writes nothing (the same
+  // for every thread of the CTA)
+  if (!chk(in_range(grp, 1, (size_t)c.B * c.H * c.cap_groups), 20)) return;
+  load_part<QW, false>(S.k, S.v, gk, gv, part, tid);
+  __syncthreads();
+  quantize_loaded(S, S.k, S.v, c, grp, part, tid);
+}
+
+// The prefill's shared memory: a second pair of row buffers (first, so the
+// asynchronous copies stay 16-byte aligned) and the flush's.
+template <int QW>
+struct PrefillSmem {
+  __half k1[kG][kSlice];
+  __half v1[kSlice][kD];
+  FlushSmem<QW> f;
+};
+
 }  // namespace
 
 // n_next >= 0: flush the sequences whose buffer cannot take n_next more
@@ -323,15 +379,18 @@ __global__ void __launch_bounds__(32 * kFlushWarps)
 }
 
 // Bulk prefill of empty caches from a prompt (k, v: fp16 [B][H][T][D]).
-// Grid (4 gmax + 2, H, B): block x < 4 gmax quantizes part x % 4 of group
-// x / 4 (if the sequence has that group); the last two blocks copy buffer
-// halves 0 and 1.  The CTA that arrives last on the sequence's ticket writes
-// the counters, so every CTA reads the old (empty) ones first.
+// Grid (nq + 2, H, B): block x < nq quantizes group quarters [x Q, x Q + Q)
+// of the sequence's head (quarter i: part i % 4 of group i / 4; Q =
+// kPrefillQuarters), the next quarter's rows copied into the second buffer
+// while the current one is quantized; the last two blocks copy buffer halves
+// 0 and 1.  The CTA that arrives last on the sequence's ticket writes the
+// counters, so every CTA reads the old (empty) ones first.
 __global__ void __launch_bounds__(32 * kPrefillWarps) prefill_kernel(qs_cache c, const uint16_t *__restrict__ k,
                                                      const uint16_t *__restrict__ v, int T,
-                                                     const int32_t *__restrict__ len, int gmax) {
+                                                     const int32_t *__restrict__ len, int nq) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
-  FlushSmem<kPrefillWarps> &S = *reinterpret_cast<FlushSmem<kPrefillWarps> *>(smem_raw);
+  PrefillSmem<kPrefillWarps> &PS = *reinterpret_cast<PrefillSmem<kPrefillWarps> *>(smem_raw);
+  FlushSmem<kPrefillWarps> &S = PS.f;
   const int x = blockIdx.x, h = blockIdx.y, b = blockIdx.z, tid = threadIdx.x;
   pdl_trigger();
   pdl_wait();
@@ -360,16 +419,46 @@ __global__ void __launch_bounds__(32 * kPrefillWarps) prefill_kernel(qs_cache c,
   const int ng = S.g, fill = S.base;
   const size_t bh = (size_t)b * c.H + h;
   const uint16_t *kp = k + bh * T * kD, *vp = v + bh * T * kD;
-  if (x < 4 * gmax) {
-    const int g = x >> 2, part = x & 3;
-    // checked build: the group's prompt rows inside the prompt array
-    if (g < ng && chk(in_range(((size_t)g + 1) * kG, 0, (size_t)T), 22))
-      quantize_part(S, reinterpret_cast<const __half *>(kp) + (size_t)g * kG * kD,
-                    reinterpret_cast<const __half *>(vp) + (size_t)g * kG * kD, c,
-                    bh * c.cap_groups + g, part, tid);
+  if (x < nq) {
+    const int q0 = x * kPrefillQuarters, q1 = min(q0 + kPrefillQuarters, 4 * ng);
+    const __half *kh = reinterpret_cast<const __half *>(kp), *vh = reinterpret_cast<const __half *>(vp);
+    // the rows of quarter i go to buffer i % 2 (one commit group per quarter:
+    // a quarter whose rows fail the checked build's range check commits an
+    // empty one, so the waits below keep counting quarters)
+    auto load = [&](int i) {
+      const int g = i >> 2;
+      if (!chk(in_range(((size_t)g + 1) * kG, 0, (size_t)T), 22))
+        cp_async_commit();
+      else if (i & 1)
+        load_part<kPrefillWarps, true>(PS.k1, PS.v1, kh + (size_t)g * kG * kD,
+                                       vh + (size_t)g * kG * kD, i & 3, tid);
+      else
+        load_part<kPrefillWarps, true>(S.k, S.v, kh + (size_t)g * kG * kD,
+                                       vh + (size_t)g * kG * kD, i & 3, tid);
+    };
+    if (q0 < q1) load(q0);
+    for (int i = q0; i < q1; ++i) {
+      if (i + 1 < q1) {
+        load(i + 1);  // into the buffer quarter i - 1 used (free since the barrier below)
+        cp_async_wait<1>();
+      } else {
+        cp_async_wait<0>();
+      }
+      __syncthreads();  // quarter i's rows, copied by every thread, are visible
+      const int g = i >> 2;
+      // checked build: the group's prompt rows inside the prompt array
+      if (chk(in_range(((size_t)g + 1) * kG, 0, (size_t)T), 22) &&
+          chk(in_range(bh * c.cap_groups + g, 1, (size_t)c.B * c.H * c.cap_groups), 20)) {
+        if (i & 1)
+          quantize_loaded(S, PS.k1, PS.v1, c, bh * c.cap_groups + g, i & 3, tid);
+        else
+          quantize_loaded(S, S.k, S.v, c, bh * c.cap_groups + g, i & 3, tid);
+      }
+      __syncthreads();  // the buffer and the scratch are free for the next quarters
+    }
   } else {
-    // buffer half x - 4 gmax: tokens i in [G half, G half + G) that are < fill
-    const int i0 = (x - 4 * gmax) * kG, i1 = min(i0 + kG, fill);
+    // buffer half x - nq: tokens i in [G half, G half + G) that are < fill
+    const int i0 = (x - nq) * kG, i1 = min(i0 + kG, fill);
     const uint4 *ks = reinterpret_cast<const uint4 *>(kp + (size_t)ng * kG * kD);
     const uint4 *vs = reinterpret_cast<const uint4 *>(vp + (size_t)ng * kG * kD);
     uint4 *kd = reinterpret_cast<uint4 *>(c.buf_k + bh * kRing * kD);
@@ -416,11 +505,12 @@ extern "C" qs_status qs_prefill(const qs_cache *c, const uint16_t *k, const uint
   if (s != QS_OK) return s;
   if (!k || !v || !d_len || T < 0 || T > (1 << 26)) return QS_ERR_ARG;
   if (!aligned16(k) || !aligned16(v)) return QS_ERR_ALIGN;
-  const int smem = (int)sizeof(FlushSmem<kPrefillWarps>);
+  const int smem = (int)sizeof(PrefillSmem<kPrefillWarps>);
   if ((s = set_smem_once((const void *)prefill_kernel, smem, &g_prefill_ready)) != QS_OK) return s;
   const int gmax = T > 2 * kG ? (T - 2 * kG + kG - 1) / kG : 0;
-  return launch_pdl(prefill_kernel, dim3(4 * gmax + 2, c->H, c->B), dim3(32 * kPrefillWarps), smem,
-                    (cudaStream_t)stream, *c, k, v, (int)T, d_len, gmax);
+  const int nq = (4 * gmax + kPrefillQuarters - 1) / kPrefillQuarters;
+  return launch_pdl(prefill_kernel, dim3(nq + 2, c->H, c->B), dim3(32 * kPrefillWarps), smem,
+                    (cudaStream_t)stream, *c, k, v, (int)T, d_len, nq);
 }
 
 extern "C" qs_status qs_quantize_flush(const qs_cache *c, const uint8_t *d_mask,
